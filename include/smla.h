@@ -1,0 +1,183 @@
+/*
+ * smla — indexer-selected sparse latent attention (MLA) for one GB300 (sm_103a).
+ *
+ * C ABI of the library built from indexer_top_sparse_score_gb300/csrc
+ * (libsmla.so). One layer step of long-context sparse attention, per query
+ * token, as described in "Optimisations de GLM-5.3, partie 2 : PCP, DCP et
+ * Hybrid HiSparse sur 16 H200" (spke.com):
+ *
+ *   1. the indexer scores every earlier token (section "Pourquoi pas TP ou
+ *      DP ?"), with the score fixed for this library as
+ *        score(t, s) = sum_h w[t,h] * ReLU(q_I[t,h,:] . k_I[s,:]) * kscale[s];
+ *   2. a causal top-k (k = 2048 on the page) keeps the best keys s <= pos(t),
+ *      ties going to the lower index;
+ *   3. sparse MLA in MQA form: every head attends over the selected rows of one
+ *      shared latent cache; QK over 576 values, PV over the first 512 (footnote
+ *      1), softmax with log-sum-exp output (section "DCP").
+ *
+ * Conventions for every entry point
+ *   - All tensor arguments are DEVICE pointers into the caller's memory unless
+ *     stated otherwise; the library never allocates, frees or synchronises
+ *     (except smla_read_status, which waits on the stream). The caller owns
+ *     every buffer. All work is enqueued on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and returns before it completes.
+ *   - Layouts are dense, row-major, C order. Pointers must be 16-byte aligned.
+ *   - Return values are smla_status codes. Argument checks happen on the host
+ *     before anything is enqueued; on error nothing is enqueued. Errors found
+ *     on the device (a page id outside the pool, a key index outside the
+ *     cache, a bounded wait that gave up) are recorded as bits in a status word
+ *     at the start of the workspace and read back with smla_read_status. The
+ *     kernels never trap: an out-of-range entry is skipped.
+ *   - The workspace is caller-owned device memory of at least the size the
+ *     matching *_workspace_size function returns; its first 256 bytes hold the
+ *     status word. Calls that share a workspace must be stream-ordered.
+ *   - The library keeps no state between calls apart from one-time kernel
+ *     attribute setup and the driver entry point used to encode TMA tensor
+ *     maps.
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, inconsistent shapes */
+  SMLA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head count, dims, topk) */
+  SMLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  SMLA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, no device) */
+  SMLA_ERR_DEVICE_BOUNDS = 5,/* (smla_read_status) an out-of-range page or key was skipped */
+  SMLA_ERR_TIMEOUT = 6       /* (smla_read_status) a bounded device wait gave up */
+} smla_status;
+
+typedef enum smla_dtype {
+  SMLA_BF16 = 0,      /* bfloat16 */
+  SMLA_FP8_E4M3 = 1   /* OCP FP8 E4M3 (e4m3fn), one byte per value */
+} smla_dtype;
+
+/* Paged cache of one layer. Token s of a sequence lives in pool page
+ * page_table[s / page_size] at slot s % page_size.
+ *   kv          [num_pages][page_size][576]  kv_dtype. The latent row: values
+ *               0..511 are the latent (also V), 512..575 the rope part.
+ *   kv_scale    [num_pages][page_size] fp32, FP8 only: value = e4m3 * scale.
+ *   k_idx       [num_pages][page_size][d_idx] idx_dtype: indexer keys.
+ *   k_idx_scale [num_pages][page_size] fp32 positive per-key indexer scale, or
+ *               NULL for 1 (footnote 3's 132-byte key = 128 FP8 + 4-byte scale).
+ * page_size must be 64. d_idx * sizeof(idx_dtype) must be 128 or 256 bytes. */
+typedef struct smla_paged_cache {
+  const void* kv;
+  const float* kv_scale;
+  const void* k_idx;
+  const float* k_idx_scale;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t kv_dtype;   /* smla_dtype */
+  int32_t idx_dtype;  /* smla_dtype */
+  int32_t d_idx;
+} smla_paged_cache;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* smla_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int smla_version(void);
+
+/* ---------------------------------------------------------------------------
+ * smla_indexer_topk — steps 1 and 2 for a batch of sequences.
+ *
+ *   page_tables [n_seqs][max_pages] int32 pool page ids.
+ *   seq_lens    [n_seqs] int32 (device): keys of each sequence INCLUDING its
+ *               q_per_seq new tokens; query j of sequence b sits at position
+ *               seq_lens[b] - q_per_seq + j and sees keys 0..that position.
+ *               Every seq_lens[b] must be >= q_per_seq and <= max_seq_len.
+ *   max_seq_len host-side upper bound of seq_lens (sizes the launch).
+ *   q_idx       [n_seqs*q_per_seq][h_idx][d_idx] idx_dtype.
+ *   w           [n_seqs*q_per_seq][h_idx] fp32 head weights.
+ *   out_idx     [n_seqs*q_per_seq][topk] int32: the selected key positions of
+ *               every query row, min(topk, pos+1) valid entries first in no
+ *               particular order, then -1.
+ *   out_scores  [n_seqs*q_per_seq][topk] fp32 scores of out_idx, or NULL.
+ * Supported: h_idx in {4, 8, 16, 32, 64}; 1 <= topk <= 2048. Integer-valued
+ * inputs make the selection bit-identical to the exact fp32 definition.
+ * ------------------------------------------------------------------------- */
+size_t smla_indexer_topk_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
+                                        int32_t h_idx, int32_t topk);
+int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
+                      int32_t n_seqs, const int32_t* seq_lens, int32_t max_seq_len, int32_t q_per_seq,
+                      const void* q_idx, const float* w, int32_t h_idx, int32_t topk, int32_t* out_idx,
+                      float* out_scores, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * smla_sparse_mla_fwd — step 3 alone over caller-given index lists.
+ *
+ * Rows are laid out as in smla_indexer_topk: n_seqs sequences of q_per_seq
+ * rows. Positions: if seq_lens is NULL there is one sequence (n_seqs must be
+ * 1) and row i sits at prefix_len + i; otherwise row j of sequence b sits at
+ * seq_lens[b] - q_per_seq + j.
+ *   q     [rows][n_heads][576] bf16 (the absorbed query, latent + rope).
+ *   idx   [rows][topk] int32 key positions. Row r reads entries
+ *         [0, min(topk, pos_r + 1)); entries < 0 or > pos_r are skipped.
+ *   out   [rows][n_heads][512] bf16 attention output (normalised).
+ *   lse   [rows][n_heads] fp32 natural-log sum of exp(sm_scale * q.K), or NULL.
+ *         A row with no usable entry gets out = 0 and lse = -inf.
+ * FP8 caches are computed with f16 tensor-core operands: |q| and the
+ * dequantised cache values must stay below 65504.
+ * Supported: n_heads in {16, 64} (16 and 64 query heads of the configurations),
+ * topk <= 2048.
+ * ------------------------------------------------------------------------- */
+size_t smla_sparse_mla_fwd_workspace_size(int32_t rows, int32_t n_heads, int32_t topk);
+int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
+                        int32_t n_seqs, const int32_t* seq_lens, int32_t prefix_len, int32_t q_per_seq,
+                        const void* q, int32_t n_heads, const int32_t* idx, int32_t topk, float sm_scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * smla_sparse_mla_prefill — steps 1-3 for n_tokens new query tokens of ONE
+ * sequence placed after prefix_len cached tokens (query i at prefix_len + i).
+ * The caller has already written the KV and indexer-key rows of all
+ * prefix_len + n_tokens tokens into the cache.
+ *   page_table [ceil((prefix_len + n_tokens) / 64)] int32.
+ *   q, q_idx, w, out, lse as above with rows = n_tokens.
+ *   out_idx    [n_tokens][topk] int32 selected indices, or NULL to keep them
+ *              in the workspace only.
+ * ------------------------------------------------------------------------- */
+size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t n_heads,
+                                              int32_t h_idx, int32_t topk);
+int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_table, int32_t prefix_len,
+                            int32_t n_tokens, const void* q, int32_t n_heads, const void* q_idx,
+                            const float* w, int32_t h_idx, int32_t topk, float sm_scale, void* out,
+                            float* lse, int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
+ * smla_sparse_mla_decode — steps 1-3 for a decode batch: n_seqs requests with
+ * q_per_seq new tokens each (1 for plain decode, 2 for one MTP draft), over a
+ * paged cache with one page table per request. Arguments as in
+ * smla_indexer_topk and smla_sparse_mla_fwd. q_per_seq must be in [1, 8].
+ * ------------------------------------------------------------------------- */
+size_t smla_sparse_mla_decode_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
+                                             int32_t n_heads, int32_t h_idx, int32_t topk);
+int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
+                           int32_t n_seqs, const int32_t* seq_lens, int32_t max_seq_len,
+                           int32_t q_per_seq, const void* q, int32_t n_heads, const void* q_idx,
+                           const float* w, int32_t h_idx, int32_t topk, float sm_scale, void* out,
+                           float* lse, int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* ---------------------------------------------------------------------------
+ * smla_read_status — waits for `stream`, then reads the device status word of
+ * `workspace` written by the calls that used it: SMLA_OK, SMLA_ERR_DEVICE_BOUNDS
+ * or SMLA_ERR_TIMEOUT (the latter wins); the raw bit mask goes to *bits if
+ * non-NULL. Each entry point clears the word when it starts.
+ * ------------------------------------------------------------------------- */
+int smla_read_status(const void* workspace, void* stream, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMLA_H_ */

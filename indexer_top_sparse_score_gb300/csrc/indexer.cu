@@ -1,0 +1,666 @@
+// Fused indexer + exact causal top-k (steps 1 and 2 of the layer step).
+//
+// "Optimisations de GLM-5.3, partie 2" (section "Pourquoi pas TP ou DP ?"):
+// the indexer scores every earlier token and sparse MLA reads the best 2,048.
+// Here the score is
+//     score(t, s) = sum_h w[t,h] * ReLU(q_I[t,h,:] . k_I[s,:]) * kscale[s]
+// and the selection keeps, per query row, the top-k keys s <= pos(t) ordered
+// by (score descending, index ascending).
+//
+// One CTA per SM (persistent). A work item is TQ query rows against a key
+// range, streamed in tiles of 128 keys:
+//   warp 0      TMA producer: q_I tile once per item, k_I tiles (two 64-row
+//               pages each, page table resolved here) into a 4-stage ring;
+//   warp 1      MMA issuer: D[128 keys x (TQ*H_I)] = k_I_tile . q_I^T with
+//               tcgen05 (kind::f8f6f4 for e4m3, kind::f16 for bf16), fp32
+//               accumulators double-buffered in TMEM;
+//   warp 2      TMEM allocator;
+//   warps 4-11  two epilogue warpgroups; each thread owns one key (TMEM lane)
+//               and computes the ReLU + head-weighted sum in registers, then
+//               streams the keys that beat the token's threshold into a
+//               per-token candidate buffer in shared memory. A full buffer is
+//               compacted to its exact top-k by a radix select, which also
+//               raises the threshold. The T x N score matrix never leaves the
+//               SM.
+// Work items: prefill ("group mode") takes TQ consecutive rows of one
+// sequence against all their keys; items are handed out in head/tail pairs
+// (the i-th cheapest with the i-th most expensive, the "V" pairing of the
+// page's PCP section applied across SMs) so every CTA gets the same mix of
+// short and long causal rows. Decode ("split mode") takes all rows of one
+// sequence against one block of 8192 keys; a merge kernel then selects the
+// exact top-k of the per-block candidate lists.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace smla {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileKeys = 128;
+constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
+constexpr int kMaxN = 128;                             // TQ * H_I
+constexpr int kEpiThreads = 256;
+constexpr int kThreads = 384;
+
+struct IdxParams {
+  const float* k_scale;  // [pool rows] or null
+  const int32_t* page_tables;
+  int32_t max_pages, num_pages;
+  int32_t n_seqs, q_per_seq, n_rows;
+  const int32_t* seq_lens;  // device or null
+  int32_t prefix_len;
+  const float* w;
+  int32_t topk;
+  int32_t tq, cap;
+  int32_t is_bf16;
+  int32_t split;
+  int32_t n_groups;   // group mode: groups per sequence
+  int32_t n_kblocks;  // split mode: key blocks per sequence
+  int32_t n_items;    // group mode: n_seqs * n_groups; split: n_seqs * n_kblocks
+  int32_t tmem_cols;
+  int32_t* out_idx;
+  float* out_scores;
+  uint32_t* cand_key;
+  uint32_t* cand_idx;
+  int32_t* cand_cnt;
+  uint32_t* status;
+};
+
+struct Item {
+  int seq, row0, nrows, pos0;
+  int key_lo, key_hi;
+  int t0, t1;
+  int kb;
+  bool trivial;
+};
+
+// The k-th item of this CTA. Returns -1 when the CTA has no more items, 0 for
+// an empty slot (skip), 1 for a real item. Every role calls this with the
+// same k sequence, so all roles agree on the schedule.
+__device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it) {
+  if (!p.split) {
+    const int G = p.n_items;
+    const int P = (G + 1) / 2;
+    const int pair = blockIdx.x + (k >> 1) * gridDim.x;
+    if (pair >= P) return -1;
+    int g = (k & 1) ? (G - 1 - pair) : pair;
+    if ((k & 1) && g == pair) return 0;
+    const int seq = g / p.n_groups;
+    const int gi = g - seq * p.n_groups;
+    const int rin = gi * p.tq;
+    it.seq = seq;
+    it.row0 = seq * p.q_per_seq + rin;
+    it.nrows = min(p.tq, p.q_per_seq - rin);
+    const int L = p.seq_lens ? p.seq_lens[seq] : p.prefix_len + p.q_per_seq;
+    it.pos0 = L - p.q_per_seq + rin;
+    it.key_lo = 0;
+    it.key_hi = it.pos0 + it.nrows;
+    it.kb = 0;
+    it.trivial = it.key_hi <= p.topk && p.out_scores == nullptr;
+  } else {
+    const int i = blockIdx.x + k * gridDim.x;
+    if (i >= p.n_items) return -1;
+    const int seq = i / p.n_kblocks;
+    const int kb = i - seq * p.n_kblocks;
+    const int L = p.seq_lens[seq];
+    if (kb * kKeyBlock >= L) return 0;
+    it.seq = seq;
+    it.row0 = seq * p.q_per_seq;
+    it.nrows = p.q_per_seq;
+    it.pos0 = L - p.q_per_seq;
+    it.key_lo = kb * kKeyBlock;
+    it.key_hi = min(L, it.key_lo + kKeyBlock);
+    it.kb = kb;
+    it.trivial = false;
+  }
+  if (it.key_hi <= it.key_lo) return 0;
+  it.t0 = it.key_lo / kTileKeys;
+  it.t1 = (it.key_hi + kTileKeys - 1) / kTileKeys;
+  return 1;
+}
+
+__device__ __forceinline__ int page_of(const IdxParams& p, const int32_t* pt, int lp) {
+  if (lp >= p.max_pages) {
+    set_status(p.status, kStatusBounds);
+    return 0;
+  }
+  const int pg = __ldg(pt + lp);
+  if (pg < 0 || pg >= p.num_pages) {
+    set_status(p.status, kStatusBounds);
+    return 0;
+  }
+  return pg;
+}
+
+template <int HI>
+__device__ __forceinline__ void tmem_ld_heads(uint32_t taddr, uint32_t* r) {
+  if constexpr (HI == 4) tmem_ld_32x32b_x4(taddr, r);
+  else if constexpr (HI == 8) tmem_ld_32x32b_x8(taddr, r);
+  else if constexpr (HI == 16) tmem_ld_32x32b_x16(taddr, r);
+  else if constexpr (HI == 32) tmem_ld_32x32b_x32(taddr, r);
+  else {
+    tmem_ld_32x32b_x32(taddr, r);
+    tmem_ld_32x32b_x32(taddr + 32, r + 32);
+  }
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
+                   const IdxParams p) {
+  constexpr int TPW_MAX = 64 / HI;  // tokens per epilogue warpgroup held in registers
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* a_tiles = smem;
+  uint8_t* b_tile = smem + kStages * kStageBytes;
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(b_tile + kMaxN * kIdxRowBytes);
+  uint32_t* cidx = ckey + kBufEntries;
+  float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][256]
+  uint32_t* scratch = hist + 512;                               // [2][8]
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 16);      // [128]
+  uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 128);     // [128]
+  uint32_t* wsum = theta + 128;                                 // [2][4]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + 8);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* b_full = acc_empty + 2;
+  uint64_t* b_empty = b_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, kStatusSetup);
+    return;
+  }
+  const int N = HI * p.tq;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiThreads / 32);
+    }
+    mbar_init(b_full, 1);
+    mbar_init(b_empty, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort_v = abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_q);
+      uint32_t sc = 0, bi = 0;
+      for (int k = 0;; ++k) {
+        Item it;
+        const int r = next_item(p, k, it);
+        if (r < 0) break;
+        if (r == 0 || it.trivial) continue;
+        if (!mbar_wait(b_empty, (bi & 1) ^ 1, abort_v, p.status)) break;
+        ++bi;
+        mbar_arrive_expect_tx(b_full, N * kIdxRowBytes);
+        tma_load_2d(b_tile, &map_q, b_full, 0, it.row0 * HI);
+        const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
+        bool ok = true;
+        for (int t = it.t0; t < it.t1 && ok; ++t, ++sc) {
+          const int s = sc % kStages;
+          if (!mbar_wait(&a_empty[s], ((sc / kStages) & 1) ^ 1, abort_v, p.status)) {
+            ok = false;
+            break;
+          }
+          const bool has1 = (2 * t + 1) * kPage < it.key_hi;
+          const int pg0 = page_of(p, pt, 2 * t);
+          const int pg1 = has1 ? page_of(p, pt, 2 * t + 1) : 0;
+          mbar_arrive_expect_tx(&a_full[s], has1 ? kStageBytes : kStageBytes / 2);
+          tma_load_2d(a_tiles + s * kStageBytes, &map_k, &a_full[s], 0, pg0 * kPage);
+          if (has1) tma_load_2d(a_tiles + s * kStageBytes + kStageBytes / 2, &map_k, &a_full[s], 0, pg1 * kPage);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = p.is_bf16 ? instr_desc(128, N, kFmtBF16, kFmtBF16, false, false)
+                                       : instr_desc(128, N, kFmtE4M3, kFmtE4M3, false, false);
+      uint32_t sc = 0, bi = 0, ac = 0;
+      const uint32_t b0 = smem_u32(b_tile);
+      for (int k = 0;; ++k) {
+        Item it;
+        const int r = next_item(p, k, it);
+        if (r < 0) break;
+        if (r == 0 || it.trivial) continue;
+        if (!mbar_wait(b_full, bi & 1, abort_v, p.status)) break;
+        ++bi;
+        tc_fence_after();
+        bool ok = true;
+        for (int t = it.t0; t < it.t1; ++t, ++sc, ++ac) {
+          const int s = sc % kStages;
+          const int buf = ac & 1;
+          if (!mbar_wait(&a_full[s], (sc / kStages) & 1, abort_v, p.status) ||
+              !mbar_wait(&acc_empty[buf], ((ac >> 1) & 1) ^ 1, abort_v, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(a_tiles + s * kStageBytes);
+          const uint32_t d = tmem + buf * N;
+#pragma unroll
+          for (int kk = 0; kk < kIdxRowBytes / 32; ++kk) {
+            const uint64_t ad = smem_desc(a0 + 32 * kk, 16, 1024);
+            const uint64_t bd = smem_desc(b0 + 32 * kk, 16, 1024);
+            if (p.is_bf16) mma_f16(d, ad, bd, idesc, kk > 0);
+            else mma_f8(d, ad, bd, idesc, kk > 0);
+          }
+          mma_commit(&a_empty[s]);
+          mma_commit(&acc_full[buf]);
+        }
+        if (!ok) break;
+        mma_commit(b_empty);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 4;
+    const int wg = ew >> 2;
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int tid_wg = (ew & 3) * 32 + lane;
+    const uint32_t bar_wg = 1 + wg;
+    uint32_t* hist_wg = hist + 256 * wg;
+    uint32_t* scr_wg = scratch + 8 * wg;
+    uint32_t* wsum_wg = wsum + 4 * wg;
+    auto wg_sync = [&]() { named_bar_sync(bar_wg, 128); };
+    const int tpw = (p.tq + 1) / 2;
+    const int j0 = wg * tpw, j1 = min(p.tq, j0 + tpw);
+    const int cap = p.cap;
+    const int topk = p.topk;
+    const uint32_t lanemask_lt = (1u << lane) - 1u;
+    uint32_t ac = 0;
+
+    // Select the best `keep` of token j's buffer; if `out` is set, write the
+    // selection to the output row, else compact it in place and raise theta.
+    auto select_token = [&](int j, int keep, bool to_output, const Item& it) {
+      const int n = cnt[j];
+      uint32_t* kb = ckey + j * cap;
+      uint32_t* ib = cidx + j * cap;
+      uint32_t tk = 0, ti = 0xFFFFFFFFu;
+      bool all = n <= keep;
+      if (!all) {
+        radix_select<128>(
+            keep, tid_wg, hist_wg, scr_wg,
+            [&](auto f) {
+              for (int e = tid_wg; e < n; e += 128) f(kb[e], ib[e]);
+            },
+            wg_sync, tk, ti);
+      }
+      const int row = it.row0 + j;
+      int base = 0;
+      for (int c0 = 0; c0 < n; c0 += 128) {
+        const int e = c0 + tid_wg;
+        uint32_t key = 0, idx = 0;
+        bool take = false;
+        if (e < n) {
+          key = kb[e];
+          idx = ib[e];
+          take = all || selected(key, idx, tk, ti);
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+        if (lane == 0) wsum_wg[ew & 3] = __popc(m);
+        wg_sync();
+        int off = base, total = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+          const int v = static_cast<int>(wsum_wg[w2]);
+          if (w2 < (ew & 3)) off += v;
+          total += v;
+        }
+        off += __popc(m & lanemask_lt);
+        wg_sync();
+        if (take) {
+          if (!to_output) {
+            kb[off] = key;
+            ib[off] = idx;
+          } else if (!p.split) {
+            p.out_idx[static_cast<size_t>(row) * topk + off] = static_cast<int32_t>(idx);
+            if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + off] = key_score(key);
+          } else {
+            const size_t slot = (static_cast<size_t>(row) * p.n_kblocks + it.kb) * topk + off;
+            p.cand_key[slot] = key;
+            p.cand_idx[slot] = idx;
+          }
+        }
+        base += total;
+      }
+      if (to_output) {
+        if (!p.split) {
+          for (int e = base + tid_wg; e < topk; e += 128) {
+            p.out_idx[static_cast<size_t>(row) * topk + e] = -1;
+            if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + e] = 0.0f;
+          }
+        } else if (tid_wg == 0) {
+          p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + it.kb] = base;
+        }
+      }
+      wg_sync();
+      if (!to_output && tid_wg == 0) {
+        cnt[j] = base;
+        theta[j] = tk;
+      }
+      wg_sync();
+    };
+
+    for (int k = 0;; ++k) {
+      Item it;
+      const int r = next_item(p, k, it);
+      if (r < 0) break;
+      if (r == 0) continue;
+      named_bar_sync(3, kEpiThreads);
+      for (int i = threadIdx.x - 128; i < N; i += kEpiThreads) {
+        const int gi = it.row0 * HI + i;
+        wbuf[i] = gi < p.n_rows * HI ? __ldg(p.w + gi) : 0.0f;
+      }
+      for (int j = threadIdx.x - 128; j < p.tq; j += kEpiThreads) {
+        cnt[j] = 0;
+        theta[j] = 0;
+      }
+      named_bar_sync(3, kEpiThreads);
+      if (it.trivial) {
+        // every key of every row is selected: write 0..pos, then -1
+        for (int j = j0; j < j1 && j < it.nrows; ++j) {
+          const int n = it.pos0 + j + 1;
+          int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + j) * topk;
+          for (int e = tid_wg; e < topk; e += 128) o[e] = e < n ? e : -1;
+        }
+        continue;
+      }
+      const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
+      bool ok = true;
+      for (int t = it.t0; t < it.t1; ++t, ++ac) {
+        const int buf = ac & 1;
+        if (!mbar_wait(&acc_full[buf], (ac >> 1) & 1, abort_v, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t raw[TPW_MAX * HI];
+#pragma unroll
+        for (int jj = 0; jj < TPW_MAX; ++jj)
+          if (j0 + jj < j1)
+            tmem_ld_heads<HI>(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N + (j0 + jj) * HI,
+                              raw + jj * HI);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+
+        const int s = t * kTileKeys + q * 32 + lane;
+        float ks = 1.0f;
+        if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+        uint32_t key[TPW_MAX];
+        bool adm[TPW_MAX];
+#pragma unroll
+        for (int jj = 0; jj < TPW_MAX; ++jj) {
+          const int j = j0 + jj;
+          adm[jj] = false;
+          key[jj] = 0;
+          if (j < j1) {
+            const float* wr = wbuf + j * HI;
+            float sc = 0.0f;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(raw[jj * HI + h]), 0.0f), sc);
+            sc *= ks;
+            key[jj] = score_key(sc);
+            const bool valid = j < it.nrows && s >= it.key_lo && s < it.key_hi && s <= it.pos0 + j;
+            adm[jj] = valid && key[jj] > theta[j];
+          }
+        }
+        wg_sync();
+        for (int j = j0; j < j1; ++j)
+          if (cnt[j] > cap - kTileKeys) select_token(j, topk, false, it);
+#pragma unroll
+        for (int jj = 0; jj < TPW_MAX; ++jj) {
+          const int j = j0 + jj;
+          if (j < j1) {
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, adm[jj]);
+            if (m) {
+              int base = 0;
+              if (lane == 0) base = atomicAdd(&cnt[j], __popc(m));
+              base = __shfl_sync(0xFFFFFFFFu, base, 0);
+              if (adm[jj]) {
+                const int pos = base + __popc(m & lanemask_lt);
+                ckey[j * cap + pos] = key[jj];
+                cidx[j * cap + pos] = static_cast<uint32_t>(s);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      wg_sync();
+      for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, p.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
+// Decode merge: exact top-k of the per-key-block candidate lists of one row.
+struct MergeParams {
+  const uint32_t* cand_key;
+  const uint32_t* cand_idx;
+  const int32_t* cand_cnt;
+  const int32_t* seq_lens;
+  int32_t q_per_seq, n_kblocks, topk;
+  int32_t* out_idx;
+  float* out_scores;
+};
+
+constexpr int kMergeThreads = 512;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t scratch[8];
+  __shared__ uint32_t wsum[kMergeThreads / 32];
+  __shared__ int32_t counts[256];
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq = row / p.q_per_seq;
+  const int nb = min((p.seq_lens[seq] + kKeyBlock - 1) / kKeyBlock, p.n_kblocks);
+  int total = 0;
+  for (int b = 0; b < nb; ++b) total += p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + b];
+  if (tid < 256) counts[tid] = 0;
+  __syncthreads();
+  for (int b = tid; b < nb && b < 256; b += kMergeThreads) counts[b] = p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + b];
+  __syncthreads();
+  const size_t base_row = static_cast<size_t>(row) * p.n_kblocks;
+  auto blk_cnt = [&](int b) { return b < 256 ? counts[b] : p.cand_cnt[base_row + b]; };
+  auto each = [&](auto f) {
+    for (int b = 0; b < nb; ++b) {
+      const int c = blk_cnt(b);
+      const size_t off = (base_row + b) * p.topk;
+      for (int i = tid; i < c; i += kMergeThreads) f(p.cand_key[off + i], p.cand_idx[off + i]);
+    }
+  };
+  auto sync = [&]() { __syncthreads(); };
+  uint32_t tk = 0, ti = 0xFFFFFFFFu;
+  const bool all = total <= p.topk;
+  if (!all) radix_select<kMergeThreads>(p.topk, tid, hist, scratch, each, sync, tk, ti);
+  int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
+  float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
+  int outn = 0;
+  const uint32_t lanemask_lt = (1u << lane) - 1u;
+  for (int b = 0; b < nb; ++b) {
+    const int c = blk_cnt(b);
+    const size_t off = (base_row + b) * p.topk;
+    for (int c0 = 0; c0 < c; c0 += kMergeThreads) {
+      const int i = c0 + tid;
+      uint32_t key = 0, idx = 0;
+      bool take = false;
+      if (i < c) {
+        key = p.cand_key[off + i];
+        idx = p.cand_idx[off + i];
+        take = all || selected(key, idx, tk, ti);
+      }
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+      if (lane == 0) wsum[warp] = __popc(m);
+      __syncthreads();
+      int pos = outn, tot = 0;
+      for (int w2 = 0; w2 < kMergeThreads / 32; ++w2) {
+        if (w2 < warp) pos += wsum[w2];
+        tot += wsum[w2];
+      }
+      pos += __popc(m & lanemask_lt);
+      __syncthreads();
+      if (take) {
+        o[pos] = static_cast<int32_t>(idx);
+        if (os) os[pos] = key_score(key);
+      }
+      outn += tot;
+    }
+  }
+  for (int e = outn + tid; e < p.topk; e += kMergeThreads) {
+    o[e] = -1;
+    if (os) os[e] = 0.0f;
+  }
+}
+
+template <int HI>
+int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
+  CUtensorMap map_k, map_q;
+  const CUtensorMapDataType dt = prm.is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t esz = prm.is_bf16 ? 2 : 1;
+  const uint32_t inner = kIdxRowBytes / esz;
+  const int N = HI * prm.tq;
+  if (!encode_2d(&map_k, dt, L.cache->k_idx, inner, static_cast<uint64_t>(L.cache->num_pages) * kPage,
+                 kIdxRowBytes, inner, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SMLA_ERR_CUDA;
+  if (!encode_2d(&map_q, dt, L.q_idx, inner, static_cast<uint64_t>(prm.n_rows) * HI, kIdxRowBytes, inner, N,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return SMLA_ERR_CUDA;
+  const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
+                      512 * 4 + 16 * 4 + 128 * 4 + 128 * 4 + 8 * 4 + 16 * 8 + 16;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    attr_done = true;
+  }
+  const int grid_items = prm.split ? prm.n_items : (prm.n_items + 1) / 2;
+  const int grid = std::max(1, std::min(num_sms(), grid_items));
+  indexer_kernel<HI><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+}  // namespace
+
+bool indexer_split_mode(int32_t q_per_seq, int32_t h_idx) {
+  // few query rows per sequence: split the keys so every SM streams some of them
+  return q_per_seq * h_idx <= kMaxN && q_per_seq <= 8;
+}
+
+int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_per_seq) {
+  const int max_tq = kMaxN / h_idx;
+  if (split) {
+    int tq = 1;
+    while (tq < q_per_seq) tq <<= 1;
+    if (tq * h_idx < 16) tq = 16 / h_idx;
+    return (tq <= max_tq && kBufEntries / tq - 2 * kTileKeys >= topk) ? tq : 0;
+  }
+  int tq = max_tq;
+  while (tq > 1 && kBufEntries / tq - 2 * kTileKeys < topk) tq >>= 1;
+  if (tq * h_idx < 16) return 0;
+  return kBufEntries / tq - 2 * kTileKeys >= topk ? tq : 0;
+}
+
+size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
+                               int32_t topk) {
+  size_t bytes = kStatusBytes;
+  if (indexer_split_mode(q_per_seq, h_idx)) {
+    const size_t nkb = (static_cast<size_t>(max_seq_len) + kKeyBlock - 1) / kKeyBlock;
+    const size_t rows = static_cast<size_t>(n_seqs) * q_per_seq;
+    bytes += rows * nkb * topk * 8 + ((rows * nkb * 4 + 255) / 256) * 256;
+  }
+  return bytes;
+}
+
+int launch_indexer(const IndexerLaunch& L) {
+  const bool split = indexer_split_mode(L.q_per_seq, L.h_idx);
+  const int tq = indexer_tokens_per_cta(L.h_idx, L.topk, split, L.q_per_seq);
+  if (tq <= 0) return SMLA_ERR_UNSUPPORTED;
+  IdxParams prm{};
+  prm.k_scale = L.cache->k_idx_scale;
+  prm.page_tables = L.page_tables;
+  prm.max_pages = L.max_pages;
+  prm.num_pages = L.cache->num_pages;
+  prm.n_seqs = L.n_seqs;
+  prm.q_per_seq = L.q_per_seq;
+  prm.n_rows = L.n_seqs * L.q_per_seq;
+  prm.seq_lens = L.seq_lens;
+  prm.prefix_len = L.prefix_len;
+  prm.w = L.w;
+  prm.topk = L.topk;
+  prm.tq = tq;
+  prm.cap = kBufEntries / tq;
+  prm.is_bf16 = L.cache->idx_dtype == SMLA_BF16;
+  prm.split = split;
+  const int N = L.h_idx * tq;
+  int cols = 32;
+  while (cols < 2 * N) cols <<= 1;
+  prm.tmem_cols = cols;
+  prm.out_idx = L.out_idx;
+  prm.out_scores = L.out_scores;
+  uint8_t* ws = static_cast<uint8_t*>(L.workspace);
+  prm.status = reinterpret_cast<uint32_t*>(ws);
+  const size_t rows = static_cast<size_t>(prm.n_rows);
+  if (split) {
+    prm.n_kblocks = (L.max_seq_len + kKeyBlock - 1) / kKeyBlock;
+    prm.n_items = L.n_seqs * prm.n_kblocks;
+    const size_t nk = static_cast<size_t>(prm.n_kblocks);
+    prm.cand_key = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+    prm.cand_idx = prm.cand_key + rows * nk * L.topk;
+    prm.cand_cnt = reinterpret_cast<int32_t*>(prm.cand_idx + rows * nk * L.topk);
+  } else {
+    prm.n_groups = (L.q_per_seq + tq - 1) / tq;
+    prm.n_items = L.n_seqs * prm.n_groups;
+  }
+  int rc;
+  switch (L.h_idx) {
+    case 4: rc = launch_indexer_t<4>(L, prm); break;
+    case 8: rc = launch_indexer_t<8>(L, prm); break;
+    case 16: rc = launch_indexer_t<16>(L, prm); break;
+    case 32: rc = launch_indexer_t<32>(L, prm); break;
+    case 64: rc = launch_indexer_t<64>(L, prm); break;
+    default: return SMLA_ERR_UNSUPPORTED;
+  }
+  if (rc != SMLA_OK || !split) return rc;
+  MergeParams mp{prm.cand_key, prm.cand_idx, prm.cand_cnt, L.seq_lens, L.q_per_seq, prm.n_kblocks, L.topk,
+                 L.out_idx, L.out_scores};
+  merge_kernel<<<prm.n_rows, kMergeThreads, 0, L.stream>>>(mp);
+  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+}  // namespace smla

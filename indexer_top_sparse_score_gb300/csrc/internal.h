@@ -1,0 +1,74 @@
+// Host-side declarations shared by the launchers and the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/smla.h"
+
+namespace smla {
+
+constexpr int kPage = 64;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr size_t kStatusBytes = 256;
+constexpr int kIdxRowBytes = 128;     // indexer key / query row bytes supported
+constexpr int kKeyBlock = 8192;       // keys per work item in split (decode) mode
+constexpr int kBufEntries = 16384;    // top-k candidate entries per indexer CTA
+
+// Geometry of one indexer launch.
+struct IndexerLaunch {
+  const smla_paged_cache* cache;
+  const int32_t* page_tables;
+  int32_t max_pages;
+  int32_t n_seqs, q_per_seq;
+  const int32_t* seq_lens;  // device, or null: one sequence at prefix_len
+  int32_t prefix_len;
+  int32_t max_seq_len;      // host bound on keys of any sequence
+  const void* q_idx;
+  const float* w;
+  int32_t h_idx, topk;
+  int32_t* out_idx;
+  float* out_scores;
+  void* workspace;          // status word + candidate lists (split mode)
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+struct MlaLaunch {
+  const smla_paged_cache* cache;
+  const int32_t* page_tables;
+  int32_t max_pages;
+  int32_t n_seqs, q_per_seq;
+  const int32_t* seq_lens;
+  int32_t prefix_len;
+  const void* q;
+  int32_t n_heads;
+  const int32_t* idx;
+  int32_t topk;
+  float sm_scale;
+  void* out;
+  float* lse;
+  uint32_t* status;
+  cudaStream_t stream;
+};
+
+// Whether the indexer runs token groups over the full key range (prefill) or
+// splits each sequence's keys into blocks merged afterwards (decode).
+bool indexer_split_mode(int32_t q_per_seq, int32_t h_idx);
+int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_per_seq);
+size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
+                               int32_t topk);
+
+int launch_indexer(const IndexerLaunch& L);   // returns smla_status
+int launch_mla(const MlaLaunch& L);           // returns smla_status
+
+// TMA tensor-map encoding through the driver entry point (no -lcuda).
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
+               uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle);
+
+int num_sms();
+
+}  // namespace smla

@@ -1,0 +1,561 @@
+// Sparse MLA over selected latent rows (step 3 of the layer step).
+//
+// "Optimisations de GLM-5.3, partie 2", section "PCP" and footnote 1: each
+// selected latent row (576 values) is read once and serves all query heads;
+// QK uses all 576 values, PV the first 512. Per query row t:
+//     l_j  = sm_scale * q[h,:] . K[s_j,:]          (s_j = selected keys)
+//     out  = softmax_j(l) . K[s_j, 0:512],   lse = log sum_j exp(l_j)
+//
+// One CTA per SM (persistent); query rows are handed out in head/tail pairs
+// (cheap causal rows with expensive ones). For each row the 2048 selected
+// rows stream through in blocks of 64:
+//   warps 8-11  gather producers: resolve key -> page -> pool row and copy the
+//               row into a 128B-swizzled shared tile (cp.async for BF16; FP8
+//               rows are loaded, widened e4m3 -> f16 and stored), 2 stages;
+//   warp 0      MMA issuer:  S[64 heads x 64 rows] = Q . K^T   (tcgen05,
+//               M=64, K=576) into one of two TMEM S buffers, and
+//               O^T[512 x H] += V^T . P^T  (M=128 per 128-dim slice of V, the
+//               same shared tile read MN-major, P^T from shared memory);
+//   warps 4-7   softmax: S from TMEM (two threads per head), online softmax
+//               in the log2 domain with a lazy rescale (O is only rescaled
+//               when a head's running max grows by more than 2^8), P to
+//               shared memory; finally O^T from TMEM, normalised, to HBM.
+//   warp 1      TMA load of the BF16 query tile (BF16 caches).
+// The FP8 path computes in f16 (e4m3 -> f16 is exact): the per-token scale
+// multiplies the logit of its row and its probability before PV.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace smla {
+
+namespace {
+
+constexpr int kBlk = 64;                     // selected rows per block
+constexpr int kChunks = kDqk / 64;           // 9 chunks of 64 values
+constexpr int kChunkBytes = kBlk * 128;      // 8 KB
+constexpr int kTileBytes = kChunks * kChunkBytes;  // 72 KB per stage / for Q
+constexpr int kPBytes = 64 * 128;            // P^T: 64 head rows x 64 values
+constexpr int kThreads = 384;
+constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+
+struct MlaParams {
+  const uint8_t* kv;
+  const float* kv_scale;
+  const int32_t* page_tables;
+  int32_t max_pages, num_pages;
+  int32_t n_seqs, q_per_seq, n_rows;
+  const int32_t* seq_lens;
+  int32_t prefix_len;
+  const uint16_t* q;
+  const int32_t* idx;
+  int32_t topk;
+  float scale_log2;  // sm_scale * log2(e)
+  uint16_t* out;
+  float* lse;
+  int32_t fp8;
+  uint32_t* status;
+};
+
+struct SmemMeta {
+  float colscale[2][kBlk];  // logit multiplier per selected row (0 if skipped)
+  float pscale[2][kBlk];    // probability multiplier (FP8 per-token scale)
+  uint8_t valid[2][kBlk];
+  float linv[64];
+  float alpha[64];
+  uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, pv_done, o_empty;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+constexpr size_t kSmemBytes = 2 * kTileBytes + kTileBytes + kPBytes + sizeof(SmemMeta);
+
+// k-th row of this CTA: head/tail pairs. -1 done, 0 skip, 1 row.
+__device__ __forceinline__ int next_row(int n_rows, int k, int& row) {
+  const int P = (n_rows + 1) / 2;
+  const int pair = blockIdx.x + (k >> 1) * gridDim.x;
+  if (pair >= P) return -1;
+  row = (k & 1) ? (n_rows - 1 - pair) : pair;
+  if ((k & 1) && row == pair) return 0;
+  return 1;
+}
+
+struct RowInfo {
+  int seq, pos, nvalid, nb;
+};
+
+__device__ __forceinline__ RowInfo row_info(const MlaParams& p, int row) {
+  RowInfo r;
+  r.seq = row / p.q_per_seq;
+  const int j = row - r.seq * p.q_per_seq;
+  const int L = p.seq_lens ? p.seq_lens[r.seq] : p.prefix_len + p.q_per_seq;
+  r.pos = L - p.q_per_seq + j;
+  r.nvalid = max(0, min(p.topk, r.pos + 1));
+  r.nb = (r.nvalid + kBlk - 1) / kBlk;
+  return r;
+}
+
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (NC == 16) tmem_ld_32x32b_x16(taddr, r);
+  else tmem_ld_32x32b_x32(taddr, r);
+}
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+  if constexpr (NC == 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+  } else {
+    tmem_st_32x32b_x32(taddr, r);
+  }
+}
+
+template <int H>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* q_tile = smem;
+  uint8_t* stage = smem + kTileBytes;  // 2 stages
+  uint8_t* p_tile = smem + 3 * kTileBytes;
+  SmemMeta& M = *reinterpret_cast<SmemMeta*>(smem + 3 * kTileBytes + kPBytes);
+
+  constexpr int kColChunk = H < 32 ? H : 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) set_status(p.status, kStatusSetup);
+    return;
+  }
+  // Q rows H..63 stay zero (the QK MMA always has M = 64)
+  if (H < 64) {
+    for (int i = threadIdx.x; i < kTileBytes / 16; i += kThreads) {
+      const int rowb = (i * 16 % kChunkBytes) / 128;
+      if (rowb >= H) reinterpret_cast<uint4*>(q_tile)[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&M.q_full, 1);
+    mbar_init(&M.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&M.kv_full[i], 128);
+      mbar_init(&M.kv_empty[i], 1);
+      mbar_init(&M.s_full[i], 1);
+      mbar_init(&M.s_empty[i], 4);
+    }
+    mbar_init(&M.p_full, 4);
+    mbar_init(&M.pv_done, 1);
+    mbar_init(&M.o_empty, 4);
+    M.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&M.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = M.tmem_slot;
+  volatile int* abort_v = &M.abort_flag;
+  const uint32_t fmt = p.fp8 ? kFmtF16 : kFmtBF16;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc_qk = instr_desc(64, 64, fmt, fmt, false, false);
+      const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, false);
+      const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage), p0 = smem_u32(p_tile);
+      uint32_t g = 0, tok = 0;
+      bool ok = true;
+      auto issue_qk = [&](uint32_t gq) -> bool {
+        const int s = gq & 1;
+        if (!mbar_wait(&M.kv_full[s], (gq >> 1) & 1, abort_v, p.status)) return false;
+        if (!mbar_wait(&M.s_empty[s], ((gq >> 1) & 1) ^ 1, abort_v, p.status)) return false;
+        tc_fence_after();
+        const uint32_t sb = st0 + s * kTileBytes;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(q0 + c * kChunkBytes + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc(sb + c * kChunkBytes + kk * 32, 16, 1024);
+            mma_f16(tmem + kColS + s * 64, ad, bd, idesc_qk, (c | kk) != 0);
+          }
+        mma_commit(&M.s_full[s]);
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        int row;
+        const int r = next_row(p.n_rows, k, row);
+        if (r < 0) break;
+        if (r == 0) continue;
+        const RowInfo ri = row_info(p, row);
+        if (!mbar_wait(&M.q_full, tok & 1, abort_v, p.status)) break;
+        tc_fence_after();
+        if (!issue_qk(g)) break;
+        for (int b = 0; b < ri.nb; ++b) {
+          const uint32_t gb = g + b;
+          if (b + 1 < ri.nb) {
+            if (!issue_qk(gb + 1)) { ok = false; break; }
+          } else {
+            mma_commit(&M.q_empty);
+          }
+          if (!mbar_wait(&M.p_full, gb & 1, abort_v, p.status)) { ok = false; break; }
+          if (b == 0 && !mbar_wait(&M.o_empty, (tok & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sb = st0 + (gb & 1) * kTileBytes;
+#pragma unroll
+          for (int dt = 0; dt < 4; ++dt)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(sb + dt * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+              const uint64_t bd = smem_desc(p0 + kk * 32, 16, 1024);
+              mma_f16(tmem + kColO + dt * 64, ad, bd, idesc_pv, (b | kk) != 0);
+            }
+          mma_commit(&M.kv_empty[gb & 1]);
+          mma_commit(&M.pv_done);
+        }
+        g += ri.nb;
+        ++tok;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- Q (BF16 via TMA)
+    if (lane == 0 && !p.fp8) {
+      prefetch_tensormap(&map_q);
+      uint32_t tok = 0;
+      for (int k = 0;; ++k) {
+        int row;
+        const int r = next_row(p.n_rows, k, row);
+        if (r < 0) break;
+        if (r == 0) continue;
+        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
+        mbar_arrive_expect_tx(&M.q_full, H * kDqk * 2);
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(q_tile + c * kChunkBytes, &map_q, &M.q_full, c * 64, row * H);
+        ++tok;
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------- gather producers
+    const int tid = threadIdx.x - 256;  // 0..127
+    const int j = tid >> 1, half = tid & 1;
+    uint32_t g = 0, tok = 0;
+    for (int k = 0;; ++k) {
+      int row;
+      const int r = next_row(p.n_rows, k, row);
+      if (r < 0) break;
+      if (r == 0) continue;
+      const RowInfo ri = row_info(p, row);
+      if (p.fp8) {
+        // widen the BF16 query to f16 into the swizzled Q tile
+        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
+        const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
+        bool over = false;
+        for (int pc = tid; pc < H * 72; pc += 128) {
+          const int h = pc / 72, pp = pc - h * 72;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qr + h * kDqk + pp * 8));
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float a = __uint_as_float(in[u] << 16), b = __uint_as_float(in[u] & 0xFFFF0000u);
+            over |= fabsf(a) > 65504.0f || fabsf(b) > 65504.0f;
+            o[u] = pack_f16(a, b);
+          }
+          const int c = pp >> 3, qq = pp & 7;
+          *reinterpret_cast<uint4*>(q_tile + c * kChunkBytes + h * 128 + ((qq ^ (h & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (over) set_status(p.status, kStatusOverflow);
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (tid == 0) mbar_arrive(&M.q_full);
+      }
+      const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
+      const int32_t* ir = p.idx + static_cast<size_t>(row) * p.topk;
+      bool ok = true;
+      for (int b = 0; b < ri.nb; ++b, ++g) {
+        const int s = g & 1;
+        if (!mbar_wait(&M.kv_empty[s], ((g >> 1) & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
+        const int e = b * kBlk + j;
+        int64_t prow = -1;
+        if (e < ri.nvalid) {
+          const int key = __ldg(ir + e);
+          if (key >= 0 && key <= ri.pos) {
+            const int lp = key >> 6;
+            const int pg = lp < p.max_pages ? __ldg(pt + lp) : -1;
+            if (pg >= 0 && pg < p.num_pages) prow = static_cast<int64_t>(pg) * kPage + (key & 63);
+            else set_status(p.status, kStatusBounds);
+          }
+        }
+        uint8_t* st = stage + s * kTileBytes;
+        if (half == 0) {
+          const float ks = (p.fp8 && prow >= 0) ? __ldg(p.kv_scale + prow) : 1.0f;
+          M.colscale[s][j] = ks * p.scale_log2;
+          M.pscale[s][j] = ks;
+          M.valid[s][j] = prow >= 0;
+        }
+        if (!p.fp8) {
+          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * (kDqk * 2);
+          const uint32_t sbase = smem_u32(st);
+#pragma unroll 4
+          for (int u = 0; u < 36; ++u) {
+            const int pc = half * 36 + u;
+            const int c = pc >> 3, qq = pc & 7;
+            cp_async_16(sbase + c * kChunkBytes + j * 128 + ((qq ^ (j & 7)) << 4), src + pc * 16,
+                        prow >= 0 ? 16u : 0u);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+        } else {
+          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
+          uint4 v[18];
+#pragma unroll
+          for (int u = 0; u < 18; ++u)
+            v[u] = prow >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (half * 18 + u) * 16))
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 18; ++u) {
+            const int p8 = half * 18 + u;  // 16 e4m3 values = 32 bytes of f16
+            const int c = p8 >> 2, qq = (p8 & 3) * 2;
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              o[2 * t] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] & 0xFFFFu));
+              o[2 * t + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] >> 16));
+            }
+            uint8_t* rowp = st + c * kChunkBytes + j * 128;
+            *reinterpret_cast<uint4*>(rowp + (((qq) ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(rowp + (((qq + 1) ^ (j & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&M.kv_full[s]);
+      }
+      if (!ok) break;
+      ++tok;
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int qd = warp & 3;
+    const int half = lane >> 4;
+    const int h = 16 * qd + (lane & 15);
+    const bool real = h < H;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    uint32_t g = 0, tok = 0;
+    for (int k = 0;; ++k) {
+      int row;
+      const int r = next_row(p.n_rows, k, row);
+      if (r < 0) break;
+      if (r == 0) continue;
+      const RowInfo ri = row_info(p, row);
+      float m_used = -INFINITY, l = 0.0f;
+      bool ok = true;
+      for (int b = 0; b < ri.nb; ++b) {
+        const uint32_t gb = g + b;
+        const int s = gb & 1;
+        if (!mbar_wait(&M.s_full[s], (gb >> 1) & 1, abort_v, p.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t raw[32];
+        tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + s * 64, raw);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&M.s_empty[s]);
+        if (!mbar_wait(&M.kv_full[s], (gb >> 1) & 1, abort_v, p.status)) { ok = false; break; }
+        float x[32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int col = half * 32 + i;
+          x[i] = M.valid[s][col] ? __uint_as_float(raw[i]) * M.colscale[s][col] : -INFINITY;
+          mx = fmaxf(mx, x[i]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const float m_new = fmaxf(m_used, mx);
+        const bool resc = real && b > 0 && m_new > m_used + kRescaleLog2;
+        const bool any = named_bar_or(1, 128, resc);
+        if (b > 0 && !mbar_wait(&M.pv_done, (gb - 1) & 1, abort_v, p.status)) { ok = false; break; }
+        if (b == 0) {
+          m_used = m_new;
+        } else if (any) {
+          const float a = resc ? exp2f(m_used - m_new) : 1.0f;
+          if (resc) {
+            m_used = m_new;
+            l *= a;
+          }
+          if (half == 0) M.alpha[h] = a;
+          named_bar_sync(1, 128);
+          tc_fence_after();
+#pragma unroll 1
+          for (int dt = 0; dt < 4; ++dt) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < H; c0 += kColChunk) {
+              uint32_t o[kColChunk];
+              const uint32_t ta = tmem + lane_base + kColO + dt * 64 + c0;
+              tmem_ld_cols<kColChunk>(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < kColChunk; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * M.alpha[c0 + c]);
+              tmem_st_cols<kColChunk>(ta, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        const float mref = m_used == -INFINITY ? 0.0f : m_used;
+        float sum = 0.0f;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int col = half * 32 + i;
+          const float p0 = exp2f(x[i] - mref), p1 = exp2f(x[i + 1] - mref);
+          sum += p0 + p1;
+          const float a = p0 * M.pscale[s][col], c = p1 * M.pscale[s][col + 1];
+          pk[i >> 1] = p.fp8 ? pack_f16(a, c) : pack_bf16(a, c);
+        }
+        l += sum;
+        uint8_t* prow = p_tile + h * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int qq = half * 4 + u;
+          *reinterpret_cast<uint4*>(prow + ((qq ^ (h & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&M.p_full);
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      if (!mbar_wait(&M.pv_done, (g + ri.nb - 1) & 1, abort_v, p.status)) break;
+      tc_fence_after();
+      const float lt = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+      if (half == 0 && real) {
+        M.linv[h] = lt > 0.0f ? 1.0f / lt : 0.0f;
+        if (p.lse)
+          p.lse[static_cast<size_t>(row) * H + h] =
+              lt > 0.0f ? (m_used + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      }
+      named_bar_sync(1, 128);
+      uint16_t* orow = p.out + static_cast<size_t>(row) * H * kDv;
+      const bool odd = lane & 1;
+#pragma unroll 1
+      for (int dt = 0; dt < 4; ++dt) {
+        const int d = dt * 128 + qd * 32 + lane;
+        const int d_even = d & ~1;
+#pragma unroll 1
+        for (int c0 = 0; c0 < H; c0 += kColChunk) {
+          uint32_t o[kColChunk];
+          tmem_ld_cols<kColChunk>(tmem + lane_base + kColO + dt * 64 + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < kColChunk; c += 2) {
+            const float v0 = __uint_as_float(o[c]) * M.linv[c0 + c];
+            const float v1 = __uint_as_float(o[c + 1]) * M.linv[c0 + c + 1];
+            const float x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? v0 : v1, 1);
+            const uint32_t word = odd ? pack_bf16(x2, v1) : pack_bf16(v0, x2);
+            const int hh = c0 + (odd ? c + 1 : c);
+            *reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(hh) * kDv + d_even) = word;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.o_empty);
+      g += ri.nb;
+      ++tok;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int H>
+int launch_t(const MlaLaunch& L, const MlaParams& prm) {
+  CUtensorMap map_q;
+  if (!encode_2d(&map_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.q, kDqk, static_cast<uint64_t>(prm.n_rows) * H,
+                 kDqk * 2, 64, H, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SMLA_ERR_CUDA;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(mla_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    attr_done = true;
+  }
+  const int grid = std::max(1, std::min(num_sms(), (prm.n_rows + 1) / 2));
+  mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(map_q, prm);
+  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+}  // namespace
+
+int launch_mla(const MlaLaunch& L) {
+  MlaParams prm{};
+  prm.kv = static_cast<const uint8_t*>(L.cache->kv);
+  prm.kv_scale = L.cache->kv_scale;
+  prm.page_tables = L.page_tables;
+  prm.max_pages = L.max_pages;
+  prm.num_pages = L.cache->num_pages;
+  prm.n_seqs = L.n_seqs;
+  prm.q_per_seq = L.q_per_seq;
+  prm.n_rows = L.n_seqs * L.q_per_seq;
+  prm.seq_lens = L.seq_lens;
+  prm.prefix_len = L.prefix_len;
+  prm.q = static_cast<const uint16_t*>(L.q);
+  prm.idx = L.idx;
+  prm.topk = L.topk;
+  prm.scale_log2 = L.sm_scale * 1.4426950408889634f;
+  prm.out = static_cast<uint16_t*>(L.out);
+  prm.lse = L.lse;
+  prm.fp8 = L.cache->kv_dtype == SMLA_FP8_E4M3;
+  prm.status = L.status;
+  if (prm.n_rows == 0) return SMLA_OK;
+  switch (L.n_heads) {
+    case 16: return launch_t<16>(L, prm);
+    case 64: return launch_t<64>(L, prm);
+    default: return SMLA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace smla

@@ -113,15 +113,25 @@ static int64_t pool_row(const oracle_problem *p, int64_t seq, int64_t s) {
     return page * p->page_size + s % p->page_size;
 }
 
-static float idx_elem(const void *base, int dtype, int64_t i) {
-    if (dtype == ORACLE_BF16) return oracle_bf16_to_float(((const uint16_t *)base)[i]);
-    return oracle_e4m3_to_float(((const uint8_t *)base)[i]);
+/* All 256 e4m3 codes decoded once with oracle_e4m3_to_float, when the
+ * library is loaded (before any thread can read the table). */
+static float e4m3_table[256];
+__attribute__((constructor)) static void init_e4m3_table(void) {
+    for (int c = 0; c < 256; ++c) e4m3_table[c] = oracle_e4m3_to_float((uint8_t)c);
 }
 
-static double kv_elem(const oracle_problem *p, int64_t prow, int d) {
-    int64_t i = prow * D_QK + d;
-    if (p->kv_dtype == ORACLE_BF16) return (double)oracle_bf16_to_float(((const uint16_t *)p->kv)[i]);
-    return (double)oracle_e4m3_to_float(((const uint8_t *)p->kv)[i]) * (double)p->kv_scale[prow];
+static float idx_elem(const void *base, int dtype, int64_t i) {
+    if (dtype == ORACLE_BF16) return oracle_bf16_to_float(((const uint16_t *)base)[i]);
+    return e4m3_table[((const uint8_t *)base)[i]];
+}
+
+/* Row `prow` of the latent cache as fp64 values (FP8: e4m3 value * token scale). */
+static void kv_row(const oracle_problem *p, int64_t prow, double *dst) {
+    for (int d = 0; d < D_QK; ++d) {
+        int64_t i = prow * D_QK + d;
+        if (p->kv_dtype == ORACLE_BF16) dst[d] = (double)oracle_bf16_to_float(((const uint16_t *)p->kv)[i]);
+        else dst[d] = (double)e4m3_table[((const uint8_t *)p->kv)[i]] * (double)p->kv_scale[prow];
+    }
 }
 
 /* Step 1: indexer scores of query `row` against keys 0..pos (fp32). */
@@ -130,23 +140,26 @@ int oracle_scores(const oracle_problem *p, int64_t row, float *scores) {
     row_place(p, row, &seq, &pos);
     const int H = p->h_idx, D = p->d_idx;
     float *qf = (float *)malloc(sizeof(float) * H * D);
+    float *kf = (float *)malloc(sizeof(float) * D);
     for (int i = 0; i < H * D; ++i) qf[i] = idx_elem(p->q_idx, p->idx_dtype, row * (int64_t)H * D + i);
     const float *wr = p->w + row * (int64_t)H;
     int bad = 0;
     for (int64_t s = 0; s <= pos; ++s) {
         int64_t pr = pool_row(p, seq, s);
         if (pr < 0) { bad = 1; scores[s] = 0.0f; continue; }
+        for (int d = 0; d < D; ++d) kf[d] = idx_elem(p->k_idx, p->idx_dtype, pr * D + d);
         float total = 0.0f;
         for (int h = 0; h < H; ++h) {
             float dot = 0.0f;
             for (int d = 0; d < D; ++d)
-                dot += qf[h * D + d] * idx_elem(p->k_idx, p->idx_dtype, pr * D + d);
+                dot += qf[h * D + d] * kf[d];
             float relu = dot > 0.0f ? dot : 0.0f;
             total += wr[h] * relu;
         }
         if (p->k_idx_scale) total *= p->k_idx_scale[pr];
         scores[s] = total;
     }
+    free(kf);
     free(qf);
     return bad;
 }
@@ -197,32 +210,53 @@ int oracle_attend(const oracle_problem *p, int64_t row, const int32_t *idx, int3
         prow[j] = pool_row(p, seq, idx[j]);
         if (prow[j] < 0) bad = 1;
     }
-    double *logit = (double *)malloc(sizeof(double) * (n_idx > 0 ? n_idx : 1));
-    double *qd = (double *)malloc(sizeof(double) * D_QK);
+    const int64_t n = n_idx > 0 ? n_idx : 1;
+    double *logit = (double *)malloc(sizeof(double) * H * n);   /* [H][n_idx] */
+    double *qd = (double *)malloc(sizeof(double) * H * D_QK);
+    double *kr = (double *)malloc(sizeof(double) * D_QK);
+    double *m = (double *)malloc(sizeof(double) * H);
+    double *denom = (double *)malloc(sizeof(double) * H);
     for (int h = 0; h < H; ++h) {
         const uint16_t *qr = p->q + (row * (int64_t)H + h) * D_QK;
-        for (int d = 0; d < D_QK; ++d) qd[d] = (double)oracle_bf16_to_float(qr[d]);
-        double m = -INFINITY;
-        for (int j = 0; j < n_idx; ++j) {
-            if (prow[j] < 0) continue;
+        for (int d = 0; d < D_QK; ++d) qd[h * D_QK + d] = (double)oracle_bf16_to_float(qr[d]);
+        m[h] = -INFINITY;
+        denom[h] = 0.0;
+    }
+    /* logits: l[h][j] = sm_scale * sum_d q[h][d] K[j][d] (d ascending) */
+    for (int j = 0; j < n_idx; ++j) {
+        if (prow[j] < 0) continue;
+        kv_row(p, prow[j], kr);
+        for (int h = 0; h < H; ++h) {
             double acc = 0.0;
-            for (int d = 0; d < D_QK; ++d) acc += qd[d] * kv_elem(p, prow[j], d);
-            logit[j] = p->sm_scale * acc;
-            if (logit[j] > m) m = logit[j];
+            const double *q = qd + h * D_QK;
+            for (int d = 0; d < D_QK; ++d) acc += q[d] * kr[d];
+            double l = p->sm_scale * acc;
+            logit[h * n + j] = l;
+            if (l > m[h]) m[h] = l;
         }
-        double denom = 0.0;
+    }
+    for (int h = 0; h < H; ++h)
         for (int j = 0; j < n_idx; ++j)
-            if (prow[j] >= 0) denom += exp(logit[j] - m);
+            if (prow[j] >= 0) denom[h] += exp(logit[h * n + j] - m[h]);
+    for (int h = 0; h < H; ++h) {
         double *o = out + (int64_t)h * D_V;
         for (int d = 0; d < D_V; ++d) o[d] = 0.0;
-        for (int j = 0; j < n_idx; ++j) {
-            double pj = prow[j] >= 0 ? exp(logit[j] - m) / denom : 0.0;
+    }
+    /* out[h] = sum_j p[h][j] V[j] (j ascending for every head) */
+    for (int j = 0; j < n_idx; ++j) {
+        if (prow[j] >= 0) kv_row(p, prow[j], kr);
+        for (int h = 0; h < H; ++h) {
+            double pj = prow[j] >= 0 ? exp(logit[h * n + j] - m[h]) / denom[h] : 0.0;
             if (probs) probs[(int64_t)h * n_idx + j] = pj;
             if (prow[j] < 0) continue;
-            for (int d = 0; d < D_V; ++d) o[d] += pj * kv_elem(p, prow[j], d);
+            double *o = out + (int64_t)h * D_V;
+            for (int d = 0; d < D_V; ++d) o[d] += pj * kr[d];
         }
-        lse[h] = denom > 0.0 ? m + log(denom) : -INFINITY;
     }
+    for (int h = 0; h < H; ++h) lse[h] = denom[h] > 0.0 ? m[h] + log(denom[h]) : -INFINITY;
+    free(kr);
+    free(m);
+    free(denom);
     free(qd);
     free(logit);
     free(prow);

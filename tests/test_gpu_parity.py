@@ -1,0 +1,201 @@
+"""CUDA path vs the CPU oracle on seeded inputs (needs a GB300).
+
+Index sets must match bit for bit (integer-valued indexer inputs make every
+score exact); attention outputs must match within the tolerances fixed for
+the layer step. Small workloads are compared row by row in full; the large
+ones at their full sizes on stratified samples of rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import indexer_top_sparse_score_gb300 as smla
+import oracle
+from indexer_top_sparse_score_gb300 import workloads as wl
+from tests.gpu_common import (compare_idx, compare_out, host_cache, run_prefill, sampled_oracle,
+                              stratified_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    smla.build()
+    oracle.build()
+    smla.lib()
+
+
+def _host(t):
+    return t.cpu().numpy()
+
+
+def test_tiny_prefill_full():
+    """Workload 1 (T=1024, 16 heads, 4x64 BF16 indexer, top-256) in full."""
+    spec = wl.SPECS["tiny"]
+    prob = wl.make(spec, "cpu")
+    dev = prob.to("cuda")
+    idx, out, lse = run_prefill(dev)
+    ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(np.arange(spec.n_tokens))
+    assert not bad.any()
+    compare_idx(_host(idx), ridx)
+    compare_out(_host(out.float()), rout, _host(lse), rlse, spec.kv_dtype)
+
+
+def test_indexer_scores_and_sets_group_mode():
+    spec = wl.scaled(wl.SPECS["tiny"], n_tokens=777, prefix_len=333, shuffled=True)
+    prob = wl.make(spec, "cpu")
+    dev = prob.to("cuda")
+    L = spec.prefix_len + spec.n_tokens
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    gidx, gsc, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx,
+                                      dev.w, spec.topk, want_scores=True)
+    assert smla.read_status(ws)[0] == 0
+    o = oracle.Oracle(prob)
+    ridx, rsc, *_ = o.rows(np.arange(spec.n_tokens), attend=False)
+    compare_idx(_host(gidx), ridx)
+    g_i, g_s = _host(gidx), _host(gsc)
+    for r in range(0, spec.n_tokens, 37):
+        full = o.scores(r)
+        ok = g_i[r] >= 0
+        assert np.array_equal(g_s[r][ok], full[g_i[r][ok]])
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_prefill_ragged_prefix_shuffled(kv_dtype):
+    """64 heads, 32x128 FP8 indexer, top-2048; T not a multiple of the CTA's
+    token group, a cached prefix, shuffled pages; rows sampled around t = k."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=3001, prefix_len=1500, shuffled=True,
+                     kv_dtype=kv_dtype)
+    dev = wl.make(spec, "cuda")
+    idx, out, lse = run_prefill(dev)
+    rows = stratified_rows(spec.prefix_len, spec.n_tokens, spec.topk, n_random=20)
+    ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
+    r = torch.as_tensor(rows, device="cuda")
+    compare_idx(_host(idx[r]), ridx)
+    compare_out(_host(out[r].float()), rout, _host(lse[r]), rlse, kv_dtype)
+
+
+def test_prefill16k_full_size_sampled():
+    """Workload 2 at its full size (the benchmarked configuration), sampled rows."""
+    spec = wl.SPECS["prefill16k"]
+    dev = wl.make(spec, "cuda")
+    idx, out, lse = run_prefill(dev)
+    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=(4095, 8191, 12287), n_random=16)
+    ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
+    r = torch.as_tensor(rows, device="cuda")
+    compare_idx(_host(idx[r]), ridx)
+    compare_out(_host(out[r].float()), rout, _host(lse[r]), rlse, spec.kv_dtype)
+    # every row: valid entries first, unique, causal
+    ih = _host(idx)
+    for t in range(0, spec.n_tokens, 997):
+        n = min(spec.topk, t + 1)
+        v = ih[t, :n]
+        assert (v >= 0).all() and (v <= t).all() and len(np.unique(v)) == n
+        assert (ih[t, n:] == -1).all()
+
+
+def test_prefill128k_chunked_sampled():
+    """Workload 3: 131072 tokens, FP8 KV, in 8192-token chunks against the growing cache."""
+    spec = wl.SPECS["prefill128k"]
+    dev = wl.make(spec, "cuda")
+    idx, out, lse = run_prefill(dev, chunk=spec.chunk)
+    edges = [c * spec.chunk + d for c in (1, 7, 15) for d in (-1, 0, 1)]
+    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=edges, n_random=6)
+    ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
+    r = torch.as_tensor(rows, device="cuda")
+    compare_idx(_host(idx[r]), ridx)
+    compare_out(_host(out[r].float()), rout, _host(lse[r]), rlse, spec.kv_dtype)
+
+
+def test_prefix1m_sampled():
+    """Workload 5: 8192 new tokens after a 1,048,576-token prefix, paged and shuffled."""
+    spec = wl.SPECS["prefix1m"]
+    dev = wl.make(spec, "cuda")
+    idx, out, lse = run_prefill(dev)
+    rows = np.array([0, 1, 4095, 8190, 8191, 1234, 5678], dtype=np.int64)
+    ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
+    r = torch.as_tensor(rows, device="cuda")
+    compare_idx(_host(idx[r]), ridx)
+    compare_out(_host(out[r].float()), rout, _host(lse[r]), rlse, spec.kv_dtype)
+
+
+def test_decode_mtp_full():
+    """Workload 4: 64 requests x 2 MTP tokens, contexts 8K-128K, shuffled paged pool; every row."""
+    spec = wl.SPECS["decode"]
+    dev = wl.make(spec, "cuda")
+    rows = spec.n_seqs * spec.q_per_seq
+    max_len = int(dev.seq_lens.max())
+    idx = torch.empty((rows, spec.topk), dtype=torch.int32, device="cuda")
+    out, lse, _, ws = smla.sparse_mla_decode(dev.cache, dev.page_table, dev.seq_lens, max_len, spec.q_per_seq,
+                                             dev.q, dev.q_idx, dev.w, spec.topk, spec.sm_scale, out_idx=idx)
+    assert smla.read_status(ws)[0] == 0
+    prob = dev.to("cpu")
+    ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(np.arange(rows))
+    assert not bad.any()
+    compare_idx(_host(idx), ridx)
+    compare_out(_host(out.float()), rout, _host(lse), rlse, spec.kv_dtype)
+
+
+def test_decode_small_batch_single_token():
+    """Plain decode (one query per request), BF16 cache, short contexts below k."""
+    spec = wl.scaled(wl.SPECS["decode"], n_seqs=5, q_per_seq=1, len_min=100, len_max=9000, kv_dtype="bf16",
+                     seed=77)
+    dev = wl.make(spec, "cuda")
+    max_len = int(dev.seq_lens.max())
+    idx = torch.empty((spec.n_seqs, spec.topk), dtype=torch.int32, device="cuda")
+    out, lse, _, ws = smla.sparse_mla_decode(dev.cache, dev.page_table, dev.seq_lens, max_len, 1, dev.q,
+                                             dev.q_idx, dev.w, spec.topk, spec.sm_scale, out_idx=idx)
+    assert smla.read_status(ws)[0] == 0
+    prob = dev.to("cpu")
+    ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(np.arange(spec.n_seqs))
+    compare_idx(_host(idx), ridx)
+    compare_out(_host(out.float()), rout, _host(lse), rlse, "bf16")
+
+
+def test_sparse_mla_given_indices_with_holes():
+    """Caller-given index lists with -1 holes, duplicates-free random keys, FP8 cache."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=300, prefix_len=5000, kv_dtype="fp8", topk=512,
+                     shuffled=True)
+    dev = wl.make(spec, "cuda")
+    g = torch.Generator().manual_seed(5)
+    T, k = spec.n_tokens, spec.topk
+    idx = torch.empty((T, k), dtype=torch.int32)
+    for t in range(T):
+        pos = spec.prefix_len + t
+        perm = torch.randperm(pos + 1, generator=g)[:k].to(torch.int32)
+        holes = torch.rand(k, generator=g) < 0.1
+        perm[holes] = -1
+        idx[t] = perm
+    out, lse, ws = smla.sparse_mla_fwd(dev.cache, dev.page_table, dev.q, idx.cuda(), spec.sm_scale,
+                                       prefix_len=spec.prefix_len)
+    assert smla.read_status(ws)[0] == 0
+    prob = dev.to("cpu")
+    o = oracle.Oracle(prob)
+    rows = np.arange(0, T, 7)
+    rout, rlse = o.attend_rows(rows, idx.numpy()[rows])
+    compare_out(_host(out.float())[rows], rout, _host(lse)[rows], rlse, "fp8")
+
+
+def test_out_of_range_page_is_reported_not_faulted():
+    """A page id outside the pool is skipped on the device and reported by read_status."""
+    spec = wl.scaled(wl.SPECS["tiny"], n_tokens=200, prefix_len=300)
+    dev = wl.make(spec, "cuda")
+    pt = dev.page_table.clone()
+    pt[2] = dev.cache.num_pages + 5
+    out, lse, _, ws = smla.sparse_mla_prefill(dev.cache, pt, spec.prefix_len, dev.q, dev.q_idx, dev.w,
+                                              spec.topk, spec.sm_scale)
+    rc, bits = smla.read_status(ws)
+    assert rc == 5 and bits & 1
+    # the same call with the good table is clean again (the status word is reset per call)
+    smla.sparse_mla_prefill(dev.cache, dev.page_table, spec.prefix_len, dev.q, dev.q_idx, dev.w, spec.topk,
+                            spec.sm_scale, ws=ws)
+    assert smla.read_status(ws)[0] == 0
+
+
+def test_repeat_calls_same_sets():
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=2500, prefix_len=0)
+    dev = wl.make(spec, "cuda")
+    a, oa, la = run_prefill(dev)
+    b, ob, lb = run_prefill(dev)
+    assert torch.equal(torch.sort(a, dim=1).values, torch.sort(b, dim=1).values)
+    assert (oa.float() - ob.float()).abs().max().item() < 1e-2
