@@ -68,7 +68,8 @@ typedef enum smla_dtype {
  *   k_idx       [num_pages][page_size][d_idx] idx_dtype: indexer keys.
  *   k_idx_scale [num_pages][page_size] fp32 positive per-key indexer scale, or
  *               NULL for 1 (footnote 3's 132-byte key = 128 FP8 + 4-byte scale).
- * page_size must be 64. d_idx * sizeof(idx_dtype) must be 128 or 256 bytes. */
+ * page_size must be 64. An indexer row must be 128 bytes: d_idx = 128 for
+ * e4m3 keys, d_idx = 64 for bf16 keys. */
 typedef struct smla_paged_cache {
   const void* kv;
   const float* kv_scale;
@@ -125,8 +126,10 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
  *   out   [rows][n_heads][512] bf16 attention output (normalised).
  *   lse   [rows][n_heads] fp32 natural-log sum of exp(sm_scale * q.K), or NULL.
  *         A row with no usable entry gets out = 0 and lse = -inf.
- * FP8 caches are computed with f16 tensor-core operands: |q| and the
- * dequantised cache values must stay below 65504.
+ * The attention MMAs run on f16 operands (q, the cache rows and the softmax
+ * probabilities are widened to f16; e4m3 widens exactly, bf16 exactly inside
+ * the f16 range), so |q| and |cache values| must stay below 65504; a query
+ * value beyond it is reported by smla_read_status as SMLA_ERR_UNSUPPORTED.
  * Supported: n_heads in {16, 64} (16 and 64 query heads of the configurations),
  * topk <= 2048.
  * ------------------------------------------------------------------------- */
@@ -173,7 +176,8 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
  * smla_read_status — waits for `stream`, then reads the device status word of
  * `workspace` written by the calls that used it: SMLA_OK, SMLA_ERR_DEVICE_BOUNDS
  * or SMLA_ERR_TIMEOUT (the latter wins); the raw bit mask goes to *bits if
- * non-NULL. Each entry point clears the word when it starts.
+ * non-NULL; SMLA_ERR_UNSUPPORTED if a value was outside the supported range.
+ * Each entry point clears the word when it starts.
  * ------------------------------------------------------------------------- */
 int smla_read_status(const void* workspace, void* stream, uint32_t* bits);
 

@@ -9,9 +9,10 @@
 // One CTA per SM (persistent); query rows are handed out in head/tail pairs
 // (cheap causal rows with expensive ones). For each row the 2048 selected
 // rows stream through in blocks of 64:
-//   warps 8-11  gather producers: resolve key -> page -> pool row and copy the
-//               row into a 128B-swizzled shared tile (cp.async for BF16; FP8
-//               rows are loaded, widened e4m3 -> f16 and stored), 2 stages;
+//   warps 8-15  gather producers: resolve key -> page -> pool row, load the
+//               row, widen it to f16 (bf16 -> f16 or e4m3 -> f16) and store it
+//               into a 128B-swizzled shared tile, 2 stages; they also widen
+//               the query to f16 once per query row;
 //   warp 0      MMA issuer:  S[64 heads x 64 rows] = Q . K^T   (tcgen05,
 //               M=64, K=576) into one of two TMEM S buffers, and
 //               O^T[512 x H] += V^T . P^T  (M=128 per 128-dim slice of V, the
@@ -20,9 +21,11 @@
 //               in the log2 domain with a lazy rescale (O is only rescaled
 //               when a head's running max grows by more than 2^8), P to
 //               shared memory; finally O^T from TMEM, normalised, to HBM.
-//   warp 1      TMA load of the BF16 query tile (BF16 caches).
-// The FP8 path computes in f16 (e4m3 -> f16 is exact): the per-token scale
-// multiplies the logit of its row and its probability before PV.
+// All MMA operands are f16: e4m3 -> f16 is exact and bf16 -> f16 is exact in
+// the f16 normal range, and f16 gives the probabilities 11 significant bits
+// (bf16 would give 8, which alone costs ~1e-3 relative output error). For
+// FP8 caches the per-token scale multiplies the logit of its row and its
+// probability before PV.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -40,7 +43,8 @@ constexpr int kChunks = kDqk / 64;           // 9 chunks of 64 values
 constexpr int kChunkBytes = kBlk * 128;      // 8 KB
 constexpr int kTileBytes = kChunks * kChunkBytes;  // 72 KB per stage / for Q
 constexpr int kPBytes = 64 * 128;            // P^T: 64 head rows x 64 values
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr int kProducers = 256;          // warps 8-15
 constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -119,6 +123,18 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// bf16 pair -> f16 pair (exact for values inside the f16 normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// 16-byte global load that bypasses L1 (each row is read once per block)
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
@@ -146,7 +162,7 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) 
 
 template <int H>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaParams p) {
+    mla_kernel(const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_tile = smem;
   uint8_t* stage = smem + kTileBytes;  // 2 stages
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&M.kv_full[i], 128);
+      mbar_init(&M.kv_full[i], kProducers);
       mbar_init(&M.kv_empty[i], 1);
       mbar_init(&M.s_full[i], 1);
       mbar_init(&M.s_empty[i], 4);
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = M.tmem_slot;
   volatile int* abort_v = &M.abort_flag;
-  const uint32_t fmt = p.fp8 ? kFmtF16 : kFmtBF16;
+  const uint32_t fmt = kFmtF16;  // every operand is widened to f16 (exact for e4m3 and in-range bf16)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA
@@ -253,27 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tok;
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- Q (BF16 via TMA)
-    if (lane == 0 && !p.fp8) {
-      prefetch_tensormap(&map_q);
-      uint32_t tok = 0;
-      for (int k = 0;; ++k) {
-        int row;
-        const int r = next_row(p.n_rows, k, row);
-        if (r < 0) break;
-        if (r == 0) continue;
-        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
-        mbar_arrive_expect_tx(&M.q_full, H * kDqk * 2);
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(q_tile + c * kChunkBytes, &map_q, &M.q_full, c * 64, row * H);
-        ++tok;
-      }
-    }
   } else if (warp >= 8) {
     // ---------------------------------------------------------------- gather producers
-    const int tid = threadIdx.x - 256;  // 0..127
-    const int j = tid >> 1, half = tid & 1;
+    const int tid = threadIdx.x - 256;  // 0..255: four threads per selected row
+    const int j = tid >> 2, qt = tid & 3;
     uint32_t g = 0, tok = 0;
     for (int k = 0;; ++k) {
       int row;
@@ -281,21 +280,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r < 0) break;
       if (r == 0) continue;
       const RowInfo ri = row_info(p, row);
-      if (p.fp8) {
+      {
         // widen the BF16 query to f16 into the swizzled Q tile
         if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
         const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
         bool over = false;
-        for (int pc = tid; pc < H * 72; pc += 128) {
+        for (int pc = tid; pc < H * 72; pc += kProducers) {
           const int h = pc / 72, pp = pc - h * 72;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qr + h * kDqk + pp * 8));
+          const uint4 v = ldg_stream(qr + h * kDqk + pp * 8);
           const uint32_t in[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float a = __uint_as_float(in[u] << 16), b = __uint_as_float(in[u] & 0xFFFF0000u);
-            over |= fabsf(a) > 65504.0f || fabsf(b) > 65504.0f;
-            o[u] = pack_f16(a, b);
+            over |= ((in[u] & 0x7FFFu) > 0x477Fu) || ((in[u] & 0x7FFF0000u) > 0x477F0000u);
+            o[u] = bf16x2_to_f16x2(in[u]);
           }
           const int c = pp >> 3, qq = pp & 7;
           *reinterpret_cast<uint4*>(q_tile + c * kChunkBytes + h * 128 + ((qq ^ (h & 7)) << 4)) =
@@ -303,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (over) set_status(p.status, kStatusOverflow);
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
+        named_bar_sync(2, kProducers);
         if (tid == 0) mbar_arrive(&M.q_full);
       }
       const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
@@ -323,35 +321,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             else set_status(p.status, kStatusBounds);
           }
         }
-        uint8_t* st = stage + s * kTileBytes;
-        if (half == 0) {
+        uint8_t* rowp = stage + s * kTileBytes + j * 128;
+        if (qt == 0) {
           const float ks = (p.fp8 && prow >= 0) ? __ldg(p.kv_scale + prow) : 1.0f;
           M.colscale[s][j] = ks * p.scale_log2;
           M.pscale[s][j] = ks;
           M.valid[s][j] = prow >= 0;
         }
         if (!p.fp8) {
-          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * (kDqk * 2);
-          const uint32_t sbase = smem_u32(st);
-#pragma unroll 4
-          for (int u = 0; u < 36; ++u) {
-            const int pc = half * 36 + u;
-            const int c = pc >> 3, qq = pc & 7;
-            cp_async_16(sbase + c * kChunkBytes + j * 128 + ((qq ^ (j & 7)) << 4), src + pc * 16,
-                        prow >= 0 ? 16u : 0u);
-          }
-          cp_async_commit();
-          cp_async_wait<0>();
-        } else {
-          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
+          // 72 pieces of 8 BF16 per row, 18 per thread; widened to f16 in place of layout
+          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv) + (prow >= 0 ? prow : 0) * kDqk;
           uint4 v[18];
 #pragma unroll
           for (int u = 0; u < 18; ++u)
-            v[u] = prow >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (half * 18 + u) * 16))
-                             : make_uint4(0, 0, 0, 0);
+            v[u] = prow >= 0 ? ldg_stream(src + (qt * 18 + u) * 8) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int u = 0; u < 18; ++u) {
-            const int p8 = half * 18 + u;  // 16 e4m3 values = 32 bytes of f16
+            const int pc = qt * 18 + u;
+            const int c = pc >> 3, qq = pc & 7;
+            *reinterpret_cast<uint4*>(rowp + c * kChunkBytes + ((qq ^ (j & 7)) << 4)) =
+                make_uint4(bf16x2_to_f16x2(v[u].x), bf16x2_to_f16x2(v[u].y), bf16x2_to_f16x2(v[u].z),
+                           bf16x2_to_f16x2(v[u].w));
+          }
+        } else {
+          // 36 pieces of 16 e4m3 per row, 9 per thread; each widens to two f16 pieces
+          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
+          uint4 v[9];
+#pragma unroll
+          for (int u = 0; u < 9; ++u)
+            v[u] = prow >= 0 ? ldg_stream(src + (qt * 9 + u) * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 9; ++u) {
+            const int p8 = qt * 9 + u;
             const int c = p8 >> 2, qq = (p8 & 3) * 2;
             const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
             uint32_t o[8];
@@ -360,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[2 * t] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] & 0xFFFFu));
               o[2 * t + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] >> 16));
             }
-            uint8_t* rowp = st + c * kChunkBytes + j * 128;
-            *reinterpret_cast<uint4*>(rowp + (((qq) ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(rowp + (((qq + 1) ^ (j & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            uint8_t* cp = rowp + c * kChunkBytes;
+            *reinterpret_cast<uint4*>(cp + ((qq ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(cp + (((qq + 1) ^ (j & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
         fence_proxy_async_smem();
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = exp2f(x[i] - mref), p1 = exp2f(x[i + 1] - mref);
           sum += p0 + p1;
           const float a = p0 * M.pscale[s][col], c = p1 * M.pscale[s][col + 1];
-          pk[i >> 1] = p.fp8 ? pack_f16(a, c) : pack_bf16(a, c);
+          pk[i >> 1] = pack_f16(a, c);
         }
         l += sum;
         uint8_t* prow = p_tile + h * 128;
@@ -511,10 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int H>
 int launch_t(const MlaLaunch& L, const MlaParams& prm) {
-  CUtensorMap map_q;
-  if (!encode_2d(&map_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L.q, kDqk, static_cast<uint64_t>(prm.n_rows) * H,
-                 kDqk * 2, 64, H, CU_TENSOR_MAP_SWIZZLE_128B))
-    return SMLA_ERR_CUDA;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(mla_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -523,7 +520,7 @@ int launch_t(const MlaLaunch& L, const MlaParams& prm) {
     attr_done = true;
   }
   const int grid = std::max(1, std::min(num_sms(), (prm.n_rows + 1) / 2));
-  mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(map_q, prm);
+  mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }

@@ -179,6 +179,27 @@ class Oracle:
         return out, lse
 
 
+def prefill_rows(prob, rows, cache_host=None, n_threads: int = 0):
+    """Full step for chosen rows of a prefill Problem whose tensors may live on a GPU.
+
+    Each chosen row becomes a one-token sequence of length pos+1 that shares the
+    prefill's page table, so only the chosen q / q_I / w rows are copied to the
+    host. Returns (idx, scores, out, lse, threads used, bad flags)."""
+    from indexer_top_sparse_score_gb300 import workloads as wl
+    spec = prob.spec
+    rows = np.asarray(rows, dtype=np.int64)
+    cache = cache_host if cache_host is not None else prob.cache.to("cpu")
+    n = len(rows)
+    pos = prob.prefix_len + rows
+    pt = prob.page_table.cpu().to(torch.int32)
+    pts = pt[None, :].expand(n, -1).contiguous()
+    r = torch.as_tensor(rows).to(prob.q.device)
+    sub = wl.Problem(wl.scaled(spec, kind="decode", n_seqs=n, q_per_seq=1), cache, pts,
+                     prob.q[r].cpu().contiguous(), prob.q_idx[r].cpu().contiguous(),
+                     prob.w[r].cpu().contiguous(), torch.as_tensor(pos + 1, dtype=torch.int32), 0, 0)
+    return Oracle(sub).rows(np.arange(n), n_threads=n_threads)
+
+
 def select_topk(scores: np.ndarray, k: int):
     """Causal top-k of one score row (ascending indices, -1 padded)."""
     scores = np.ascontiguousarray(scores, dtype=np.float32)

@@ -76,26 +76,6 @@ def host_cache(dev):
 
 
 def sampled_oracle(dev, rows, cache_host=None, n_threads=0):
-    """Oracle on chosen prefill rows of a device Problem.
-
-    Each chosen row becomes a one-token sequence of length pos+1 that shares the
-    prefill's page table, so only its own q / q_I / w rows are copied to the host.
-    Returns (idx, scores, out, lse, threads)."""
-    from indexer_top_sparse_score_gb300 import workloads as wl
-    spec = dev.spec
-    rows = np.asarray(rows, dtype=np.int64)
-    cache = cache_host if cache_host is not None else host_cache(dev)
-    n = len(rows)
-    pos = dev.prefix_len + rows
-    pt = dev.page_table.cpu().to(torch.int32)
-    pts = pt[None, :].expand(n, -1).contiguous()
-    r = torch.as_tensor(rows)
-    sub = wl.Problem(wl.scaled(spec, kind="decode", n_seqs=n, q_per_seq=1), cache, pts,
-                     dev.q[r.to(dev.q.device)].cpu().contiguous(),
-                     dev.q_idx[r.to(dev.q.device)].cpu().contiguous(),
-                     dev.w[r.to(dev.q.device)].cpu().contiguous(),
-                     torch.as_tensor(pos + 1, dtype=torch.int32), 0, 0)
-    o = oracle.Oracle(sub)
-    idx, sc, out, lse, used, bad = o.rows(np.arange(n), n_threads=n_threads)
+    idx, sc, out, lse, used, bad = oracle.prefill_rows(dev, rows, cache_host, n_threads)
     assert not bad.any()
     return idx, sc, out, lse, used
