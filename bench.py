@@ -182,6 +182,45 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_e2e(args, spec, dev, out, lse, stream, world):
+    """Same step through smla_sparse_mla_prefill with host inputs/outputs: every
+    step copies q, q_I and w from pinned host memory and reads out and lse back."""
+    T, H, k, P = spec.n_tokens, spec.n_heads, spec.topk, spec.prefix_len
+    q_h = dev.q.cpu().pin_memory()
+    qi_h = dev.q_idx.cpu().pin_memory()
+    w_h = dev.w.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, qi_d, w_d = torch.empty_like(dev.q), torch.empty_like(dev.q_idx), torch.empty_like(dev.w)
+    ws_p = smla.workspace(smla.prefill_workspace_bytes(P, T, H, spec.h_idx, k))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        qi_d.copy_(qi_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        smla.sparse_mla_prefill(dev.cache, dev.page_table, P, q_d, qi_d, w_d, k, spec.sm_scale, out=out,
+                                lse=lse, ws=ws_p)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    e_s.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    assert smla.read_status(ws_p)[0] == 0
+    ms_e2e = reduce_max(e_s.elapsed_time(e_e) / n_e2e, world)
+    h2d = q_h.numel() * q_h.element_size() + qi_h.numel() * qi_h.element_size() + w_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return ms_e2e, h2d, d2h
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -189,7 +228,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--workload", default=WORKLOAD, choices=["prefill16k"],
+                    help="benchmarked workload (the 16,384-token prefill)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: use this many query tokens instead of the workload's")
+    ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the host-buffer pass")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_setup(args.gpus)
@@ -201,7 +245,9 @@ def main():
         smla.build()
     barrier(world)
     L = smla.lib()
-    spec = wl.SPECS[WORKLOAD]
+    spec = wl.SPECS[args.workload]
+    if args.tokens:
+        spec = wl.scaled(spec, n_tokens=args.tokens)
     dev = wl.make(spec, "cuda")
     T, H, k = spec.n_tokens, spec.n_heads, spec.topk
     P = spec.prefix_len
@@ -253,37 +299,10 @@ def main():
     value = world * T / (ms_step_max / 1e3)
 
     # ------------------------------------------------------------------ e2e through host buffers
-    q_h = dev.q.cpu().pin_memory()
-    qi_h = dev.q_idx.cpu().pin_memory()
-    w_h = dev.w.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, qi_d, w_d = torch.empty_like(dev.q), torch.empty_like(dev.q_idx), torch.empty_like(dev.w)
-    ws_p = smla.workspace(smla.prefill_workspace_bytes(P, T, H, spec.h_idx, k))
-
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        qi_d.copy_(qi_h, non_blocking=True)
-        w_d.copy_(w_h, non_blocking=True)
-        smla.sparse_mla_prefill(dev.cache, dev.page_table, P, q_d, qi_d, w_d, k, spec.sm_scale, out=out,
-                                lse=lse, ws=ws_p)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, min(args.steps, 10))
-    e_s.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    e_e.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = reduce_max(e_s.elapsed_time(e_e) / n_e2e, world)
-    h2d = q_h.numel() * q_h.element_size() + qi_h.numel() * qi_h.element_size() + w_h.numel() * 4
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    if args.no_e2e:
+        ms_e2e, h2d, d2h = float("nan"), 0, 0
+    else:
+        ms_e2e, h2d, d2h = run_e2e(args, spec, dev, out, lse, stream, world)
 
     # ------------------------------------------------------------------ roofline
     pk = peaks()
@@ -317,7 +336,8 @@ def main():
                    "indexer_dtype": "fp8(e4m3) operands, fp32 accumulate", "parallelism": f"replicas x{world}",
                    "l2": "256 MB buffer written between timed steps", "wall_s_timed_region": wall},
         "roofline": roof, "kernels": kernels,
-        "e2e": {"value": world * T / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": world * T / (ms_e2e / 1e3) if ms_e2e == ms_e2e else None, "unit": UNIT,
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse"},
         "gpu_launches": 2 * args.steps,

@@ -205,35 +205,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // The whole warp walks the items; each lane fetches one page id of the
+    // next 32 pages (16 tiles) so page-table latency is paid once per 16
+    // tiles, and lane 0 issues the copies.
     if (lane == 0) {
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_q);
-      uint32_t sc = 0, bi = 0;
-      for (int k = 0;; ++k) {
-        Item it;
-        const int r = next_item(p, k, it);
-        if (r < 0) break;
-        if (r == 0 || it.trivial) continue;
-        if (!mbar_wait(b_empty, (bi & 1) ^ 1, abort_v, p.status)) break;
-        ++bi;
-        mbar_arrive_expect_tx(b_full, N * kIdxRowBytes);
-        tma_load_2d(b_tile, &map_q, b_full, 0, it.row0 * HI);
-        const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
-        bool ok = true;
-        for (int t = it.t0; t < it.t1 && ok; ++t, ++sc) {
-          const int s = sc % kStages;
-          if (!mbar_wait(&a_empty[s], ((sc / kStages) & 1) ^ 1, abort_v, p.status)) {
-            ok = false;
-            break;
-          }
-          const bool has1 = (2 * t + 1) * kPage < it.key_hi;
-          const int pg0 = page_of(p, pt, 2 * t);
-          const int pg1 = has1 ? page_of(p, pt, 2 * t + 1) : 0;
-          mbar_arrive_expect_tx(&a_full[s], has1 ? kStageBytes : kStageBytes / 2);
-          tma_load_2d(a_tiles + s * kStageBytes, &map_k, &a_full[s], 0, pg0 * kPage);
-          if (has1) tma_load_2d(a_tiles + s * kStageBytes + kStageBytes / 2, &map_k, &a_full[s], 0, pg1 * kPage);
+    }
+    uint32_t sc = 0, bi = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Item it;
+      const int r = next_item(p, k, it);
+      if (r < 0) break;
+      if (r == 0 || it.trivial) continue;
+      if (lane == 0) {
+        ok = mbar_wait(b_empty, (bi & 1) ^ 1, abort_v, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(b_full, N * kIdxRowBytes);
+          tma_load_2d(b_tile, &map_q, b_full, 0, it.row0 * HI);
         }
-        if (!ok) break;
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      ++bi;
+      const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
+      for (int tw = it.t0; tw < it.t1 && ok; tw += 16) {
+        const int lp = 2 * tw + lane;
+        const int pg = lp * kPage < it.key_hi ? page_of(p, pt, lp) : 0;
+        const int tend = min(tw + 16, it.t1);
+        for (int t = tw; t < tend; ++t, ++sc) {
+          const int pg0 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (t - tw));
+          const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (t - tw) + 1);
+          if (lane == 0) {
+            const int s = sc % kStages;
+            ok = mbar_wait(&a_empty[s], ((sc / kStages) & 1) ^ 1, abort_v, p.status);
+            if (ok) {
+              const bool has1 = (2 * t + 1) * kPage < it.key_hi;
+              mbar_arrive_expect_tx(&a_full[s], has1 ? kStageBytes : kStageBytes / 2);
+              tma_load_2d(a_tiles + s * kStageBytes, &map_k, &a_full[s], 0, pg0 * kPage);
+              if (has1)
+                tma_load_2d(a_tiles + s * kStageBytes + kStageBytes / 2, &map_k, &a_full[s], 0, pg1 * kPage);
+            }
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
+        }
       }
     }
   } else if (warp == 1) {

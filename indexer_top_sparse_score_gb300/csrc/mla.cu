@@ -104,6 +104,18 @@ __device__ __forceinline__ RowInfo row_info(const MlaParams& p, int row) {
   return r;
 }
 
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
   uint32_t r;
   asm volatile(
@@ -211,89 +223,178 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA
+    // One thread issues QK^T and PV for the CTA's rows in whatever order their
+    // inputs become ready: QK(b) needs the gathered tile and a free S buffer,
+    // PV(b) needs P(b) (and, for a row's first block, the previous row's O
+    // read out). Polling both keeps PV(b) from waiting behind QK(b+1)'s gather.
     if (lane == 0) {
       const uint32_t idesc_qk = instr_desc(64, 64, fmt, fmt, false, false);
       const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, false);
       const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage), p0 = smem_u32(p_tile);
-      uint32_t g = 0, tok = 0;
-      bool ok = true;
-      auto issue_qk = [&](uint32_t gq) -> bool {
-        const int s = gq & 1;
-        if (!mbar_wait(&M.kv_full[s], (gq >> 1) & 1, abort_v, p.status)) return false;
-        if (!mbar_wait(&M.s_empty[s], ((gq >> 1) & 1) ^ 1, abort_v, p.status)) return false;
-        tc_fence_after();
-        const uint32_t sb = st0 + s * kTileBytes;
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(q0 + c * kChunkBytes + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc(sb + c * kChunkBytes + kk * 32, 16, 1024);
-            mma_f16(tmem + kColS + s * 64, ad, bd, idesc_qk, (c | kk) != 0);
-          }
-        mma_commit(&M.s_full[s]);
-        return true;
+      struct Cursor {
+        int k, b, nb;
+        uint32_t g, tok;
+        bool done;
       };
-      for (int k = 0; ok; ++k) {
-        int row;
-        const int r = next_row(p.n_rows, k, row);
-        if (r < 0) break;
-        if (r == 0) continue;
-        const RowInfo ri = row_info(p, row);
-        if (!mbar_wait(&M.q_full, tok & 1, abort_v, p.status)) break;
-        tc_fence_after();
-        if (!issue_qk(g)) break;
-        for (int b = 0; b < ri.nb; ++b) {
-          const uint32_t gb = g + b;
-          if (b + 1 < ri.nb) {
-            if (!issue_qk(gb + 1)) { ok = false; break; }
-          } else {
-            mma_commit(&M.q_empty);
-          }
-          if (!mbar_wait(&M.p_full, gb & 1, abort_v, p.status)) { ok = false; break; }
-          if (b == 0 && !mbar_wait(&M.o_empty, (tok & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sb = st0 + (gb & 1) * kTileBytes;
-#pragma unroll
-          for (int dt = 0; dt < 4; ++dt)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc(sb + dt * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-              const uint64_t bd = smem_desc(p0 + kk * 32, 16, 1024);
-              mma_f16(tmem + kColO + dt * 64, ad, bd, idesc_pv, (b | kk) != 0);
-            }
-          mma_commit(&M.kv_empty[gb & 1]);
-          mma_commit(&M.pv_done);
+      auto seek = [&](Cursor& c) {
+        while (true) {
+          int row;
+          const int r = next_row(p.n_rows, c.k, row);
+          if (r < 0) { c.done = true; return; }
+          if (r == 0) { ++c.k; continue; }
+          c.nb = row_info(p, row).nb;
+          c.b = 0;
+          if (c.nb > 0) return;
+          ++c.k;
         }
-        g += ri.nb;
-        ++tok;
+      };
+      Cursor qc{0, 0, 0, 0, 0, false}, pc{0, 0, 0, 0, 0, false};
+      seek(qc);
+      seek(pc);
+      uint64_t t_last = globaltimer_ns();
+      while (!pc.done) {
+        bool prog = false;
+        if (!qc.done) {
+          const uint32_t gq = qc.g;
+          const int s = gq & 1;
+          if ((qc.b != 0 || mbar_test(&M.q_full, qc.tok & 1)) && mbar_test(&M.kv_full[s], (gq >> 1) & 1) &&
+              mbar_test(&M.s_empty[s], ((gq >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t sb = st0 + s * kTileBytes;
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc(q0 + c * kChunkBytes + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc(sb + c * kChunkBytes + kk * 32, 16, 1024);
+                mma_f16(tmem + kColS + s * 64, ad, bd, idesc_qk, (c | kk) != 0);
+              }
+            mma_commit(&M.s_full[s]);
+            ++qc.g;
+            if (++qc.b == qc.nb) {
+              mma_commit(&M.q_empty);  // all QK of this row issued: Q may be replaced once they finish
+              ++qc.tok;
+              ++qc.k;
+              seek(qc);
+            }
+            prog = true;
+          }
+        }
+        if (pc.g < qc.g || (qc.done && !pc.done)) {
+          const uint32_t gp = pc.g;
+          if (mbar_test(&M.p_full, gp & 1) && (pc.b != 0 || mbar_test(&M.o_empty, (pc.tok & 1) ^ 1))) {
+            tc_fence_after();
+            const uint32_t sb = st0 + (gp & 1) * kTileBytes;
+#pragma unroll
+            for (int dt = 0; dt < 4; ++dt)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc(sb + dt * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+                const uint64_t bd = smem_desc(p0 + kk * 32, 16, 1024);
+                mma_f16(tmem + kColO + dt * 64, ad, bd, idesc_pv, (pc.b | kk) != 0);
+              }
+            mma_commit(&M.kv_empty[gp & 1]);
+            mma_commit(&M.pv_done);
+            ++pc.g;
+            if (++pc.b == pc.nb) {
+              ++pc.tok;
+              ++pc.k;
+              seek(pc);
+            }
+            prog = true;
+          }
+        }
+        if (prog) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_v) break;
+          if (globaltimer_ns() - t_last > 2000000000ull) {
+            set_status(p.status, kStatusTimeout);
+            *abort_v = 1;
+            break;
+          }
+        }
       }
     }
   } else if (warp >= 8) {
     // ---------------------------------------------------------------- gather producers
-    const int tid = threadIdx.x - 256;  // 0..255: four threads per selected row
-    const int j = tid >> 2, qt = tid & 3;
+    // Eight threads per selected row read consecutive 16-byte pieces (one
+    // 128-byte line per row per load), 32 rows per pass, two passes per
+    // 64-row block. The loads of block b+1 are issued right after block b is
+    // stored (registers act as a third stage) and the key -> page lookups of
+    // the next block run while the current block's data is in flight.
+    const int tid = threadIdx.x - 256;
+    const int rr = tid >> 3, part = tid & 7;  // row within a pass, piece lane
+    constexpr int kPB = 9;                    // BF16: 72 pieces per row / 8 threads
+    constexpr int kP8 = 5;                    // FP8: 36 pieces per row / 8 threads (rounded up)
     uint32_t g = 0, tok = 0;
-    for (int k = 0;; ++k) {
+    uint4 v[2][kPB];
+    auto lookup = [&](const RowInfo& ri, const int32_t* ir, const int32_t* pt, int b, int jrow) -> int64_t {
+      const int e = b * kBlk + jrow;
+      if (e >= ri.nvalid) return -1;
+      const int key = __ldg(ir + e);
+      if (key < 0 || key > ri.pos) return -1;
+      const int lp = key >> 6;
+      const int pg = lp < p.max_pages ? __ldg(pt + lp) : -1;
+      if (pg < 0 || pg >= p.num_pages) {
+        set_status(p.status, kStatusBounds);
+        return -1;
+      }
+      return static_cast<int64_t>(pg) * kPage + (key & 63);
+    };
+    auto load_block = [&](const int64_t* prow) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        if (!p.fp8) {
+          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv) + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
+#pragma unroll
+          for (int u = 0; u < kPB; ++u)
+            v[h2][u] = prow[h2] >= 0 ? ldg_stream(src + (part + 8 * u) * 8) : make_uint4(0, 0, 0, 0);
+        } else {
+          const uint8_t* src = p.kv + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
+#pragma unroll
+          for (int u = 0; u < kP8; ++u) {
+            const int pc = part + 8 * u;
+            v[h2][u] = (prow[h2] >= 0 && pc < 36) ? ldg_stream(src + pc * 16) : make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+    };
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
       int row;
       const int r = next_row(p.n_rows, k, row);
       if (r < 0) break;
       if (r == 0) continue;
       const RowInfo ri = row_info(p, row);
+      if (ri.nb == 0) continue;
+      const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
+      const int32_t* ir = p.idx + static_cast<size_t>(row) * p.topk;
+      // widen the BF16 query to f16 into the swizzled Q tile
       {
-        // widen the BF16 query to f16 into the swizzled Q tile
-        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
         const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
-        bool over = false;
-        for (int pc = tid; pc < H * 72; pc += kProducers) {
+        constexpr int kQPieces = (H * 72 + kProducers - 1) / kProducers;
+        uint4* vq = &v[0][0];
+#pragma unroll
+        for (int u = 0; u < kQPieces; ++u) {
+          const int pc = tid + u * kProducers;
           const int h = pc / 72, pp = pc - h * 72;
-          const uint4 v = ldg_stream(qr + h * kDqk + pp * 8);
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          if (pc < H * 72) vq[u] = ldg_stream(qr + h * kDqk + pp * 8);
+        }
+        int64_t prow[2] = {lookup(ri, ir, pt, 0, rr), lookup(ri, ir, pt, 0, rr + 32)};
+        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
+        bool over = false;
+#pragma unroll
+        for (int u = 0; u < kQPieces; ++u) {
+          const int pc = tid + u * kProducers;
+          if (pc >= H * 72) break;
+          const int h = pc / 72, pp = pc - h * 72;
+          const uint32_t in[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
           uint32_t o[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            over |= ((in[u] & 0x7FFFu) > 0x477Fu) || ((in[u] & 0x7FFF0000u) > 0x477F0000u);
-            o[u] = bf16x2_to_f16x2(in[u]);
+          for (int t = 0; t < 4; ++t) {
+            over |= ((in[t] & 0x7FFFu) > 0x477Fu) || ((in[t] & 0x7FFF0000u) > 0x477F0000u);
+            o[t] = bf16x2_to_f16x2(in[t]);
           }
           const int c = pp >> 3, qq = pp & 7;
           *reinterpret_cast<uint4*>(q_tile + c * kChunkBytes + h * 128 + ((qq ^ (h & 7)) << 4)) =
@@ -303,73 +404,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(2, kProducers);
         if (tid == 0) mbar_arrive(&M.q_full);
-      }
-      const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
-      const int32_t* ir = p.idx + static_cast<size_t>(row) * p.topk;
-      bool ok = true;
-      for (int b = 0; b < ri.nb; ++b, ++g) {
-        const int s = g & 1;
-        if (!mbar_wait(&M.kv_empty[s], ((g >> 1) & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
-        const int e = b * kBlk + j;
-        int64_t prow = -1;
-        if (e < ri.nvalid) {
-          const int key = __ldg(ir + e);
-          if (key >= 0 && key <= ri.pos) {
-            const int lp = key >> 6;
-            const int pg = lp < p.max_pages ? __ldg(pt + lp) : -1;
-            if (pg >= 0 && pg < p.num_pages) prow = static_cast<int64_t>(pg) * kPage + (key & 63);
-            else set_status(p.status, kStatusBounds);
+        load_block(prow);
+        for (int b = 0; b < ri.nb; ++b, ++g) {
+          const int s = g & 1;
+          int64_t prow_next[2] = {-1, -1};
+          if (b + 1 < ri.nb) {
+            prow_next[0] = lookup(ri, ir, pt, b + 1, rr);
+            prow_next[1] = lookup(ri, ir, pt, b + 1, rr + 32);
           }
-        }
-        uint8_t* rowp = stage + s * kTileBytes + j * 128;
-        if (qt == 0) {
-          const float ks = (p.fp8 && prow >= 0) ? __ldg(p.kv_scale + prow) : 1.0f;
-          M.colscale[s][j] = ks * p.scale_log2;
-          M.pscale[s][j] = ks;
-          M.valid[s][j] = prow >= 0;
-        }
-        if (!p.fp8) {
-          // 72 pieces of 8 BF16 per row, 18 per thread; widened to f16 in place of layout
-          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv) + (prow >= 0 ? prow : 0) * kDqk;
-          uint4 v[18];
-#pragma unroll
-          for (int u = 0; u < 18; ++u)
-            v[u] = prow >= 0 ? ldg_stream(src + (qt * 18 + u) * 8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int u = 0; u < 18; ++u) {
-            const int pc = qt * 18 + u;
-            const int c = pc >> 3, qq = pc & 7;
-            *reinterpret_cast<uint4*>(rowp + c * kChunkBytes + ((qq ^ (j & 7)) << 4)) =
-                make_uint4(bf16x2_to_f16x2(v[u].x), bf16x2_to_f16x2(v[u].y), bf16x2_to_f16x2(v[u].z),
-                           bf16x2_to_f16x2(v[u].w));
+          float ks[2] = {1.0f, 1.0f};
+          if (p.fp8 && part == 0) {
+            if (prow[0] >= 0) ks[0] = __ldg(p.kv_scale + prow[0]);
+            if (prow[1] >= 0) ks[1] = __ldg(p.kv_scale + prow[1]);
           }
-        } else {
-          // 36 pieces of 16 e4m3 per row, 9 per thread; each widens to two f16 pieces
-          const uint8_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
-          uint4 v[9];
+          if (!mbar_wait(&M.kv_empty[s], ((g >> 1) & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
 #pragma unroll
-          for (int u = 0; u < 9; ++u)
-            v[u] = prow >= 0 ? ldg_stream(src + (qt * 9 + u) * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int u = 0; u < 9; ++u) {
-            const int p8 = qt * 9 + u;
-            const int c = p8 >> 2, qq = (p8 & 3) * 2;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              o[2 * t] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] & 0xFFFFu));
-              o[2 * t + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] >> 16));
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = rr + 32 * h2;
+            uint8_t* rowp = stage + s * kTileBytes + j * 128;
+            if (part == 0) {
+              M.colscale[s][j] = ks[h2] * p.scale_log2;
+              M.pscale[s][j] = ks[h2];
+              M.valid[s][j] = prow[h2] >= 0;
             }
-            uint8_t* cp = rowp + c * kChunkBytes;
-            *reinterpret_cast<uint4*>(cp + ((qq ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(cp + (((qq + 1) ^ (j & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            if (!p.fp8) {
+#pragma unroll
+              for (int u = 0; u < kPB; ++u) {
+                // piece part + 8u: chunk u, 16-byte slot `part`
+                *reinterpret_cast<uint4*>(rowp + u * kChunkBytes + ((part ^ (j & 7)) << 4)) =
+                    make_uint4(bf16x2_to_f16x2(v[h2][u].x), bf16x2_to_f16x2(v[h2][u].y),
+                               bf16x2_to_f16x2(v[h2][u].z), bf16x2_to_f16x2(v[h2][u].w));
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < kP8; ++u) {
+                const int p8 = part + 8 * u;  // 16 e4m3 values = 32 bytes of f16
+                if (p8 >= 36) break;
+                const int c = p8 >> 2, qq = (p8 & 3) * 2;
+                const uint32_t w[4] = {v[h2][u].x, v[h2][u].y, v[h2][u].z, v[h2][u].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  o[2 * t] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] & 0xFFFFu));
+                  o[2 * t + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] >> 16));
+                }
+                uint8_t* cp = rowp + c * kChunkBytes;
+                *reinterpret_cast<uint4*>(cp + ((qq ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(cp + (((qq + 1) ^ (j & 7)) << 4)) =
+                    make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
           }
+          fence_proxy_async_smem();
+          mbar_arrive(&M.kv_full[s]);
+          if (b + 1 < ri.nb) load_block(prow_next);
+          prow[0] = prow_next[0];
+          prow[1] = prow_next[1];
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&M.kv_full[s]);
       }
-      if (!ok) break;
       ++tok;
     }
   } else if (warp >= 4) {

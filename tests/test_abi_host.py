@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: every symbol declared in include/smla.h is exported,
+and argument checks return the documented status codes before anything is
+enqueued (the fake device pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import indexer_top_sparse_score_gb300 as smla
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "smla.h")
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def L():
+    smla.build()
+    return smla.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\**\s*(smla_\w+)\s*\(", text, re.M)))
+
+
+def test_header_symbols_exported(L):
+    names = declared_functions()
+    assert len(names) == 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(smla._SIGS), "binding signatures and header disagree"
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.smla_status_string(code).decode().startswith("SMLA_")
+    assert L.smla_status_string(99) == b"SMLA_ERR_UNKNOWN"
+
+
+def _cache(**kw):
+    c = dict(kv=FAKE, kv_scale=FAKE, k_idx=FAKE, k_idx_scale=None, num_pages=300, page_size=64,
+             kv_dtype=smla.SMLA_FP8_E4M3, idx_dtype=smla.SMLA_FP8_E4M3, d_idx=128)
+    c.update(kw)
+    return smla.PagedCache(**c)
+
+
+def _prefill(L, cache, *, prefix=1000, T=4096, H=64, h_idx=32, topk=2048, ws_bytes=None, q=FAKE, out=FAKE,
+             pt=FAKE, sm=0.04):
+    need = L.smla_sparse_mla_prefill_workspace_size(prefix, T, H, h_idx, topk)
+    ws = need if ws_bytes is None else ws_bytes
+    return L.smla_sparse_mla_prefill(ctypes.byref(cache), pt, prefix, T, q, H, FAKE, FAKE, h_idx, topk, sm,
+                                     out, FAKE, None, FAKE, ws, None)
+
+
+def test_prefill_argument_checks(L):
+    assert _prefill(L, _cache(), q=None) == INVALID
+    assert _prefill(L, _cache(), out=FAKE + 8) == INVALID          # misaligned
+    assert _prefill(L, _cache(), pt=None) == INVALID
+    assert _prefill(L, _cache(), T=0) == INVALID
+    assert _prefill(L, _cache(), prefix=-1) == INVALID
+    assert _prefill(L, _cache(page_size=32)) == UNSUPPORTED
+    assert _prefill(L, _cache(d_idx=64)) == UNSUPPORTED             # e4m3 x 64 = 64-byte rows
+    assert _prefill(L, _cache(kv_scale=None)) == INVALID            # FP8 needs scales
+    assert _prefill(L, _cache(kv_dtype=7)) == INVALID
+    assert _prefill(L, _cache(), H=32) == UNSUPPORTED
+    assert _prefill(L, _cache(), h_idx=12) == UNSUPPORTED
+    assert _prefill(L, _cache(), topk=4096) == UNSUPPORTED
+    assert _prefill(L, _cache(), topk=0) == INVALID
+    assert _prefill(L, _cache(), sm=float("nan")) == INVALID
+    assert _prefill(L, _cache(), ws_bytes=100) == WORKSPACE
+
+
+def test_decode_and_indexer_argument_checks(L):
+    c = _cache()
+    need = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
+    call = lambda **kw: L.smla_sparse_mla_decode(
+        ctypes.byref(c), kw.get("pt", FAKE), kw.get("max_pages", 2048), 64, kw.get("lens", FAKE),
+        kw.get("max_len", 131072), kw.get("qps", 2), FAKE, 64, FAKE, FAKE, 32, 2048, 0.04, FAKE, FAKE, None,
+        FAKE, kw.get("ws", need), None)
+    assert call(lens=None) == INVALID
+    assert call(max_pages=10) == INVALID        # table shorter than max_seq_len
+    assert call(qps=9) == UNSUPPORTED
+    assert call(ws=need - 1) == WORKSPACE
+    n = L.smla_indexer_topk(ctypes.byref(c), FAKE, 2048, 64, FAKE, 131072, 2, FAKE, FAKE, 32, 2048, None,
+                            None, FAKE, 1 << 30, None)
+    assert n == INVALID                          # out_idx required
+
+
+def test_workspace_sizes(L):
+    # prefill keeps the index list: status word + T x topk int32
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048) == 256 + 16384 * 2048 * 4
+    # decode: candidate lists of every (row, 8192-key block) + counts + index list
+    rows, nkb, k = 128, 16, 2048
+    dec = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
+    assert dec >= 256 + rows * nkb * k * 8 + rows * nkb * 4 + rows * k * 4
+    assert L.smla_sparse_mla_fwd_workspace_size(100, 64, 2048) == 256
