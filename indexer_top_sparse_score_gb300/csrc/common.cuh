@@ -29,6 +29,10 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float(u);
 }
 
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool in, uint32_t bin) {
+  if (in) atomicAdd(&hist[bin], 1u);
+}
+
 // ---------------------------------------------------------------------------
 // Exact selection of the `k` best (key descending, index ascending) among `n`
 // entries. Cooperative over NT threads that share `hist` (256 uint32) and
@@ -53,7 +57,8 @@ __device__ __forceinline__ void radix_select(int k, int tid, uint32_t* hist, uin
     for (int b = tid; b < 256; b += NT) hist[b] = 0;
     sync();
     each([&](uint32_t key, uint32_t) {
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      const bool in = (key & mask) == prefix;
+      hist_add(hist, in, (key >> shift) & 255u);
     });
     sync();
     if (tid < 32) {
@@ -107,7 +112,8 @@ __device__ __forceinline__ void radix_select(int k, int tid, uint32_t* hist, uin
     for (int b = tid; b < 256; b += NT) hist[b] = 0;
     sync();
     each([&](uint32_t key, uint32_t idx) {
-      if (key == prefix && (idx & imask) == iprefix) atomicAdd(&hist[(idx >> shift) & 255u], 1u);
+      const bool in = key == prefix && (idx & imask) == iprefix;
+      hist_add(hist, in, (idx >> shift) & 255u);
     });
     sync();
     if (tid < 32) {
@@ -152,6 +158,128 @@ __device__ __forceinline__ void radix_select(int k, int tid, uint32_t* hist, uin
 
 __device__ __forceinline__ bool selected(uint32_t key, uint32_t idx, uint32_t thr_key, uint32_t thr_idx) {
   return key > thr_key || (key == thr_key && idx <= thr_idx);
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-k threshold over entries held in shared memory: keys[0..n),
+// idxs[0..n) (n > k >= 1), 128 cooperating threads synchronised by `sync()`,
+// `hist` = 256 words, `red` = 16 words of shared scratch. Returns
+// (thr_key, thr_idx): entry e is among the best k (key descending, index
+// ascending) iff key > thr_key, or key == thr_key and idx <= thr_idx.
+//
+// Method: a radix select whose bins span only the live key range [lo, hi]
+// (found by a min/max pass) and halve it by 8 bits per pass, so values that
+// share a float exponent still spread over the bins; then, if the k-th key is
+// tied and not all ties are needed, the same on the indices of the ties
+// (ascending). Key passes read keys only, 4 per 16-byte load.
+template <typename Sync>
+__device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* idxs, int n, int k, int tid,
+                                          uint32_t* hist, uint32_t* red, Sync sync, uint32_t& thr_key,
+                                          uint32_t& thr_idx) {
+  const int lane = tid & 31, w = tid >> 5;
+  // visit keys (and optionally indices) 4 at a time; f(value, idx_or_0, valid)
+  auto each4 = [&](bool with_idx, auto f) {
+    for (int e0 = tid * 4; e0 < n; e0 += 512) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(keys + e0);
+      uint4 iv = make_uint4(0, 0, 0, 0);
+      if (with_idx) iv = *reinterpret_cast<const uint4*>(idxs + e0);
+      f(kv.x, iv.x, e0 + 0 < n);
+      f(kv.y, iv.y, e0 + 1 < n);
+      f(kv.z, iv.z, e0 + 2 < n);
+      f(kv.w, iv.w, e0 + 3 < n);
+    }
+  };
+  // min / max of a (filtered) value over all entries
+  auto minmax = [&](bool ties, uint32_t tk, uint32_t& lo, uint32_t& hi) {
+    uint32_t a = 0xFFFFFFFFu, b = 0;
+    each4(ties, [&](uint32_t kk, uint32_t ii, bool ok) {
+      if (!ok) return;
+      const uint32_t v = ties ? ii : kk;
+      if (ties && kk != tk) return;
+      a = min(a, v);
+      b = max(b, v);
+    });
+    a = __reduce_min_sync(0xFFFFFFFFu, a);
+    b = __reduce_max_sync(0xFFFFFFFFu, b);
+    if (lane == 0) {
+      red[w] = a;
+      red[4 + w] = b;
+    }
+    sync();
+    lo = min(min(red[0], red[1]), min(red[2], red[3]));
+    hi = max(max(red[4], red[5]), max(red[6], red[7]));
+    sync();
+  };
+  // narrow [lo, hi] to the bin holding the r-th value (descending for keys,
+  // ascending for tie indices) until it is a single value
+  auto refine = [&](bool ties, uint32_t tk, uint32_t lo, uint32_t hi, int& r, uint32_t& value, uint32_t& count) {
+    while (true) {
+      const uint32_t range = hi - lo;
+      const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
+      for (int b = tid; b < 256; b += 128) hist[b] = 0;
+      sync();
+      each4(ties, [&](uint32_t kk, uint32_t ii, bool ok) {
+        if (!ok) return;
+        const uint32_t v = ties ? ii : kk;
+        if ((ties && kk != tk) || v < lo || v > hi) return;
+        atomicAdd(&hist[(v - lo) >> shift], 1u);
+      });
+      sync();
+      if (w == 0) {
+        // lane l owns 8 consecutive bins in scan order
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int bin = ties ? 8 * lane + i : 255 - 8 * lane - i;
+          c[i] = hist[bin];
+          sum += c[i];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const uint32_t excl = incl - sum;
+        if (excl < static_cast<uint32_t>(r) && incl >= static_cast<uint32_t>(r)) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + c[i] >= static_cast<uint32_t>(r)) {
+              red[8] = ties ? 8 * lane + i : 255 - 8 * lane - i;
+              red[9] = static_cast<uint32_t>(r) - run;
+              red[10] = c[i];
+              break;
+            }
+            run += c[i];
+          }
+        }
+      }
+      sync();
+      const uint32_t bin = red[8];
+      r = static_cast<int>(red[9]);
+      count = red[10];
+      sync();
+      const uint64_t nlo = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(bin) << shift);
+      const uint64_t nhi = nlo + ((1ull << shift) - 1ull);
+      lo = static_cast<uint32_t>(nlo);
+      hi = static_cast<uint32_t>(nhi < hi ? nhi : hi);
+      if (shift == 0) {
+        value = lo;
+        return;
+      }
+    }
+  };
+  uint32_t lo, hi, cnt;
+  int r = k;
+  minmax(false, 0, lo, hi);
+  refine(false, 0, lo, hi, r, thr_key, cnt);
+  if (static_cast<uint32_t>(r) == cnt) {
+    thr_idx = 0xFFFFFFFFu;
+    return;
+  }
+  minmax(true, thr_key, lo, hi);
+  refine(true, thr_key, lo, hi, r, thr_idx, cnt);
 }
 
 }  // namespace smla

@@ -159,11 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* cidx = ckey + kBufEntries;
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][256]
-  uint32_t* scratch = hist + 512;                               // [2][8]
-  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 16);      // [128]
+  uint32_t* scratch = hist + 512;                               // [2][16]
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [128]
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 128);     // [128]
-  uint32_t* wsum = theta + 128;                                 // [2][4]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + 8);
+  uint32_t* wsum = theta + 128;                                 // [2][2][4]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + 16);
   uint64_t* a_full = bars;
   uint64_t* a_empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid_wg = (ew & 3) * 32 + lane;
     const uint32_t bar_wg = 1 + wg;
     uint32_t* hist_wg = hist + 256 * wg;
-    uint32_t* scr_wg = scratch + 8 * wg;
-    uint32_t* wsum_wg = wsum + 4 * wg;
+    uint32_t* scr_wg = scratch + 16 * wg;
+    uint32_t* wsum_wg = wsum + 8 * wg;
     auto wg_sync = [&]() { named_bar_sync(bar_wg, 128); };
     const int tpw = (p.tq + 1) / 2;
     const int j0 = wg * tpw, j1 = min(p.tq, j0 + tpw);
@@ -311,57 +311,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lanemask_lt = (1u << lane) - 1u;
     uint32_t ac = 0;
 
-    // Select the best `keep` of token j's buffer; if `out` is set, write the
-    // selection to the output row, else compact it in place and raise theta.
+    // Select the best `keep` of token j's buffer. If `to_output`, write the
+    // selection to the output row (or the split-mode candidate slot); else
+    // compact the buffer in place (stable) and raise the token's threshold.
     auto select_token = [&](int j, int keep, bool to_output, const Item& it) {
       const int n = cnt[j];
       uint32_t* kb = ckey + j * cap;
       uint32_t* ib = cidx + j * cap;
       uint32_t tk = 0, ti = 0xFFFFFFFFu;
-      bool all = n <= keep;
-      if (!all) {
-        radix_select<128>(
-            keep, tid_wg, hist_wg, scr_wg,
-            [&](auto f) {
-              for (int e = tid_wg; e < n; e += 128) f(kb[e], ib[e]);
-            },
-            wg_sync, tk, ti);
-      }
+      const bool all = n <= keep;
+      if (!all) wg_select(kb, ib, n, keep, tid_wg, hist_wg, scr_wg, wg_sync, tk, ti);
       const int row = it.row0 + j;
       int base = 0;
-      for (int c0 = 0; c0 < n; c0 += 128) {
-        const int e = c0 + tid_wg;
-        uint32_t key = 0, idx = 0;
-        bool take = false;
-        if (e < n) {
-          key = kb[e];
-          idx = ib[e];
-          take = all || selected(key, idx, tk, ti);
+      for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
+        const int e0 = r0 + tid_wg * 4;
+        uint4 kv = make_uint4(0, 0, 0, 0), iv = make_uint4(0, 0, 0, 0);
+        if (e0 < n) {
+          kv = *reinterpret_cast<const uint4*>(kb + e0);
+          iv = *reinterpret_cast<const uint4*>(ib + e0);
         }
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
-        if (lane == 0) wsum_wg[ew & 3] = __popc(m);
+        const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w}, ii[4] = {iv.x, iv.y, iv.z, iv.w};
+        bool take[4];
+        int c = 0;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          take[q4] = e0 + q4 < n && (all || selected(kk[q4], ii[q4], tk, ti));
+          c += take[q4];
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        uint32_t* ws = wsum_wg + 4 * (rnd & 1);
+        if (lane == 31) ws[ew & 3] = incl;
         wg_sync();
         int off = base, total = 0;
 #pragma unroll
         for (int w2 = 0; w2 < 4; ++w2) {
-          const int v = static_cast<int>(wsum_wg[w2]);
+          const int v = static_cast<int>(ws[w2]);
           if (w2 < (ew & 3)) off += v;
           total += v;
         }
-        off += __popc(m & lanemask_lt);
-        wg_sync();
-        if (take) {
+        off += incl - c;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (!take[q4]) continue;
           if (!to_output) {
-            kb[off] = key;
-            ib[off] = idx;
+            kb[off] = kk[q4];
+            ib[off] = ii[q4];
           } else if (!p.split) {
-            p.out_idx[static_cast<size_t>(row) * topk + off] = static_cast<int32_t>(idx);
-            if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + off] = key_score(key);
+            p.out_idx[static_cast<size_t>(row) * topk + off] = static_cast<int32_t>(ii[q4]);
+            if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + off] = key_score(kk[q4]);
           } else {
             const size_t slot = (static_cast<size_t>(row) * p.n_kblocks + it.kb) * topk + off;
-            p.cand_key[slot] = key;
-            p.cand_idx[slot] = idx;
+            p.cand_key[slot] = kk[q4];
+            p.cand_idx[slot] = ii[q4];
           }
+          ++off;
         }
         base += total;
       }
@@ -575,7 +583,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      512 * 4 + 16 * 4 + 128 * 4 + 128 * 4 + 8 * 4 + 16 * 8 + 16;
+                      512 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + 16 * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -127,6 +127,13 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
   return r != 0;
 }
 
+// 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = 0
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -503,15 +510,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
         const float m_new = fmaxf(m_used, mx);
         const bool resc = real && b > 0 && m_new > m_used + kRescaleLog2;
+        if (b == 0) m_used = m_new;
+        // probabilities against the running max (unchanged unless this head rescales),
+        // computed before waiting for the previous PV so they overlap it
+        float sum = 0.0f;
+        uint32_t pk[16];
+        auto make_p = [&]() {
+          const float mref = m_used == -INFINITY ? 0.0f : m_used;
+          sum = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int col = half * 32 + i;
+            const float p0 = fast_exp2(x[i] - mref), p1 = fast_exp2(x[i + 1] - mref);
+            sum += p0 + p1;
+            pk[i >> 1] = pack_f16(p0 * M.pscale[s][col], p1 * M.pscale[s][col + 1]);
+          }
+        };
+        if (!resc) make_p();
         const bool any = named_bar_or(1, 128, resc);
         if (b > 0 && !mbar_wait(&M.pv_done, (gb - 1) & 1, abort_v, p.status)) { ok = false; break; }
-        if (b == 0) {
-          m_used = m_new;
-        } else if (any) {
-          const float a = resc ? exp2f(m_used - m_new) : 1.0f;
+        if (any) {
+          const float a = resc ? fast_exp2(m_used - m_new) : 1.0f;
           if (resc) {
             m_used = m_new;
             l *= a;
+            make_p();
           }
           if (half == 0) M.alpha[h] = a;
           named_bar_sync(1, 128);
@@ -531,17 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
           tc_fence_before();
-        }
-        const float mref = m_used == -INFINITY ? 0.0f : m_used;
-        float sum = 0.0f;
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int col = half * 32 + i;
-          const float p0 = exp2f(x[i] - mref), p1 = exp2f(x[i + 1] - mref);
-          sum += p0 + p1;
-          const float a = p0 * M.pscale[s][col], c = p1 * M.pscale[s][col + 1];
-          pk[i >> 1] = pack_f16(a, c);
         }
         l += sum;
         uint8_t* prow = p_tile + h * 128;

@@ -199,3 +199,30 @@ def test_repeat_calls_same_sets():
     b, ob, lb = run_prefill(dev)
     assert torch.equal(torch.sort(a, dim=1).values, torch.sort(b, dim=1).values)
     assert (oa.float() - ob.float()).abs().max().item() < 1e-2
+
+
+@pytest.mark.parametrize("mode", ["constant", "binary"])
+def test_indexer_heavy_ties(mode):
+    """Ties everywhere: constant keys (all scores equal -> the lowest k indices) and
+    keys in {0,1} (few distinct scores); the lower index must win every tie."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=700, prefix_len=6000, shuffled=True)
+    prob = wl.make(spec, "cpu")
+    k = prob.cache.k_idx
+    if mode == "constant":
+        row = k.view(-1, spec.d_idx)[0].clone()
+        k.view(-1, spec.d_idx)[:] = row
+    else:
+        g = torch.Generator().manual_seed(3)
+        v = torch.randint(0, 2, k.shape, generator=g).to(torch.float32)
+        k.copy_(v.to(torch.float8_e4m3fn).view(torch.uint8))
+    dev = prob.to("cuda")
+    L = spec.prefix_len + spec.n_tokens
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    gidx, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
+                                 spec.topk)
+    assert smla.read_status(ws)[0] == 0
+    rows = np.arange(0, spec.n_tokens, 23)
+    ridx, *_ = oracle.Oracle(prob).rows(rows, attend=False)
+    compare_idx(_host(gidx)[rows], ridx)
+    if mode == "constant":
+        assert (np.sort(_host(gidx)[rows], axis=1) == np.arange(spec.topk)[None, :]).all()
