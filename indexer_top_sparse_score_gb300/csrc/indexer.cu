@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = p.is_bf16 ? instr_desc(128, N, kFmtBF16, kFmtBF16, false, false)
                                        : instr_desc(128, N, kFmtE4M3, kFmtE4M3, false, false);
       uint32_t sc = 0, bi = 0, ac = 0;
-      const uint32_t b0 = smem_u32(b_tile);
+      const uint64_t a_desc0 = smem_desc(smem_u32(a_tiles), 16, 1024);
+      const uint64_t b_desc0 = smem_desc(smem_u32(b_tile), 16, 1024);
       for (int k = 0;; ++k) {
         Item it;
         const int r = next_item(p, k, it);
@@ -277,14 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(a_tiles + s * kStageBytes);
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * kStageBytes) >> 4);
           const uint32_t d = tmem + buf * N;
 #pragma unroll
           for (int kk = 0; kk < kIdxRowBytes / 32; ++kk) {
-            const uint64_t ad = smem_desc(a0 + 32 * kk, 16, 1024);
-            const uint64_t bd = smem_desc(b0 + 32 * kk, 16, 1024);
-            if (p.is_bf16) mma_f16(d, ad, bd, idesc, kk > 0);
-            else mma_f8(d, ad, bd, idesc, kk > 0);
+            const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+            if (p.is_bf16) mma_f16(d, ad + off, b_desc0 + off, idesc, kk > 0);
+            else mma_f8(d, ad + off, b_desc0 + off, idesc, kk > 0);
           }
           mma_commit(&a_empty[s]);
           mma_commit(&acc_full[buf]);

@@ -66,10 +66,14 @@ struct MlaParams {
   uint32_t* status;
 };
 
+// Per selected row j of a stage: {logit multiplier, bias (0, or -inf for a
+// skipped row)} and the probability multiplier (FP8 token scale). Rows 32..63
+// sit one slot further so the two halves of a softmax warp hit different banks.
+__host__ __device__ constexpr int meta_slot(int j) { return j + (j >= 32 ? 1 : 0); }
+
 struct SmemMeta {
-  float colscale[2][kBlk];  // logit multiplier per selected row (0 if skipped)
-  float pscale[2][kBlk];    // probability multiplier (FP8 per-token scale)
-  uint8_t valid[2][kBlk];
+  float2 col[2][kBlk + 1];
+  float pscale[2][kBlk + 1];
   float linv[64];
   float alpha[64];
   uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, pv_done, o_empty;
@@ -238,6 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_qk = instr_desc(64, 64, fmt, fmt, false, false);
       const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, false);
       const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage), p0 = smem_u32(p_tile);
+      // K-major 128B-swizzled operands: SBO = 1024 (8-row groups); the gathered
+      // tile read MN-major as V^T: LBO = one 64-value chunk of all rows.
+      const uint64_t q_desc = smem_desc(q0, 16, 1024);
+      const uint64_t st_desc0 = smem_desc(st0, 16, 1024), st_desc1 = smem_desc(st0 + kTileBytes, 16, 1024);
+      const uint64_t vt_desc0 = smem_desc(st0, kChunkBytes, 1024);
+      const uint64_t vt_desc1 = smem_desc(st0 + kTileBytes, kChunkBytes, 1024);
+      const uint64_t p_desc = smem_desc(p0, 16, 1024);
       struct Cursor {
         int k, b, nb;
         uint32_t g, tok;
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor qc{0, 0, 0, 0, 0, false}, pc{0, 0, 0, 0, 0, false};
       seek(qc);
       seek(pc);
-      uint64_t t_last = globaltimer_ns();
+      long long t_last = clock64();
       while (!pc.done) {
         bool prog = false;
         if (!qc.done) {
@@ -267,14 +278,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((qc.b != 0 || mbar_test(&M.q_full, qc.tok & 1)) && mbar_test(&M.kv_full[s], (gq >> 1) & 1) &&
               mbar_test(&M.s_empty[s], ((gq >> 1) & 1) ^ 1)) {
             tc_fence_after();
-            const uint32_t sb = st0 + s * kTileBytes;
-#pragma unroll 1
+            // descriptors advance by (byte offset >> 4) in their start-address field
+            const uint64_t bd0 = s ? st_desc1 : st_desc0;
+            const uint32_t dS = tmem + kColS + s * 64;
+#pragma unroll
             for (int c = 0; c < kChunks; ++c)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc(q0 + c * kChunkBytes + kk * 32, 16, 1024);
-                const uint64_t bd = smem_desc(sb + c * kChunkBytes + kk * 32, 16, 1024);
-                mma_f16(tmem + kColS + s * 64, ad, bd, idesc_qk, (c | kk) != 0);
+                const uint64_t off = static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
+                mma_f16(dS, q_desc + off, bd0 + off, idesc_qk, (c | kk) != 0);
               }
             mma_commit(&M.s_full[s]);
             ++qc.g;
@@ -291,15 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t gp = pc.g;
           if (mbar_test(&M.p_full, gp & 1) && (pc.b != 0 || mbar_test(&M.o_empty, (pc.tok & 1) ^ 1))) {
             tc_fence_after();
-            const uint32_t sb = st0 + (gp & 1) * kTileBytes;
+            const uint64_t ad0 = (gp & 1) ? vt_desc1 : vt_desc0;
 #pragma unroll
             for (int dt = 0; dt < 4; ++dt)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc(sb + dt * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-                const uint64_t bd = smem_desc(p0 + kk * 32, 16, 1024);
-                mma_f16(tmem + kColO + dt * 64, ad, bd, idesc_pv, (pc.b | kk) != 0);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16(tmem + kColO + dt * 64, ad0 + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
+                        p_desc + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (pc.b | kk) != 0);
             mma_commit(&M.kv_empty[gp & 1]);
             mma_commit(&M.pv_done);
             ++pc.g;
@@ -312,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (prog) {
-          t_last = globaltimer_ns();
+          t_last = clock64();
         } else {
           if (*abort_v) break;
-          if (globaltimer_ns() - t_last > 2000000000ull) {
+          if (clock64() - t_last > kWaitLimitCycles) {
             set_status(p.status, kStatusTimeout);
             *abort_v = 1;
             break;
@@ -430,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = rr + 32 * h2;
             uint8_t* rowp = stage + s * kTileBytes + j * 128;
             if (part == 0) {
-              M.colscale[s][j] = ks[h2] * p.scale_log2;
-              M.pscale[s][j] = ks[h2];
-              M.valid[s][j] = prow[h2] >= 0;
+              M.col[s][meta_slot(j)] = prow[h2] >= 0 ? make_float2(ks[h2] * p.scale_log2, 0.0f)
+                                                     : make_float2(0.0f, -INFINITY);
+              M.pscale[s][meta_slot(j)] = ks[h2];
             }
             if (!p.fp8) {
 #pragma unroll
@@ -501,10 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&M.kv_full[s], (gb >> 1) & 1, abort_v, p.status)) { ok = false; break; }
         float x[32];
         float mx = -INFINITY;
+        const float2* meta = &M.col[s][meta_slot(half * 32)];
+        const float* pmeta = &M.pscale[s][meta_slot(half * 32)];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int col = half * 32 + i;
-          x[i] = M.valid[s][col] ? __uint_as_float(raw[i]) * M.colscale[s][col] : -INFINITY;
+          const float2 m2 = meta[i];  // same address across the half: broadcast
+          x[i] = fmaf(__uint_as_float(raw[i]), m2.x, m2.y);
           mx = fmaxf(mx, x[i]);
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
@@ -520,10 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const int col = half * 32 + i;
             const float p0 = fast_exp2(x[i] - mref), p1 = fast_exp2(x[i + 1] - mref);
             sum += p0 + p1;
-            pk[i >> 1] = pack_f16(p0 * M.pscale[s][col], p1 * M.pscale[s][col + 1]);
+            pk[i >> 1] = p.fp8 ? pack_f16(p0 * pmeta[i], p1 * pmeta[i + 1]) : pack_f16(p0, p1);
           }
         };
         if (!resc) make_p();

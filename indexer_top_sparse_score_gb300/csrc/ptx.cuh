@@ -59,17 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity`. Gives up after `limit_ns` of wall time or
+// About four seconds of SM clock at GB300 clocks: the limit of every bounded wait.
+constexpr long long kWaitLimitCycles = 8000000000ll;
+
+// Bounded wait on phase `parity`. Gives up after kWaitLimitCycles SM cycles or
 // when another thread has raised `*abort`; on giving up it records a timeout
-// in `*status` (if non-null), raises `*abort` and returns false.
+// in `*status` (if non-null), raises `*abort` and returns false. The limit is
+// checked on the SM cycle counter (cheap to read, unlike the global timer).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, uint64_t limit_ns = 2000000000ull) {
+                                          uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       if (status) atomicOr(status, kStatusTimeout);
       if (abort) *abort = 1;
       return false;
