@@ -173,6 +173,32 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
                            void* stream);
 
 /* ---------------------------------------------------------------------------
+ * smla_sparse_mla_prefill_noalloc — the same step as smla_sparse_mla_prefill
+ * for callers that cannot allocate device memory and so cannot provide a
+ * workspace: for example a plugin that is handed only input and output
+ * pointers by its host framework, or an engine whose device memory is all
+ * owned by a pool that outside code may not draw from. (This entry point has
+ * no counterpart in the pages; it only changes where the scratch lives.)
+ *
+ * It allocates nothing. Its scratch (status word + the selected-index list)
+ * is a fixed 16 MiB array inside the library, held by every GPU that loads
+ * the library until the process exits. Limit: n_tokens * topk * 4 + 256
+ * bytes must fit in 16 MiB (e.g. 2047 tokens at topk = 2048); larger calls
+ * return SMLA_ERR_WORKSPACE and enqueue nothing. The selected indices are
+ * not returned. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. Every call on a device shares the one
+ * array and leaves its contents behind (each call clears the status word
+ * and rewrites the index list): calls whose work overlaps on the GPU, on
+ * different streams or threads, race and give wrong results. Arguments
+ * otherwise as smla_sparse_mla_prefill.
+ * ------------------------------------------------------------------------- */
+int smla_sparse_mla_prefill_noalloc(const smla_paged_cache* cache, const int32_t* page_table,
+                                    int32_t prefix_len, int32_t n_tokens, const void* q, int32_t n_heads,
+                                    const void* q_idx, const float* w, int32_t h_idx, int32_t topk,
+                                    float sm_scale, void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
  * smla_read_status — waits for `stream`, then reads the device status word of
  * `workspace` written by the calls that used it: SMLA_OK, SMLA_ERR_DEVICE_BOUNDS
  * or SMLA_ERR_TIMEOUT (the latter wins); the raw bit mask goes to *bits if

@@ -22,7 +22,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libsmla.so")
-SOURCES = ["api.cu", "indexer.cu", "mla.cu"]
+SOURCES = ["api.cu", "indexer.cu", "mla.cu", "noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 
@@ -104,6 +104,8 @@ _SIGS = {
     "smla_sparse_mla_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "smla_sparse_mla_decode": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32,
                                                _i32, _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "smla_sparse_mla_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
+                                                        _f32, _vp, _vp, _vp]),
     "smla_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
