@@ -192,7 +192,7 @@ def run_e2e(args, spec, dev, out, lse, stream, world):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     q_d, qi_d, w_d = torch.empty_like(dev.q), torch.empty_like(dev.q_idx), torch.empty_like(dev.w)
-    ws_p = smla.workspace(smla.prefill_workspace_bytes(P, T, H, spec.h_idx, k))
+    ws_p = smla.workspace(smla.prefill_workspace_bytes(P, T, H, spec.h_idx, k, spec.kv_dtype))
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
@@ -257,7 +257,7 @@ def main():
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
     ws_i = smla.workspace(L.smla_indexer_topk_workspace_size(1, P + T, T, spec.h_idx, k))
-    ws_m = smla.workspace(256)
+    ws_m = smla.workspace(L.smla_sparse_mla_fwd_workspace_size(P + T, T, H, k, smla._dtype_code(spec.kv_dtype)))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
     def step():

@@ -132,8 +132,13 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
  * value beyond it is reported by smla_read_status as SMLA_ERR_UNSUPPORTED.
  * Supported: n_heads in {16, 64} (16 and 64 query heads of the configurations),
  * topk <= 2048.
+ * Workspace: 256 bytes suffice. For a BF16 cache of one sequence (seq_lens
+ * NULL) a larger workspace, as returned for max_keys = prefix_len + q_per_seq,
+ * lets the call first widen the sequence's rows to f16 once (576 * 2 bytes per
+ * key) so the attention gathers them without per-row conversion.
  * ------------------------------------------------------------------------- */
-size_t smla_sparse_mla_fwd_workspace_size(int32_t rows, int32_t n_heads, int32_t topk);
+size_t smla_sparse_mla_fwd_workspace_size(int32_t max_keys, int32_t rows, int32_t n_heads, int32_t topk,
+                                          int32_t kv_dtype);
 int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
                         int32_t n_seqs, const int32_t* seq_lens, int32_t prefix_len, int32_t q_per_seq,
                         const void* q, int32_t n_heads, const int32_t* idx, int32_t topk, float sm_scale,
@@ -148,9 +153,13 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
  *   q, q_idx, w, out, lse as above with rows = n_tokens.
  *   out_idx    [n_tokens][topk] int32 selected indices, or NULL to keep them
  *              in the workspace only.
+ * Workspace: at least 256 + n_tokens * topk * 4 bytes (rounded to 256); the
+ * size returned for kv_dtype = SMLA_BF16 adds an f16 copy of the sequence's
+ * prefix_len + n_tokens cache rows, written once per call, which the attention
+ * then gathers without per-row conversion (used only when it fits).
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t n_heads,
-                                              int32_t h_idx, int32_t topk);
+                                              int32_t h_idx, int32_t topk, int32_t kv_dtype);
 int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_table, int32_t prefix_len,
                             int32_t n_tokens, const void* q, int32_t n_heads, const void* q_idx,
                             const float* w, int32_t h_idx, int32_t topk, float sm_scale, void* out,
@@ -184,7 +193,8 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
  * is a fixed 16 MiB array inside the library, held by every GPU that loads
  * the library until the process exits. Limit: n_tokens * topk * 4 + 256
  * bytes must fit in 16 MiB (e.g. 2047 tokens at topk = 2048); larger calls
- * return SMLA_ERR_WORKSPACE and enqueue nothing. The selected indices are
+ * return SMLA_ERR_WORKSPACE and enqueue nothing. The f16 copy of a BF16 cache
+ * (see smla_sparse_mla_prefill) is made only if it fits in the rest. The selected indices are
  * not returned. The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture. Every call on a device shares the one

@@ -95,10 +95,10 @@ _SIGS = {
     "smla_indexer_topk_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "smla_indexer_topk": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp,
                                           _vp, _vp, _sz, _vp]),
-    "smla_sparse_mla_fwd_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "smla_sparse_mla_fwd_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "smla_sparse_mla_fwd": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _f32,
                                             _vp, _vp, _vp, _sz, _vp]),
-    "smla_sparse_mla_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "smla_sparse_mla_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "smla_sparse_mla_prefill": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _i32, _f32,
                                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "smla_sparse_mla_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
@@ -200,7 +200,9 @@ def sparse_mla_fwd(cache, page_tables, q, idx, sm_scale, *, prefix_len=0, seq_le
     if lse is None:
         lse = torch.empty((rows, H), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = workspace(L.smla_sparse_mla_fwd_workspace_size(rows, H, topk), q.device)
+        max_keys = prefix_len + q_per_seq if seq_lens is None else 0
+        ws = workspace(L.smla_sparse_mla_fwd_workspace_size(max_keys, rows, H, topk, _dtype_code(cache.kv_dtype)),
+                       q.device)
     c = make_cache(cache)
     rc = L.smla_sparse_mla_fwd(ctypes.byref(c), _p(pt), max_pages, n_seqs, _p(seq_lens), prefix_len,
                                q_per_seq, _p(q), H, _p(idx), topk, float(sm_scale), _p(out), _p(lse),
@@ -209,8 +211,9 @@ def sparse_mla_fwd(cache, page_tables, q, idx, sm_scale, *, prefix_len=0, seq_le
     return out, lse, ws
 
 
-def prefill_workspace_bytes(prefix_len, n_tokens, n_heads, h_idx, topk) -> int:
-    return lib().smla_sparse_mla_prefill_workspace_size(prefix_len, n_tokens, n_heads, h_idx, topk)
+def prefill_workspace_bytes(prefix_len, n_tokens, n_heads, h_idx, topk, kv_dtype="bf16") -> int:
+    return lib().smla_sparse_mla_prefill_workspace_size(prefix_len, n_tokens, n_heads, h_idx, topk,
+                                                        _dtype_code(kv_dtype))
 
 
 def sparse_mla_prefill(cache, page_table, prefix_len, q, q_idx, w, topk, sm_scale, *, out=None, lse=None,
@@ -224,7 +227,7 @@ def sparse_mla_prefill(cache, page_table, prefix_len, q, q_idx, w, topk, sm_scal
     if lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = workspace(prefill_workspace_bytes(prefix_len, T, H, h_idx, topk), q.device)
+        ws = workspace(prefill_workspace_bytes(prefix_len, T, H, h_idx, topk, cache.kv_dtype), q.device)
     c = make_cache(cache)
     rc = L.smla_sparse_mla_prefill(ctypes.byref(c), _p(page_table), prefix_len, T, _p(q), H, _p(q_idx), _p(w),
                                    h_idx, topk, float(sm_scale), _p(out), _p(lse), _p(out_idx), _p(ws),

@@ -75,6 +75,11 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t prefill_min_workspace(int32_t n_tokens, int32_t topk) {
+  if (n_tokens <= 0 || topk <= 0) return kStatusBytes;
+  return kStatusBytes + (static_cast<size_t>(n_tokens) * topk * 4 + 255) / 256 * 256;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -145,7 +150,9 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
 }
 
 // ----------------------------------------------------------------- sparse MLA (given indices)
-size_t smla_sparse_mla_fwd_workspace_size(int32_t, int32_t, int32_t) { return kStatusBytes; }
+size_t smla_sparse_mla_fwd_workspace_size(int32_t max_keys, int32_t, int32_t, int32_t, int32_t kv_dtype) {
+  return kStatusBytes + (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(max_keys) : 0);
+}
 
 static int mla_checks(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
                       int32_t n_seqs, int32_t q_per_seq, const void* q, int32_t n_heads, int32_t topk,
@@ -179,14 +186,23 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
   if ((rc = reset_status(workspace, st))) return rc;
   MlaLaunch L{cache, page_tables, max_pages, n_seqs, q_per_seq, seq_lens, prefix_len, q, n_heads, idx, topk,
               sm_scale, out, lse, static_cast<uint32_t*>(workspace), st};
+  // one BF16 sequence and room in the workspace: widen its rows once, gather f16
+  const int32_t n_keys = prefix_len + q_per_seq;
+  if (!seq_lens && cache->kv_dtype == SMLA_BF16 &&
+      workspace_bytes >= kStatusBytes + mla_shadow_bytes(n_keys)) {
+    L.shadow = static_cast<uint8_t*>(workspace) + kStatusBytes;
+    L.shadow_rows = n_keys;
+    if ((rc = launch_shadow_convert(L))) return rc;
+  }
   return launch_mla(L);
 }
 
 // ----------------------------------------------------------------- prefill
 size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t, int32_t,
-                                              int32_t topk) {
+                                              int32_t topk, int32_t kv_dtype) {
   if (prefix_len < 0 || n_tokens <= 0 || topk <= 0) return kStatusBytes;
-  return kStatusBytes + round256(static_cast<size_t>(n_tokens) * topk * 4);
+  return prefill_min_workspace(n_tokens, topk) +
+         (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(prefix_len + n_tokens) : 0);
 }
 
 int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_table, int32_t prefix_len,
@@ -207,8 +223,8 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   if (!(sm_scale == sm_scale)) return SMLA_ERR_INVALID_ARG;
   if (indexer_tokens_per_cta(h_idx, topk, false, n_tokens) <= 0) return SMLA_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return SMLA_ERR_WORKSPACE;
-  if (workspace_bytes < smla_sparse_mla_prefill_workspace_size(prefix_len, n_tokens, n_heads, h_idx, topk))
-    return SMLA_ERR_WORKSPACE;
+  const size_t ws_min = prefill_min_workspace(n_tokens, topk);
+  if (workspace_bytes < ws_min) return SMLA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((rc = reset_status(workspace, st))) return rc;
   int32_t* idx = out_idx ? out_idx : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
@@ -217,6 +233,12 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   if ((rc = launch_indexer(IL))) return rc;
   MlaLaunch ML{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, q, n_heads, idx, topk, sm_scale, out,
                lse, static_cast<uint32_t*>(workspace), st};
+  // BF16 cache and room in the workspace: widen the sequence's rows once, gather f16
+  if (cache->kv_dtype == SMLA_BF16 && workspace_bytes >= ws_min + mla_shadow_bytes(static_cast<int32_t>(total))) {
+    ML.shadow = static_cast<uint8_t*>(workspace) + ws_min;
+    ML.shadow_rows = static_cast<int32_t>(total);
+    if ((rc = launch_shadow_convert(ML))) return rc;
+  }
   return launch_mla(ML);
 }
 

@@ -42,7 +42,12 @@ constexpr int kBlk = 64;                     // selected rows per block
 constexpr int kChunks = kDqk / 64;           // 9 chunks of 64 values
 constexpr int kChunkBytes = kBlk * 128;      // 8 KB
 constexpr int kTileBytes = kChunks * kChunkBytes;  // 72 KB per stage / for Q
-constexpr int kPBytes = 64 * 128;            // P^T: 64 head rows x 64 values
+// P^T (64 head rows x 64 selected rows, f16) of block b is written into the
+// rope chunk (chunk 8) of block b's own stage: QK(b) has finished reading it
+// once S(b) is ready, and the stage is not refilled before PV(b) completes.
+// Every block therefore has its own P buffer, and the softmax of block b+1
+// never waits for PV(b) unless it has to rescale O.
+constexpr int kPChunk = kChunks - 1;
 constexpr int kThreads = 512;
 constexpr int kProducers = 256;          // warps 8-15
 constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
@@ -64,6 +69,8 @@ struct MlaParams {
   float* lse;
   int32_t fp8;
   uint32_t* status;
+  const uint16_t* shadow;  // f16 rows by logical position, or null
+  int32_t shadow_rows;
 };
 
 // Per selected row j of a stage: {logit multiplier, bias (0, or -inf for a
@@ -76,12 +83,12 @@ struct SmemMeta {
   float pscale[2][kBlk + 1];
   float linv[64];
   float alpha[64];
-  uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, pv_done, o_empty;
+  uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], o_empty;
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 2 * kTileBytes + kTileBytes + kPBytes + sizeof(SmemMeta);
+constexpr size_t kSmemBytes = 2 * kTileBytes + kTileBytes + sizeof(SmemMeta);
 
 // k-th row of this CTA: head/tail pairs. -1 done, 0 skip, 1 row.
 __device__ __forceinline__ int next_row(int n_rows, int k, int& row) {
@@ -189,8 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_tile = smem;
   uint8_t* stage = smem + kTileBytes;  // 2 stages
-  uint8_t* p_tile = smem + 3 * kTileBytes;
-  SmemMeta& M = *reinterpret_cast<SmemMeta*>(smem + 3 * kTileBytes + kPBytes);
+  SmemMeta& M = *reinterpret_cast<SmemMeta*>(smem + 3 * kTileBytes);
 
   constexpr int kColChunk = H < 32 ? H : 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,9 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&M.kv_empty[i], 1);
       mbar_init(&M.s_full[i], 1);
       mbar_init(&M.s_empty[i], 4);
+      // per stage: the softmax may finish P(b+1) before PV(b) is issued, so one
+      // barrier for all blocks could run two phases ahead of the MMA thread
+      mbar_init(&M.p_full[i], 4);
     }
-    mbar_init(&M.p_full, 4);
-    mbar_init(&M.pv_done, 1);
     mbar_init(&M.o_empty, 4);
     M.abort_flag = 0;
     fence_mbar_init();
@@ -241,14 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = instr_desc(64, 64, fmt, fmt, false, false);
       const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, false);
-      const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage), p0 = smem_u32(p_tile);
+      const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage);
       // K-major 128B-swizzled operands: SBO = 1024 (8-row groups); the gathered
       // tile read MN-major as V^T: LBO = one 64-value chunk of all rows.
       const uint64_t q_desc = smem_desc(q0, 16, 1024);
       const uint64_t st_desc0 = smem_desc(st0, 16, 1024), st_desc1 = smem_desc(st0 + kTileBytes, 16, 1024);
       const uint64_t vt_desc0 = smem_desc(st0, kChunkBytes, 1024);
       const uint64_t vt_desc1 = smem_desc(st0 + kTileBytes, kChunkBytes, 1024);
-      const uint64_t p_desc = smem_desc(p0, 16, 1024);
+      const uint64_t p_desc0 = smem_desc(st0 + kPChunk * kChunkBytes, 16, 1024);
+      const uint64_t p_desc1 = smem_desc(st0 + kTileBytes + kPChunk * kChunkBytes, 16, 1024);
       struct Cursor {
         int k, b, nb;
         uint32_t g, tok;
@@ -301,9 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (pc.g < qc.g || (qc.done && !pc.done)) {
           const uint32_t gp = pc.g;
-          if (mbar_test(&M.p_full, gp & 1) && (pc.b != 0 || mbar_test(&M.o_empty, (pc.tok & 1) ^ 1))) {
+          if (mbar_test(&M.p_full[gp & 1], (gp >> 1) & 1) && (pc.b != 0 || mbar_test(&M.o_empty, (pc.tok & 1) ^ 1))) {
             tc_fence_after();
             const uint64_t ad0 = (gp & 1) ? vt_desc1 : vt_desc0;
+            const uint64_t p_desc = (gp & 1) ? p_desc1 : p_desc0;
 #pragma unroll
             for (int dt = 0; dt < 4; ++dt)
 #pragma unroll
@@ -311,7 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16(tmem + kColO + dt * 64, ad0 + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
                         p_desc + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (pc.b | kk) != 0);
             mma_commit(&M.kv_empty[gp & 1]);
-            mma_commit(&M.pv_done);
             ++pc.g;
             if (++pc.b == pc.nb) {
               ++pc.tok;
@@ -351,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e >= ri.nvalid) return -1;
       const int key = __ldg(ir + e);
       if (key < 0 || key > ri.pos) return -1;
+      if (p.shadow) return key < p.shadow_rows ? key : -1;  // shadow rows are logical positions
       const int lp = key >> 6;
       const int pg = lp < p.max_pages ? __ldg(pt + lp) : -1;
       if (pg < 0 || pg >= p.num_pages) {
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return static_cast<int64_t>(pg) * kPage + (key & 63);
     };
     auto load_block = [&](const int64_t* prow) {
+      if (p.shadow) return;  // shadow rows are copied with cp.async once the stage is free
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         if (!p.fp8) {
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!mbar_wait(&M.kv_empty[s], ((g >> 1) & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
+          for (int h2 = 0; h2 < 2 && !p.shadow; ++h2) {
             const int j = rr + 32 * h2;
             uint8_t* rowp = stage + s * kTileBytes + j * 128;
             if (part == 0) {
@@ -471,6 +481,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(o[4], o[5], o[6], o[7]);
               }
             }
+          }
+          if (p.shadow) {
+            // f16 rows already widened: 9 x 16-byte async copies per row and thread
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = rr + 32 * h2;
+              const uint32_t rowp = smem_u32(stage + s * kTileBytes + j * 128);
+              if (part == 0) {
+                M.col[s][meta_slot(j)] = prow[h2] >= 0 ? make_float2(p.scale_log2, 0.0f) : make_float2(0.0f, -INFINITY);
+                M.pscale[s][meta_slot(j)] = 1.0f;
+              }
+              const uint16_t* src = p.shadow + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
+              const uint32_t nb = prow[h2] >= 0 ? 16u : 0u;
+#pragma unroll
+              for (int u = 0; u < kPB; ++u)
+                cp_async_16(rowp + u * kChunkBytes + ((part ^ (j & 7)) << 4), src + (part + 8 * u) * 8, nb);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
           }
           fence_proxy_async_smem();
           mbar_arrive(&M.kv_full[s]);
@@ -539,8 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (!resc) make_p();
         const bool any = named_bar_or(1, 128, resc);
-        if (b > 0 && !mbar_wait(&M.pv_done, (gb - 1) & 1, abort_v, p.status)) { ok = false; break; }
         if (any) {
+          // O must hold exactly PV(0..b-1) while it is rescaled. kv_empty[stage]
+          // completes when the PV of that stage's block finishes; for block b-1
+          // it is at most one phase away from this wait (its stage was refilled
+          // for b-1 only after PV(b-3) completed), so the parity is unambiguous.
+          const uint32_t gp = gb - 1;
+          if (!mbar_wait(&M.kv_empty[gp & 1], (gp >> 1) & 1, abort_v, p.status)) { ok = false; break; }
           const float a = resc ? fast_exp2(m_used - m_new) : 1.0f;
           if (resc) {
             m_used = m_new;
@@ -567,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
         }
         l += sum;
-        uint8_t* prow = p_tile + h * 128;
+        uint8_t* prow = stage + s * kTileBytes + kPChunk * kChunkBytes + h * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int qq = half * 4 + u;
@@ -576,11 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&M.p_full);
+        if (lane == 0) mbar_arrive(&M.p_full[s]);
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      if (!mbar_wait(&M.pv_done, (g + ri.nb - 1) & 1, abort_v, p.status)) break;
+      {
+        // last PV of this row done (same reasoning as for the rescale wait)
+        const uint32_t gl = g + ri.nb - 1;
+        if (!mbar_wait(&M.kv_empty[gl & 1], (gl >> 1) & 1, abort_v, p.status)) break;
+      }
       tc_fence_after();
       const float lt = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
       if (half == 0 && real) {
@@ -640,7 +678,54 @@ int launch_t(const MlaLaunch& L, const MlaParams& prm) {
   return SMLA_OK;
 }
 
+// Widen the BF16 rows of one sequence (logical positions 0..n_rows-1, through
+// its page table) to f16, stored contiguously by position.
+__global__ void __launch_bounds__(256) shadow_convert_kernel(const uint16_t* __restrict__ kv,
+                                                             const int32_t* __restrict__ pt, int32_t max_pages,
+                                                             int32_t num_pages, int32_t n_rows,
+                                                             uint16_t* __restrict__ shadow, uint32_t* status) {
+  const int64_t pieces = static_cast<int64_t>(n_rows) * 72;  // 8 values each
+  bool over = false, bad = false;
+  for (int64_t pc = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; pc < pieces;
+       pc += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(pc / 72), c = static_cast<int>(pc % 72);
+    const int lp = r >> 6;
+    const int pg = lp < max_pages ? __ldg(pt + lp) : -1;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (pg >= 0 && pg < num_pages) {
+      const uint4 v = ldg_stream(kv + (static_cast<int64_t>(pg) * kPage + (r & 63)) * kDqk + c * 8);
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        over |= ((in[t] & 0x7FFFu) > 0x477Fu) || ((in[t] & 0x7FFF0000u) > 0x477F0000u);
+        w[t] = bf16x2_to_f16x2(in[t]);
+      }
+      o = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      bad = true;
+    }
+    *reinterpret_cast<uint4*>(shadow + static_cast<int64_t>(r) * kDqk + c * 8) = o;
+  }
+  if (over) set_status(status, kStatusOverflow);
+  if (bad) set_status(status, kStatusBounds);
+}
+
 }  // namespace
+
+size_t mla_shadow_bytes(int32_t n_keys) {
+  return n_keys > 0 ? (static_cast<size_t>(n_keys) * kDqk * 2 + 255) / 256 * 256 : 0;
+}
+
+int launch_shadow_convert(const MlaLaunch& L) {
+  const int64_t pieces = static_cast<int64_t>(L.shadow_rows) * 72;
+  const int64_t want = (pieces + 255) / 256;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8LL * num_sms())));
+  shadow_convert_kernel<<<grid, 256, 0, L.stream>>>(static_cast<const uint16_t*>(L.cache->kv), L.page_tables,
+                                                   L.max_pages, L.cache->num_pages, L.shadow_rows,
+                                                   static_cast<uint16_t*>(L.shadow), L.status);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
 
 int launch_mla(const MlaLaunch& L) {
   MlaParams prm{};
@@ -662,6 +747,8 @@ int launch_mla(const MlaLaunch& L) {
   prm.lse = L.lse;
   prm.fp8 = L.cache->kv_dtype == SMLA_FP8_E4M3;
   prm.status = L.status;
+  prm.shadow = static_cast<const uint16_t*>(L.shadow);
+  prm.shadow_rows = L.shadow_rows;
   if (prm.n_rows == 0) return SMLA_OK;
   switch (L.n_heads) {
     case 16: return launch_t<16>(L, prm);

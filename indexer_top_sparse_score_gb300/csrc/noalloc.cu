@@ -29,8 +29,9 @@ extern "C" int smla_sparse_mla_prefill_noalloc(const smla_paged_cache* cache, co
                                                int32_t h_idx, int32_t topk, float sm_scale, void* out,
                                                float* lse, void* stream) {
   if (prefix_len < 0 || n_tokens <= 0 || topk <= 0) return SMLA_ERR_INVALID_ARG;
-  const size_t need = smla_sparse_mla_prefill_workspace_size(prefix_len, n_tokens, n_heads, h_idx, topk);
-  if (need > kNoAllocScratchBytes) return SMLA_ERR_WORKSPACE;  // n_tokens * topk * 4 + 256 > 16 MiB
+  // status word + index list must fit; the optional f16 copy of a BF16 cache is
+  // used only when it fits in what is left
+  if (smla::prefill_min_workspace(n_tokens, topk) > kNoAllocScratchBytes) return SMLA_ERR_WORKSPACE;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMLA_ERR_CUDA;
   void* scratch = nullptr;

@@ -25,7 +25,7 @@ def run_prefill(dev, chunk=0, want_idx=True):
     for c0 in range(0, T, step):
         c1 = min(T, c0 + step)
         P = dev.prefix_len + c0
-        need = smla.prefill_workspace_bytes(P, c1 - c0, H, spec.h_idx, spec.topk)
+        need = smla.prefill_workspace_bytes(P, c1 - c0, H, spec.h_idx, spec.topk, spec.kv_dtype)
         if ws is None or ws.numel() < need:
             ws = smla.workspace(need)
         smla.sparse_mla_prefill(dev.cache, dev.page_table, P, dev.q[c0:c1], dev.q_idx[c0:c1], dev.w[c0:c1],

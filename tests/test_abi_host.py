@@ -48,7 +48,7 @@ def _cache(**kw):
 
 def _prefill(L, cache, *, prefix=1000, T=4096, H=64, h_idx=32, topk=2048, ws_bytes=None, q=FAKE, out=FAKE,
              pt=FAKE, sm=0.04):
-    need = L.smla_sparse_mla_prefill_workspace_size(prefix, T, H, h_idx, topk)
+    need = L.smla_sparse_mla_prefill_workspace_size(prefix, T, H, h_idx, topk, cache.kv_dtype)
     ws = need if ws_bytes is None else ws_bytes
     return L.smla_sparse_mla_prefill(ctypes.byref(cache), pt, prefix, T, q, H, FAKE, FAKE, h_idx, topk, sm,
                                      out, FAKE, None, FAKE, ws, None)
@@ -90,9 +90,14 @@ def test_decode_and_indexer_argument_checks(L):
 
 def test_workspace_sizes(L):
     # prefill keeps the index list: status word + T x topk int32
-    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048) == 256 + 16384 * 2048 * 4
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4
+    # a BF16 cache adds an f16 copy of the sequence's rows (576 values x 2 bytes per key)
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 0) == \
+        256 + 16384 * 2048 * 4 + 16384 * 576 * 2
     # decode: candidate lists of every (row, 8192-key block) + counts + index list
     rows, nkb, k = 128, 16, 2048
     dec = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
     assert dec >= 256 + rows * nkb * k * 8 + rows * nkb * 4 + rows * k * 4
-    assert L.smla_sparse_mla_fwd_workspace_size(100, 64, 2048) == 256
+    assert L.smla_sparse_mla_fwd_workspace_size(0, 100, 64, 2048, 0) == 256
+    assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 1) == 256
+    assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 0) == 256 + 1000 * 1152
