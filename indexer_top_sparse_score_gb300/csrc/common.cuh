@@ -163,21 +163,24 @@ __device__ __forceinline__ bool selected(uint32_t key, uint32_t idx, uint32_t th
 // ---------------------------------------------------------------------------
 // Exact top-k threshold over entries held in shared memory: keys[0..n),
 // idxs[0..n) (n > k >= 1), 128 cooperating threads synchronised by `sync()`,
-// `hist` = 256 words, `red` = 16 words of shared scratch. Returns
+// `hist` = 3 x 256 words and `red` = 16 words of shared scratch. Returns
 // (thr_key, thr_idx): entry e is among the best k (key descending, index
 // ascending) iff key > thr_key, or key == thr_key and idx <= thr_idx.
 //
 // Method: a radix select whose bins span only the live key range [lo, hi]
-// (found by a min/max pass) and halve it by 8 bits per pass, so values that
+// (found by a min/max pass) and shrink it by 8 bits per pass, so values that
 // share a float exponent still spread over the bins; then, if the k-th key is
 // tied and not all ties are needed, the same on the indices of the ties
-// (ascending). Key passes read keys only, 4 per 16-byte load.
+// (ascending). Key passes read keys only, 4 per 16-byte load. Each pass costs
+// one barrier: histograms rotate over three buffers (the one a pass fills was
+// last read two passes ago and is cleared one pass ahead), and every warp
+// scans the finished histogram itself instead of waiting for a broadcast.
 template <typename Sync>
 __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* idxs, int n, int k, int tid,
                                           uint32_t* hist, uint32_t* red, Sync sync, uint32_t& thr_key,
                                           uint32_t& thr_idx) {
   const int lane = tid & 31, w = tid >> 5;
-  // visit keys (and optionally indices) 4 at a time; f(value, idx_or_0, valid)
+  int hb = 0;  // histogram buffer of the next pass
   auto each4 = [&](bool with_idx, auto f) {
     for (int e0 = tid * 4; e0 < n; e0 += 512) {
       const uint4 kv = *reinterpret_cast<const uint4*>(keys + e0);
@@ -189,26 +192,25 @@ __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* 
       f(kv.w, iv.w, e0 + 3 < n);
     }
   };
-  // min / max of a (filtered) value over all entries
-  auto minmax = [&](bool ties, uint32_t tk, uint32_t& lo, uint32_t& hi) {
-    uint32_t a = 0xFFFFFFFFu, b = 0;
+  // min / max of a (filtered) value; also clears the first histogram buffer
+  auto minmax = [&](bool ties, uint32_t tk, uint32_t& lo, uint32_t& hi, int slot) {
+    for (int b = tid; b < 256; b += 128) hist[256 * hb + b] = 0;
+    uint32_t a = 0xFFFFFFFFu, bmax = 0;
     each4(ties, [&](uint32_t kk, uint32_t ii, bool ok) {
-      if (!ok) return;
+      if (!ok || (ties && kk != tk)) return;
       const uint32_t v = ties ? ii : kk;
-      if (ties && kk != tk) return;
       a = min(a, v);
-      b = max(b, v);
+      bmax = max(bmax, v);
     });
     a = __reduce_min_sync(0xFFFFFFFFu, a);
-    b = __reduce_max_sync(0xFFFFFFFFu, b);
+    bmax = __reduce_max_sync(0xFFFFFFFFu, bmax);
     if (lane == 0) {
-      red[w] = a;
-      red[4 + w] = b;
+      red[slot + w] = a;
+      red[slot + 4 + w] = bmax;
     }
     sync();
-    lo = min(min(red[0], red[1]), min(red[2], red[3]));
-    hi = max(max(red[4], red[5]), max(red[6], red[7]));
-    sync();
+    lo = min(min(red[slot], red[slot + 1]), min(red[slot + 2], red[slot + 3]));
+    hi = max(max(red[slot + 4], red[slot + 5]), max(red[slot + 6], red[slot + 7]));
   };
   // narrow [lo, hi] to the bin holding the r-th value (descending for keys,
   // ascending for tie indices) until it is a single value
@@ -216,50 +218,51 @@ __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* 
     while (true) {
       const uint32_t range = hi - lo;
       const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
-      for (int b = tid; b < 256; b += 128) hist[b] = 0;
-      sync();
+      uint32_t* h = hist + 256 * hb;
+      uint32_t* hn = hist + 256 * ((hb + 1) % 3);
+      for (int b = tid; b < 256; b += 128) hn[b] = 0;  // next pass's buffer (read two passes ago)
       each4(ties, [&](uint32_t kk, uint32_t ii, bool ok) {
         if (!ok) return;
         const uint32_t v = ties ? ii : kk;
         if ((ties && kk != tk) || v < lo || v > hi) return;
-        atomicAdd(&hist[(v - lo) >> shift], 1u);
+        atomicAdd(&h[(v - lo) >> shift], 1u);
       });
       sync();
-      if (w == 0) {
-        // lane l owns 8 consecutive bins in scan order
-        uint32_t c[8], sum = 0;
+      hb = (hb + 1) % 3;
+      // every warp finds the bin holding the r-th value; lane l owns 8 consecutive bins
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int bin = ties ? 8 * lane + i : 255 - 8 * lane - i;
+        c[i] = h[bin];
+        sum += c[i];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t excl = incl - sum;
+      uint32_t mine = 0;
+      if (excl < static_cast<uint32_t>(r) && incl >= static_cast<uint32_t>(r)) {
+        uint32_t run = excl;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int bin = ties ? 8 * lane + i : 255 - 8 * lane - i;
-          c[i] = hist[bin];
-          sum += c[i];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const uint32_t excl = incl - sum;
-        if (excl < static_cast<uint32_t>(r) && incl >= static_cast<uint32_t>(r)) {
-          uint32_t run = excl;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (run + c[i] >= static_cast<uint32_t>(r)) {
-              red[8] = ties ? 8 * lane + i : 255 - 8 * lane - i;
-              red[9] = static_cast<uint32_t>(r) - run;
-              red[10] = c[i];
-              break;
-            }
-            run += c[i];
+          if (run + c[i] >= static_cast<uint32_t>(r)) {
+            const uint32_t bin = ties ? 8 * lane + i : 255 - 8 * lane - i;
+            mine = 0x80000000u | (bin << 16) | (static_cast<uint32_t>(r) - run);  // r <= k <= 2048: 16 bits
+            count = c[i];
+            break;
           }
+          run += c[i];
         }
       }
-      sync();
-      const uint32_t bin = red[8];
-      r = static_cast<int>(red[9]);
-      count = red[10];
-      sync();
+      const uint32_t found = __reduce_or_sync(0xFFFFFFFFu, mine);
+      const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine != 0)) - 1;
+      count = __shfl_sync(0xFFFFFFFFu, count, src);
+      const uint32_t bin = (found >> 16) & 0xFFu;
+      r = static_cast<int>(found & 0xFFFFu);
       const uint64_t nlo = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(bin) << shift);
       const uint64_t nhi = nlo + ((1ull << shift) - 1ull);
       lo = static_cast<uint32_t>(nlo);
@@ -270,16 +273,86 @@ __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* 
       }
     }
   };
-  uint32_t lo, hi, cnt;
+  uint32_t lo, hi, cnt = 0;
   int r = k;
-  minmax(false, 0, lo, hi);
+  minmax(false, 0, lo, hi, 0);
   refine(false, 0, lo, hi, r, thr_key, cnt);
   if (static_cast<uint32_t>(r) == cnt) {
     thr_idx = 0xFFFFFFFFu;
     return;
   }
-  minmax(true, thr_key, lo, hi);
+  minmax(true, thr_key, lo, hi, 8);  // other red[] slot: the first may still be read
   refine(true, thr_key, lo, hi, r, thr_idx, cnt);
+}
+
+// ---------------------------------------------------------------------------
+// Conservative cut for a buffer that only needs shrinking (not the exact top-k):
+// returns the largest L such that at least k entries have key >= L, to bin
+// resolution: one min/max pass and one histogram pass over the live range.
+// Every entry with key < L is beaten by k entries of the buffer and so by k
+// earlier keys. Same cooperation contract and scratch as wg_select.
+template <typename Sync>
+__device__ __forceinline__ uint32_t wg_cut(const uint32_t* keys, int n, int k, int tid, uint32_t* hist,
+                                           uint32_t* red, Sync sync) {
+  const int lane = tid & 31, w = tid >> 5;
+  for (int b = tid; b < 256; b += 128) hist[b] = 0;
+  uint32_t a = 0xFFFFFFFFu, bmax = 0;
+  for (int e0 = tid * 4; e0 < n; e0 += 512) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(keys + e0);
+    const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (e0 + q < n) {
+        a = min(a, v4[q]);
+        bmax = max(bmax, v4[q]);
+      }
+  }
+  a = __reduce_min_sync(0xFFFFFFFFu, a);
+  bmax = __reduce_max_sync(0xFFFFFFFFu, bmax);
+  if (lane == 0) {
+    red[w] = a;
+    red[4 + w] = bmax;
+  }
+  sync();
+  const uint32_t lo = min(min(red[0], red[1]), min(red[2], red[3]));
+  const uint32_t hi = max(max(red[4], red[5]), max(red[6], red[7]));
+  const uint32_t range = hi - lo;
+  const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
+  for (int e0 = tid * 4; e0 < n; e0 += 512) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(keys + e0);
+    const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (e0 + q < n) atomicAdd(&hist[(v4[q] - lo) >> shift], 1u);
+  }
+  sync();
+  uint32_t c[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = hist[255 - 8 * lane - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const uint32_t excl = incl - sum;
+  uint32_t mine = 0;
+  if (excl < static_cast<uint32_t>(k) && incl >= static_cast<uint32_t>(k)) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (run + c[i] >= static_cast<uint32_t>(k)) {
+        mine = 0x80000000u | (255u - 8u * lane - i);
+        break;
+      }
+      run += c[i];
+    }
+  }
+  const uint32_t bin = __reduce_or_sync(0xFFFFFFFFu, mine) & 0xFFu;
+  return lo + (bin << shift);
 }
 
 }  // namespace smla

@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* ckey = reinterpret_cast<uint32_t*>(b_tile + kMaxN * kIdxRowBytes);
   uint32_t* cidx = ckey + kBufEntries;
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][256]
-  uint32_t* scratch = hist + 512;                               // [2][16]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]
+  uint32_t* scratch = hist + 1536;                              // [2][16]
   int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [128]
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 128);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant of this warp
     const int tid_wg = (ew & 3) * 32 + lane;
     const uint32_t bar_wg = 1 + wg;
-    uint32_t* hist_wg = hist + 256 * wg;
+    uint32_t* hist_wg = hist + 768 * wg;
     uint32_t* scr_wg = scratch + 16 * wg;
     uint32_t* wsum_wg = wsum + 8 * wg;
     auto wg_sync = [&]() { named_bar_sync(bar_wg, 128); };
@@ -320,23 +320,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* ib = cidx + j * cap;
       uint32_t tk = 0, ti = 0xFFFFFFFFu;
       const bool all = n <= keep;
-      if (!all) wg_select(kb, ib, n, keep, tid_wg, hist_wg, scr_wg, wg_sync, tk, ti);
+      bool cut = false;  // mid-stream: keep key >= tk (a superset of the top-k)
+      if (!all) {
+        if (!to_output) {
+          tk = wg_cut(kb, n, keep, tid_wg, hist_wg, scr_wg, wg_sync);
+          // the cut bin may hold many ties; fall back to the exact selection
+          // when the cut would not free a full tile of room
+          uint32_t kept = 0;
+          for (int e = tid_wg; e < n; e += 128) kept += kb[e] >= tk;
+          kept = __reduce_add_sync(0xFFFFFFFFu, kept);
+          if ((tid_wg & 31) == 0) scr_wg[12 + (tid_wg >> 5)] = kept;
+          wg_sync();
+          kept = scr_wg[12] + scr_wg[13] + scr_wg[14] + scr_wg[15];
+          cut = static_cast<int>(kept) <= cap - 2 * kTileKeys;
+          wg_sync();
+        }
+        if (!cut) wg_select(kb, ib, n, keep, tid_wg, hist_wg, scr_wg, wg_sync, tk, ti);
+      }
       const int row = it.row0 + j;
       int base = 0;
-      for (int r0 = 0, rnd = 0; r0 < n; r0 += 512, ++rnd) {
-        const int e0 = r0 + tid_wg * 4;
-        uint4 kv = make_uint4(0, 0, 0, 0), iv = make_uint4(0, 0, 0, 0);
-        if (e0 < n) {
-          kv = *reinterpret_cast<const uint4*>(kb + e0);
-          iv = *reinterpret_cast<const uint4*>(ib + e0);
-        }
-        const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w}, ii[4] = {iv.x, iv.y, iv.z, iv.w};
-        bool take[4];
+      // rounds of 2048 entries: thread t owns e = r0 + 4t + 512v + q (v, q < 4);
+      // every write lands below the round's end, after all of its reads
+      for (int r0 = 0, rnd = 0; r0 < n; r0 += 2048, ++rnd) {
+        uint32_t kk[16], ii[16];
+        bool take[16];
         int c = 0;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          take[q4] = e0 + q4 < n && (all || selected(kk[q4], ii[q4], tk, ti));
-          c += take[q4];
+        for (int v = 0; v < 4; ++v) {
+          const int e0 = r0 + 4 * tid_wg + 512 * v;
+          uint4 kv = make_uint4(0, 0, 0, 0), iv = make_uint4(0, 0, 0, 0);
+          if (e0 < n) {
+            kv = *reinterpret_cast<const uint4*>(kb + e0);
+            iv = *reinterpret_cast<const uint4*>(ib + e0);
+          }
+          kk[4 * v + 0] = kv.x; kk[4 * v + 1] = kv.y; kk[4 * v + 2] = kv.z; kk[4 * v + 3] = kv.w;
+          ii[4 * v + 0] = iv.x; ii[4 * v + 1] = iv.y; ii[4 * v + 2] = iv.z; ii[4 * v + 3] = iv.w;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            take[4 * v + q4] = e0 + q4 < n && (all || (cut ? kk[4 * v + q4] >= tk
+                                                            : selected(kk[4 * v + q4], ii[4 * v + q4], tk, ti)));
+            c += take[4 * v + q4];
+          }
         }
         int incl = c;
 #pragma unroll
@@ -356,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         off += incl - c;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 16; ++q4) {
           if (!take[q4]) continue;
           if (!to_output) {
             kb[off] = kk[q4];
@@ -386,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wg_sync();
       if (!to_output && tid_wg == 0) {
         cnt[j] = base;
-        theta[j] = tk;
+        // admit later keys only above the cut (exact: above the k-th key; a
+        // later key equal to it loses the tie to every kept entry)
+        theta[j] = cut ? (tk > 0 ? tk - 1 : 0) : tk;
       }
       wg_sync();
     };
@@ -583,7 +609,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      512 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + 16 * 8 + 16;
+                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + 16 * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
