@@ -16,6 +16,7 @@ the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -47,6 +48,34 @@ def peaks():
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sust=d["bf16_tflops_sustained"],
                     src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+def kernel_sources_digest():
+    """SHA-256 (first 16 hex digits) of the kernel sources and the C header,
+    each file hashed as its repository path then its bytes, in path order."""
+    csrc = os.path.join("indexer_top_sparse_score_gb300", "csrc")
+    rel = sorted([os.path.join(csrc, f) for f in os.listdir(os.path.join(ROOT, csrc))
+                  if os.path.isfile(os.path.join(ROOT, csrc, f))] + [os.path.join("include", "smla.h")])
+    h = hashlib.sha256()
+    for r in rel:
+        h.update(r.replace(os.sep, "/").encode())
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel, summary="dram_traffic_prefill16k.md"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    digest = kernel_sources_digest()
+    for line in open(path):
+        f = line.split()
+        if len(f) == 5 and f[0] == "traffic" and f[1] == kernel and f[3] == "sources":
+            return int(f[2]) if f[4] == digest else None
+    return None
 
 
 def dist_setup(n_gpus):
@@ -318,7 +347,9 @@ def main():
             "peak": pk["bf16"] if dominant_is_mla else fp8_peak,
             "peak_src": (f"{pk['src']} bf16 burst" if dominant_is_mla else
                          f"{pk['src']} bf16 burst x2 (nominal fp8/bf16 ratio)"),
-            "traffic": None}
+            "traffic": measured_traffic("mla_kernel" if dominant_is_mla else "indexer_kernel")}
+    if T != wl.SPECS[args.workload].n_tokens:
+        roof["traffic"] = None  # the capture is of the full-size workload
     roof["frac"] = roof["achieved"] / roof["peak"]
     kernels = {
         "indexer_topk": {"ms": ms_idx, "share": ms_idx / (ms_idx + ms_mla), "tflops_fp8": idx_tflops,
@@ -340,7 +371,8 @@ def main():
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse"},
-        "gpu_launches": 2 * args.steps,
+        # per step: indexer_kernel, shadow_convert_kernel (BF16 cache only), mla_kernel
+        "gpu_launches": (3 if spec.kv_dtype == "bf16" else 2) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:
