@@ -188,7 +188,7 @@ def run_reference(args, rank, world):
     spec = wl.SPECS[WORKLOAD]
     dev_name = "cuda" if torch.cuda.is_available() else "cpu"
     dev = wl.make(spec, dev_name)
-    rows_per_step = 32
+    rows_per_step = 256
     for _ in range(args.warmup):
         cpu_oracle_sample(spec, dev, 4)
     vals = []
@@ -257,7 +257,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=2560)
     ap.add_argument("--workload", default=WORKLOAD, choices=["prefill16k"],
                     help="benchmarked workload (the 16,384-token prefill)")
     ap.add_argument("--tokens", type=int, default=0,
