@@ -68,8 +68,9 @@ typedef enum smla_dtype {
  *   k_idx       [num_pages][page_size][d_idx] idx_dtype: indexer keys.
  *   k_idx_scale [num_pages][page_size] fp32 positive per-key indexer scale, or
  *               NULL for 1 (footnote 3's 132-byte key = 128 FP8 + 4-byte scale).
- * page_size must be 64. An indexer row must be 128 bytes: d_idx = 128 for
- * e4m3 keys, d_idx = 64 for bf16 keys. */
+ * page_size must be 64 and num_pages at most 2^25 (pool rows are indexed
+ * with 32-bit integers; more is SMLA_ERR_UNSUPPORTED). An indexer row must be
+ * 128 bytes: d_idx = 128 for e4m3 keys, d_idx = 64 for bf16 keys. */
 typedef struct smla_paged_cache {
   const void* kv;
   const float* kv_scale;

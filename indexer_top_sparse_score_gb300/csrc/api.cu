@@ -37,6 +37,7 @@ int check_cache(const smla_paged_cache* c, bool need_kv, bool need_idx) {
   if (c->page_size != kPage || c->num_pages <= 0) return c->page_size != kPage && c->page_size > 0
                                                                ? SMLA_ERR_UNSUPPORTED
                                                                : SMLA_ERR_INVALID_ARG;
+  if (c->num_pages > (1 << 25)) return SMLA_ERR_UNSUPPORTED;  // pool rows must fit int32
   if (need_kv) {
     if (!c->kv || !aligned16(c->kv)) return SMLA_ERR_INVALID_ARG;
     if (c->kv_dtype != SMLA_BF16 && c->kv_dtype != SMLA_FP8_E4M3) return SMLA_ERR_INVALID_ARG;

@@ -7,20 +7,27 @@
 //     out  = softmax_j(l) . K[s_j, 0:512],   lse = log sum_j exp(l_j)
 //
 // One CTA per SM (persistent); query rows are handed out in head/tail pairs
-// (cheap causal rows with expensive ones). For each row the 2048 selected
-// rows stream through in blocks of 64:
-//   warps 8-15  gather producers: resolve key -> page -> pool row, load the
-//               row, widen it to f16 (bf16 -> f16 or e4m3 -> f16) and store it
-//               into a 128B-swizzled shared tile, 2 stages; they also widen
-//               the query to f16 once per query row;
-//   warp 0      MMA issuer:  S[64 heads x 64 rows] = Q . K^T   (tcgen05,
-//               M=64, K=576) into one of two TMEM S buffers, and
-//               O^T[512 x H] += V^T . P^T  (M=128 per 128-dim slice of V, the
-//               same shared tile read MN-major, P^T from shared memory);
-//   warps 4-7   softmax: S from TMEM (two threads per head), online softmax
-//               in the log2 domain with a lazy rescale (O is only rescaled
-//               when a head's running max grows by more than 2^8), P to
-//               shared memory; finally O^T from TMEM, normalised, to HBM.
+// (cheap causal rows with expensive ones). For each query row the selected
+// rows stream through in blocks of 128, and every product is computed with
+// the block's rows on the 128 TMEM lanes, so both MMAs run at M = 128:
+//   S^T[128 rows x H]   = K_blk . Q^T            (K = 576)
+//   O^T[512 x H]       += V_blk^T . P^T           (four M = 128 slices, K = 128)
+// The block's rows live in one 144 KB shared tile of nine 64-value chunks,
+// filled in five groups ({0,1} {2,3} {4,5} {6,7} {8}). PV slice d frees
+// group d, so the next block's chunks load while PV is still running; the
+// rope chunk (8) holds P^T once QK has read it.
+//   warps 8-15  gather producers: key -> page -> pool row, row pieces into the
+//               swizzled tile (cp.async from an f16 copy of the rows, or load +
+//               widen bf16/e4m3 -> f16), per-row logit/probability scales; they
+//               also widen the query to f16 once per query row;
+//   warp 0      MMA issuer (one thread);
+//   warps 4-7   softmax, one thread per selected row: logits of all heads of
+//               its row, online softmax in the log2 domain against a per-head
+//               reference max that is only raised (and O, l rescaled) when a
+//               logit exceeds it by more than 2^8, P^T row to shared memory,
+//               per-row partial sums of P in TMEM; at the end of a query row
+//               the partial sums are reduced across rows and O^T is
+//               normalised and written out.
 // All MMA operands are f16: e4m3 -> f16 is exact and bf16 -> f16 is exact in
 // the f16 normal range, and f16 gives the probabilities 11 significant bits
 // (bf16 would give 8, which alone costs ~1e-3 relative output error). For
@@ -38,19 +45,17 @@ namespace smla {
 
 namespace {
 
-constexpr int kBlk = 64;                     // selected rows per block
-constexpr int kChunks = kDqk / 64;           // 9 chunks of 64 values
-constexpr int kChunkBytes = kBlk * 128;      // 8 KB
-constexpr int kTileBytes = kChunks * kChunkBytes;  // 72 KB per stage / for Q
-// P^T (64 head rows x 64 selected rows, f16) of block b is written into the
-// rope chunk (chunk 8) of block b's own stage: QK(b) has finished reading it
-// once S(b) is ready, and the stage is not refilled before PV(b) completes.
-// Every block therefore has its own P buffer, and the softmax of block b+1
-// never waits for PV(b) unless it has to rescale O.
-constexpr int kPChunk = kChunks - 1;
+constexpr int kBlk = 128;                          // selected rows per block (MMA M)
+constexpr int kChunks = kDqk / 64;                 // 9 chunks of 64 values
+constexpr int kChunkBytes = kBlk * 128;            // 16 KB: 128 rows x 64 f16
+constexpr int kStageBytes = kChunks * kChunkBytes;  // 144 KB
+constexpr int kQChunkBytes = 64 * 128;             // 8 KB: up to 64 heads x 64 f16
+constexpr int kQBytes = kChunks * kQChunkBytes;    // 72 KB
+constexpr int kGroups = 5;                         // chunk groups {0,1} {2,3} {4,5} {6,7} {8}
+constexpr int kPChunk = kChunks - 1;               // rope chunk, reused for P^T after QK
 constexpr int kThreads = 512;
-constexpr int kProducers = 256;          // warps 8-15
-constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
+constexpr int kProducers = 128;                    // warps 12-15
+constexpr uint32_t kColO = 0, kColS = 256, kColL = 320, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct MlaParams {
@@ -73,22 +78,21 @@ struct MlaParams {
   int32_t shadow_rows;
 };
 
-// Per selected row j of a stage: {logit multiplier, bias (0, or -inf for a
-// skipped row)} and the probability multiplier (FP8 token scale). Rows 32..63
-// sit one slot further so the two halves of a softmax warp hit different banks.
-__host__ __device__ constexpr int meta_slot(int j) { return j + (j >= 32 ? 1 : 0); }
-
 struct SmemMeta {
-  float2 col[2][kBlk + 1];
-  float pscale[2][kBlk + 1];
+  // per selected row of a block (two blocks in flight): {logit multiplier,
+  // probability multiplier, valid, -}
+  float4 row[2][kBlk];
+  float m[64];        // reference max per head (log2 domain)
+  float alpha[64];    // rescale factor per head
+  float red[4][64];   // cross-warp reduction
   float linv[64];
-  float alpha[64];
-  uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], o_empty;
+  uint64_t q_full, q_empty, full[kGroups], empty[4], s_full, p_full, o_empty;
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 2 * kTileBytes + kTileBytes + sizeof(SmemMeta);
+constexpr size_t kSmemBytes = kQBytes + kStageBytes + sizeof(SmemMeta);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // k-th row of this CTA: head/tail pairs. -1 done, 0 skip, 1 row.
 __device__ __forceinline__ int next_row(int n_rows, int k, int& row) {
@@ -113,18 +117,6 @@ __device__ __forceinline__ RowInfo row_info(const MlaParams& p, int row) {
   r.nvalid = max(0, min(p.topk, r.pos + 1));
   r.nb = (r.nvalid + kBlk - 1) / kBlk;
   return r;
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
@@ -157,6 +149,9 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
+__device__ __forceinline__ bool bf16x2_over_f16(uint32_t w) {
+  return ((w & 0x7FFFu) > 0x477Fu) || ((w & 0x7FFF0000u) > 0x477F0000u);
+}
 // 16-byte global load that bypasses L1 (each row is read once per block)
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
@@ -173,12 +168,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
 
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
-  if constexpr (NC == 16) tmem_ld_32x32b_x16(taddr, r);
+  static_assert(NC == 8 || NC == 16 || NC == 32, "columns");
+  if constexpr (NC == 8) tmem_ld_32x32b_x8(taddr, r);
+  else if constexpr (NC == 16) tmem_ld_32x32b_x16(taddr, r);
   else tmem_ld_32x32b_x32(taddr, r);
 }
 template <int NC>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
-  if constexpr (NC == 16) {
+  static_assert(NC == 8 || NC == 16 || NC == 32, "columns");
+  if constexpr (NC == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+  } else if constexpr (NC == 16) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -190,41 +192,67 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) 
   }
 }
 
+// Warp reduce-scatter of NV values per lane (NV = 8, 16 or 32): afterwards
+// lane L holds op over all lanes of value L / (32 / NV).
+template <int NV, typename Op>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane, Op op) {
+  static_assert(NV == 8 || NV == 16 || NV == 32, "values per lane");
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int off = 16 >> s;
+    const int n = NV >> s;  // values still held before this step
+    if (n > 1) {
+      const bool up = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < n / 2) {
+          const float send = up ? v[i] : v[i + n / 2];
+          const float keep = up ? v[i + n / 2] : v[i];
+          v[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, off));
+        }
+      }
+    } else {
+      v[0] = op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], off));
+    }
+  }
+  return v[0];
+}
+
+struct MaxOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct AddOp {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+
+// Byte offset of 16-byte piece j of row r in a 128B-swizzled tile of 128-byte rows.
+__device__ __forceinline__ uint32_t sw_off(int r, int j) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
 template <int H>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const MlaParams p) {
+  static_assert(H == 16 || H == 64, "heads");
+  constexpr int kHalf = H < 32 ? H : 32;  // heads per softmax pass
+  constexpr int kHalves = H / kHalf;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_tile = smem;
-  uint8_t* stage = smem + kTileBytes;  // 2 stages
-  SmemMeta& M = *reinterpret_cast<SmemMeta*>(smem + 3 * kTileBytes);
-
-  constexpr int kColChunk = H < 32 ? H : 32;
+  uint8_t* stage = smem + kQBytes;
+  SmemMeta& M = *reinterpret_cast<SmemMeta*>(smem + kQBytes + kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(p.status, kStatusSetup);
     return;
   }
-  // Q rows H..63 stay zero (the QK MMA always has M = 64)
-  if (H < 64) {
-    for (int i = threadIdx.x; i < kTileBytes / 16; i += kThreads) {
-      const int rowb = (i * 16 % kChunkBytes) / 128;
-      if (rowb >= H) reinterpret_cast<uint4*>(q_tile)[i] = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
-  }
   if (threadIdx.x == 0) {
     mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&M.kv_full[i], kProducers);
-      mbar_init(&M.kv_empty[i], 1);
-      mbar_init(&M.s_full[i], 1);
-      mbar_init(&M.s_empty[i], 4);
-      // per stage: the softmax may finish P(b+1) before PV(b) is issued, so one
-      // barrier for all blocks could run two phases ahead of the MMA thread
-      mbar_init(&M.p_full[i], 4);
-    }
-    mbar_init(&M.o_empty, 4);
+    for (int i = 0; i < kGroups; ++i) mbar_init(&M.full[i], kProducers);
+    for (int i = 0; i < 4; ++i) mbar_init(&M.empty[i], 1);
+    mbar_init(&M.s_full, 1);
+    mbar_init(&M.p_full, 8);
+    mbar_init(&M.o_empty, 8);
     M.abort_flag = 0;
     fence_mbar_init();
   }
@@ -241,153 +269,83 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA
-    // One thread issues QK^T and PV for the CTA's rows in whatever order their
-    // inputs become ready: QK(b) needs the gathered tile and a free S buffer,
-    // PV(b) needs P(b) (and, for a row's first block, the previous row's O
-    // read out). Polling both keeps PV(b) from waiting behind QK(b+1)'s gather.
+    // Per block: QK^T chunk group by chunk group as the groups arrive, then
+    // (after the softmax) PV slice by slice, each slice's commit freeing the
+    // chunks it read. The tensor pipe runs them in issue order.
     if (lane == 0) {
-      const uint32_t idesc_qk = instr_desc(64, 64, fmt, fmt, false, false);
-      const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, false);
+      const uint32_t idesc_qk = instr_desc(128, H, fmt, fmt, false, false);
+      const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, true);
       const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage);
-      // K-major 128B-swizzled operands: SBO = 1024 (8-row groups); the gathered
-      // tile read MN-major as V^T: LBO = one 64-value chunk of all rows.
+      // K-major operands (rows of 128 bytes, 8-row groups 1024 bytes apart):
+      // the gathered rows (A of QK) and the query (B of QK). MN-major operands:
+      // the same rows read as V^T (A of PV; the two 64-value chunks of a
+      // 128-value slice are one chunk apart) and P^T (B of PV).
+      const uint64_t k_desc = smem_desc(st0, 16, 1024);
       const uint64_t q_desc = smem_desc(q0, 16, 1024);
-      const uint64_t st_desc0 = smem_desc(st0, 16, 1024), st_desc1 = smem_desc(st0 + kTileBytes, 16, 1024);
-      const uint64_t vt_desc0 = smem_desc(st0, kChunkBytes, 1024);
-      const uint64_t vt_desc1 = smem_desc(st0 + kTileBytes, kChunkBytes, 1024);
-      const uint64_t p_desc0 = smem_desc(st0 + kPChunk * kChunkBytes, 16, 1024);
-      const uint64_t p_desc1 = smem_desc(st0 + kTileBytes + kPChunk * kChunkBytes, 16, 1024);
-      struct Cursor {
-        int k, b, nb;
-        uint32_t g, tok;
-        bool done;
-      };
-      auto seek = [&](Cursor& c) {
-        while (true) {
-          int row;
-          const int r = next_row(p.n_rows, c.k, row);
-          if (r < 0) { c.done = true; return; }
-          if (r == 0) { ++c.k; continue; }
-          c.nb = row_info(p, row).nb;
-          c.b = 0;
-          if (c.nb > 0) return;
-          ++c.k;
-        }
-      };
-      Cursor qc{0, 0, 0, 0, 0, false}, pc{0, 0, 0, 0, 0, false};
-      seek(qc);
-      seek(pc);
-      long long t_last = clock64();
-      while (!pc.done) {
-        bool prog = false;
-        if (!qc.done) {
-          const uint32_t gq = qc.g;
-          const int s = gq & 1;
-          if ((qc.b != 0 || mbar_test(&M.q_full, qc.tok & 1)) && mbar_test(&M.kv_full[s], (gq >> 1) & 1) &&
-              mbar_test(&M.s_empty[s], ((gq >> 1) & 1) ^ 1)) {
+      const uint64_t vt_desc = smem_desc(st0, kChunkBytes, 1024);
+      const uint64_t p_desc = smem_desc(st0 + kPChunk * kChunkBytes, kChunkBytes, 1024);
+      uint32_t g = 0, tok = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int row;
+        const int r = next_row(p.n_rows, k, row);
+        if (r < 0) break;
+        if (r == 0) continue;
+        const RowInfo ri = row_info(p, row);
+        if (ri.nb == 0) continue;
+        if (!mbar_wait(&M.q_full, tok & 1, abort_v, p.status)) break;
+        for (int b = 0; b < ri.nb; ++b, ++g) {
+          const uint32_t ph = g & 1;
+#pragma unroll 1
+          for (int grp = 0; grp < kGroups; ++grp) {
+            if (!mbar_wait(&M.full[grp], ph, abort_v, p.status)) { ok = false; break; }
             tc_fence_after();
-            // descriptors advance by (byte offset >> 4) in their start-address field
-            const uint64_t bd0 = s ? st_desc1 : st_desc0;
-            const uint32_t dS = tmem + kColS + s * 64;
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t off = static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
-                mma_f16(dS, q_desc + off, bd0 + off, idesc_qk, (c | kk) != 0);
-              }
-            mma_commit(&M.s_full[s]);
-            ++qc.g;
-            if (++qc.b == qc.nb) {
-              mma_commit(&M.q_empty);  // all QK of this row issued: Q may be replaced once they finish
-              ++qc.tok;
-              ++qc.k;
-              seek(qc);
-            }
-            prog = true;
-          }
-        }
-        if (pc.g < qc.g || (qc.done && !pc.done)) {
-          const uint32_t gp = pc.g;
-          if (mbar_test(&M.p_full[gp & 1], (gp >> 1) & 1) && (pc.b != 0 || mbar_test(&M.o_empty, (pc.tok & 1) ^ 1))) {
-            tc_fence_after();
-            const uint64_t ad0 = (gp & 1) ? vt_desc1 : vt_desc0;
-            const uint64_t p_desc = (gp & 1) ? p_desc1 : p_desc0;
-#pragma unroll
-            for (int dt = 0; dt < 4; ++dt)
+            const int c1 = grp < 4 ? 2 * grp + 2 : kChunks;
+#pragma unroll 1
+            for (int c = 2 * grp; c < c1; ++c) {
+              const uint64_t ka = k_desc + static_cast<uint64_t>((c * kChunkBytes) >> 4);
+              const uint64_t qb = q_desc + static_cast<uint64_t>((c * kQChunkBytes) >> 4);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_f16(tmem + kColO + dt * 64, ad0 + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
-                        p_desc + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (pc.b | kk) != 0);
-            mma_commit(&M.kv_empty[gp & 1]);
-            ++pc.g;
-            if (++pc.b == pc.nb) {
-              ++pc.tok;
-              ++pc.k;
-              seek(pc);
+                mma_f16(tmem + kColS, ka + static_cast<uint64_t>(kk * 2), qb + static_cast<uint64_t>(kk * 2),
+                        idesc_qk, (c | kk) != 0);
             }
-            prog = true;
           }
-        }
-        if (prog) {
-          t_last = clock64();
-        } else {
-          if (*abort_v) break;
-          if (clock64() - t_last > kWaitLimitCycles) {
-            set_status(p.status, kStatusTimeout);
-            *abort_v = 1;
+          if (!ok) break;
+          mma_commit(&M.s_full);
+          if (b == ri.nb - 1) mma_commit(&M.q_empty);  // Q may be replaced once these finish
+          if (!mbar_wait(&M.p_full, ph, abort_v, p.status) ||
+              (b == 0 && !mbar_wait(&M.o_empty, (tok & 1) ^ 1, abort_v, p.status))) {
+            ok = false;
             break;
           }
-        }
-      }
-    }
-  } else if (warp >= 8) {
-    // ---------------------------------------------------------------- gather producers
-    // Eight threads per selected row read consecutive 16-byte pieces (one
-    // 128-byte line per row per load), 32 rows per pass, two passes per
-    // 64-row block. The loads of block b+1 are issued right after block b is
-    // stored (registers act as a third stage) and the key -> page lookups of
-    // the next block run while the current block's data is in flight.
-    const int tid = threadIdx.x - 256;
-    const int rr = tid >> 3, part = tid & 7;  // row within a pass, piece lane
-    constexpr int kPB = 9;                    // BF16: 72 pieces per row / 8 threads
-    constexpr int kP8 = 5;                    // FP8: 36 pieces per row / 8 threads (rounded up)
-    uint32_t g = 0, tok = 0;
-    uint4 v[2][kPB];
-    auto lookup = [&](const RowInfo& ri, const int32_t* ir, const int32_t* pt, int b, int jrow) -> int64_t {
-      const int e = b * kBlk + jrow;
-      if (e >= ri.nvalid) return -1;
-      const int key = __ldg(ir + e);
-      if (key < 0 || key > ri.pos) return -1;
-      if (p.shadow) return key < p.shadow_rows ? key : -1;  // shadow rows are logical positions
-      const int lp = key >> 6;
-      const int pg = lp < p.max_pages ? __ldg(pt + lp) : -1;
-      if (pg < 0 || pg >= p.num_pages) {
-        set_status(p.status, kStatusBounds);
-        return -1;
-      }
-      return static_cast<int64_t>(pg) * kPage + (key & 63);
-    };
-    auto load_block = [&](const int64_t* prow) {
-      if (p.shadow) return;  // shadow rows are copied with cp.async once the stage is free
+          tc_fence_after();
+#pragma unroll 1
+          for (int dt = 0; dt < 4; ++dt) {
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        if (!p.fp8) {
-          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv) + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
-#pragma unroll
-          for (int u = 0; u < kPB; ++u)
-            v[h2][u] = prow[h2] >= 0 ? ldg_stream(src + (part + 8 * u) * 8) : make_uint4(0, 0, 0, 0);
-        } else {
-          const uint8_t* src = p.kv + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
-#pragma unroll
-          for (int u = 0; u < kP8; ++u) {
-            const int pc = part + 8 * u;
-            v[h2][u] = (prow[h2] >= 0 && pc < 36) ? ldg_stream(src + pc * 16) : make_uint4(0, 0, 0, 0);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16(tmem + kColO + dt * 64,
+                      vt_desc + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
+                      p_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (b | kk) != 0);
+            mma_commit(&M.empty[dt]);
           }
         }
+        ++tok;
       }
-    };
+    }
+  } else if (warp >= 12) {
+    // ---------------------------------------------------------------- gather producers
+    // Warp pw owns rows 32pw..32pw+31 of every block: lane l resolves the key
+    // of row 32pw+l (keys two blocks ahead, page ids one block ahead), and a
+    // chunk is copied in 8 passes of 4 rows x 8 pieces of 16 bytes, so every
+    // warp instruction touches 4 full 128-byte lines.
+    const int pw = warp - 12;
+    const int tid = threadIdx.x - 384;
+    const int psub = lane >> 3, pj = lane & 7;  // pass row offset, 16-byte piece
+    const uint32_t st0 = smem_u32(stage);
+    uint32_t g = 0, tok = 0;
     bool ok = true;
+    bool over = false;
     for (int k = 0; ok; ++k) {
       int row;
       const int r = next_row(p.n_rows, k, row);
@@ -397,264 +355,334 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ri.nb == 0) continue;
       const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
       const int32_t* ir = p.idx + static_cast<size_t>(row) * p.topk;
+      auto fetch_key = [&](int b) -> int {
+        const int e = b * kBlk + 32 * pw + lane;
+        return (b < ri.nb && e < ri.nvalid) ? __ldg(ir + e) : -1;
+      };
+      auto fetch_page = [&](int key) -> int {
+        if (p.shadow || key < 0 || key > ri.pos) return 0;
+        const int lp = key >> 6;
+        return lp < p.max_pages ? __ldg(pt + lp) : -1;
+      };
+      // pool (or shadow) row of a key, -1 when it is masked or out of range
+      auto locate = [&](int key, int pg) -> int {
+        if (key < 0 || key > ri.pos) return -1;
+        if (p.shadow) return key < p.shadow_rows ? key : -1;
+        if (pg < 0 || pg >= p.num_pages) {
+          set_status(p.status, kStatusBounds);
+          return -1;
+        }
+        return pg * kPage + (key & 63);
+      };
       // widen the BF16 query to f16 into the swizzled Q tile
       {
         const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
         constexpr int kQPieces = (H * 72 + kProducers - 1) / kProducers;
-        uint4* vq = &v[0][0];
+        constexpr int kQBatch = 12;
+#pragma unroll 1
+        for (int u0 = 0; u0 < kQPieces; u0 += kQBatch) {
+          uint4 vq[kQBatch];
 #pragma unroll
-        for (int u = 0; u < kQPieces; ++u) {
-          const int pc = tid + u * kProducers;
-          const int h = pc / 72, pp = pc - h * 72;
-          if (pc < H * 72) vq[u] = ldg_stream(qr + h * kDqk + pp * 8);
-        }
-        int64_t prow[2] = {lookup(ri, ir, pt, 0, rr), lookup(ri, ir, pt, 0, rr + 32)};
-        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) break;
-        bool over = false;
-#pragma unroll
-        for (int u = 0; u < kQPieces; ++u) {
-          const int pc = tid + u * kProducers;
-          if (pc >= H * 72) break;
-          const int h = pc / 72, pp = pc - h * 72;
-          const uint32_t in[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
-          uint32_t o[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            over |= ((in[t] & 0x7FFFu) > 0x477Fu) || ((in[t] & 0x7FFF0000u) > 0x477F0000u);
-            o[t] = bf16x2_to_f16x2(in[t]);
+          for (int u = 0; u < kQBatch; ++u) {
+            const int pc = tid + (u0 + u) * kProducers;
+            const int h = pc / 72, pp = pc - h * 72;
+            if (u0 + u < kQPieces && pc < H * 72) vq[u] = ldg_stream(qr + h * kDqk + pp * 8);
           }
-          const int c = pp >> 3, qq = pp & 7;
-          *reinterpret_cast<uint4*>(q_tile + c * kChunkBytes + h * 128 + ((qq ^ (h & 7)) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
+          if (u0 == 0 && !mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
+#pragma unroll
+          for (int u = 0; u < kQBatch; ++u) {
+            const int pc = tid + (u0 + u) * kProducers;
+            if (u0 + u >= kQPieces || pc >= H * 72) break;
+            const int h = pc / 72, pp = pc - h * 72;
+            const uint32_t in[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              over |= bf16x2_over_f16(in[t]);
+              o[t] = bf16x2_to_f16x2(in[t]);
+            }
+            *reinterpret_cast<uint4*>(q_tile + (pp >> 3) * kQChunkBytes + sw_off(h, pp & 7)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+          }
         }
-        if (over) set_status(p.status, kStatusOverflow);
+        if (!ok) break;
         fence_proxy_async_smem();
         named_bar_sync(2, kProducers);
         if (tid == 0) mbar_arrive(&M.q_full);
-        load_block(prow);
-        for (int b = 0; b < ri.nb; ++b, ++g) {
-          const int s = g & 1;
-          int64_t prow_next[2] = {-1, -1};
-          if (b + 1 < ri.nb) {
-            prow_next[0] = lookup(ri, ir, pt, b + 1, rr);
-            prow_next[1] = lookup(ri, ir, pt, b + 1, rr + 32);
-          }
-          float ks[2] = {1.0f, 1.0f};
-          if (p.fp8 && part == 0) {
-            if (prow[0] >= 0) ks[0] = __ldg(p.kv_scale + prow[0]);
-            if (prow[1] >= 0) ks[1] = __ldg(p.kv_scale + prow[1]);
-          }
-          if (!mbar_wait(&M.kv_empty[s], ((g >> 1) & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
+      }
+      int key0 = fetch_key(0), key1 = fetch_key(1);
+      int pg0 = fetch_page(key0);
+      for (int b = 0; b < ri.nb && ok; ++b, ++g) {
+        const int loc = locate(key0, pg0);
+        float ks = 1.0f;
+        if (p.fp8 && loc >= 0) ks = __ldg(p.kv_scale + loc);
+        const int key2 = fetch_key(b + 2);
+        const int pg1 = fetch_page(key1);
+        int rl[8];  // pool rows of this lane's copy passes
 #pragma unroll
-          for (int h2 = 0; h2 < 2 && !p.shadow; ++h2) {
-            const int j = rr + 32 * h2;
-            uint8_t* rowp = stage + s * kTileBytes + j * 128;
-            if (part == 0) {
-              M.col[s][meta_slot(j)] = prow[h2] >= 0 ? make_float2(ks[h2] * p.scale_log2, 0.0f)
-                                                     : make_float2(0.0f, -INFINITY);
-              M.pscale[s][meta_slot(j)] = ks[h2];
-            }
-            if (!p.fp8) {
+        for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
+        const uint32_t ph_e = (g & 1) ^ 1;  // slot of block g free: PV of block g-1 done
+        auto meta = [&]() {
+          M.row[g & 1][32 * pw + lane] =
+              loc >= 0 ? make_float4(ks * p.scale_log2, ks, 1.0f, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        if (p.shadow) {
 #pragma unroll
-              for (int u = 0; u < kPB; ++u) {
-                // piece part + 8u: chunk u, 16-byte slot `part`
-                *reinterpret_cast<uint4*>(rowp + u * kChunkBytes + ((part ^ (j & 7)) << 4)) =
-                    make_uint4(bf16x2_to_f16x2(v[h2][u].x), bf16x2_to_f16x2(v[h2][u].y),
-                               bf16x2_to_f16x2(v[h2][u].z), bf16x2_to_f16x2(v[h2][u].w));
+          for (int grp = 0; grp < kGroups; ++grp) {
+            if (!mbar_wait(&M.empty[grp < 4 ? grp : 3], ph_e, abort_v, p.status)) { ok = false; break; }
+#pragma unroll
+            for (int c = 2 * grp; c < (grp < 4 ? 2 * grp + 2 : kChunks); ++c)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int rw = 32 * pw + psub + 4 * i;
+                cp_async_16(st0 + c * kChunkBytes + sw_off(rw, pj),
+                            p.shadow + static_cast<int64_t>(rl[i] >= 0 ? rl[i] : 0) * kDqk + c * 64 + pj * 8,
+                            rl[i] >= 0 ? 16u : 0u);
               }
-            } else {
-#pragma unroll
-              for (int u = 0; u < kP8; ++u) {
-                const int p8 = part + 8 * u;  // 16 e4m3 values = 32 bytes of f16
-                if (p8 >= 36) break;
-                const int c = p8 >> 2, qq = (p8 & 3) * 2;
-                const uint32_t w[4] = {v[h2][u].x, v[h2][u].y, v[h2][u].z, v[h2][u].w};
-                uint32_t o[8];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  o[2 * t] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] & 0xFFFFu));
-                  o[2 * t + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[t] >> 16));
-                }
-                uint8_t* cp = rowp + c * kChunkBytes;
-                *reinterpret_cast<uint4*>(cp + ((qq ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(cp + (((qq + 1) ^ (j & 7)) << 4)) =
-                    make_uint4(o[4], o[5], o[6], o[7]);
-              }
-            }
-          }
-          if (p.shadow) {
-            // f16 rows already widened: 9 x 16-byte async copies per row and thread
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int j = rr + 32 * h2;
-              const uint32_t rowp = smem_u32(stage + s * kTileBytes + j * 128);
-              if (part == 0) {
-                M.col[s][meta_slot(j)] = prow[h2] >= 0 ? make_float2(p.scale_log2, 0.0f) : make_float2(0.0f, -INFINITY);
-                M.pscale[s][meta_slot(j)] = 1.0f;
-              }
-              const uint16_t* src = p.shadow + (prow[h2] >= 0 ? prow[h2] : 0) * kDqk;
-              const uint32_t nb = prow[h2] >= 0 ? 16u : 0u;
-#pragma unroll
-              for (int u = 0; u < kPB; ++u)
-                cp_async_16(rowp + u * kChunkBytes + ((part ^ (j & 7)) << 4), src + (part + 8 * u) * 8, nb);
-            }
             cp_async_commit();
-            cp_async_wait<0>();
+            if (grp > 0) {
+              cp_async_wait<1>();
+              fence_proxy_async_smem();
+              mbar_arrive(&M.full[grp - 1]);
+            }
           }
+          if (!ok) break;
+          cp_async_wait<0>();
+          meta();
           fence_proxy_async_smem();
-          mbar_arrive(&M.kv_full[s]);
-          if (b + 1 < ri.nb) load_block(prow_next);
-          prow[0] = prow_next[0];
-          prow[1] = prow_next[1];
+          mbar_arrive(&M.full[kGroups - 1]);
+        } else {
+          // load + widen in units of half a chunk (4 of the 8 passes); unit
+          // u+1 is loaded before unit u is stored
+          constexpr int kUnits = 2 * kChunks;
+          uint4 st[2][4];
+          auto load = [&](int u, uint4* dst) {
+            const int c = u >> 1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rw = rl[4 * (u & 1) + i];
+              if (rw < 0) {
+                dst[i] = make_uint4(0, 0, 0, 0);
+              } else if (!p.fp8) {
+                dst[i] = ldg_stream(reinterpret_cast<const uint16_t*>(p.kv) + static_cast<int64_t>(rw) * kDqk +
+                                    c * 64 + pj * 8);
+              } else {
+                const uint2 w =
+                    *reinterpret_cast<const uint2*>(p.kv + static_cast<int64_t>(rw) * kDqk + c * 64 + pj * 8);
+                dst[i] = make_uint4(w.x, w.y, 0, 0);
+              }
+            }
+          };
+          load(0, st[0]);
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            const int c = u >> 1;
+            const int grp = c < 8 ? c >> 1 : 4;
+            if (u + 1 < kUnits) load(u + 1, st[(u + 1) & 1]);
+            if ((u & 3) == 0 && !mbar_wait(&M.empty[grp < 4 ? grp : 3], ph_e, abort_v, p.status)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 w = st[u & 1][i];
+              uint4 o;
+              if (!p.fp8) {
+                over |= bf16x2_over_f16(w.x) | bf16x2_over_f16(w.y) | bf16x2_over_f16(w.z) | bf16x2_over_f16(w.w);
+                o = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                               bf16x2_to_f16x2(w.w));
+              } else {
+                o = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xFFFFu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+              }
+              *reinterpret_cast<uint4*>(stage + c * kChunkBytes + sw_off(32 * pw + psub + 4 * (4 * (u & 1) + i), pj)) = o;
+            }
+            if ((u & 3) == 3 || u == kUnits - 1) {
+              if (u == kUnits - 1) meta();
+              fence_proxy_async_smem();
+              mbar_arrive(&M.full[grp]);
+            }
+          }
         }
+        key0 = key1;
+        key1 = key2;
+        pg0 = pg1;
       }
       ++tok;
     }
+    cp_async_wait<0>();
+    if (over) set_status(p.status, kStatusOverflow);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
+    // Warps 4-7 take heads [0, H/2) and warps 8-11 heads [H/2, H) of the rows
+    // on their TMEM lane quadrant.
+    constexpr int HW = H / 2;
     const int qd = warp & 3;
-    const int half = lane >> 4;
-    const int h = 16 * qd + (lane & 15);
-    const bool real = h < H;
+    const int hq = (warp - 4) >> 2;
+    const int h0 = hq * HW;
+    const int tid = threadIdx.x - 128;  // 0..255
+    const int rrow = qd * 32 + lane;     // selected row of the block = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-    uint32_t g = 0, tok = 0;
+    const uint32_t p_row = smem_u32(stage + kPChunk * kChunkBytes);
+    uint32_t g = 0;
     for (int k = 0;; ++k) {
       int row;
       const int r = next_row(p.n_rows, k, row);
       if (r < 0) break;
       if (r == 0) continue;
       const RowInfo ri = row_info(p, row);
-      float m_used = -INFINITY, l = 0.0f;
+      uint16_t* orow = p.out + static_cast<size_t>(row) * H * kDv;
+      if (ri.nb == 0) {
+        for (int i = tid; i < H * kDv / 8; i += 256) reinterpret_cast<uint4*>(orow)[i] = make_uint4(0, 0, 0, 0);
+        if (p.lse && tid < H) p.lse[static_cast<size_t>(row) * H + tid] = -INFINITY;
+        continue;
+      }
       bool ok = true;
       for (int b = 0; b < ri.nb; ++b) {
-        const uint32_t gb = g + b;
-        const int s = gb & 1;
-        if (!mbar_wait(&M.s_full[s], (gb >> 1) & 1, abort_v, p.status)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t raw[32];
-        tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + s * 64, raw);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&M.s_empty[s]);
-        if (!mbar_wait(&M.kv_full[s], (gb >> 1) & 1, abort_v, p.status)) { ok = false; break; }
-        float x[32];
-        float mx = -INFINITY;
-        const float2* meta = &M.col[s][meta_slot(half * 32)];
-        const float* pmeta = &M.pscale[s][meta_slot(half * 32)];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 m2 = meta[i];  // same address across the half: broadcast
-          x[i] = fmaf(__uint_as_float(raw[i]), m2.x, m2.y);
-          mx = fmaxf(mx, x[i]);
+        const uint32_t gb = g + b, ph = gb & 1;
+        if (!mbar_wait(&M.s_full, ph, abort_v, p.status) || !mbar_wait(&M.full[kGroups - 1], ph, abort_v, p.status)) {
+          ok = false;
+          break;
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-        const float m_new = fmaxf(m_used, mx);
-        const bool resc = real && b > 0 && m_new > m_used + kRescaleLog2;
-        if (b == 0) m_used = m_new;
-        // probabilities against the running max (unchanged unless this head rescales),
-        // computed before waiting for the previous PV so they overlap it
-        float sum = 0.0f;
-        uint32_t pk[16];
-        auto make_p = [&]() {
-          const float mref = m_used == -INFINITY ? 0.0f : m_used;
-          sum = 0.0f;
+        tc_fence_after();
+        const float4 mt = M.row[ph][rrow];
+        const bool valid = mt.z != 0.0f;
+        // (tcgen05.ld and its wait are warp-collective: every lane executes them,
+        // `valid` only gates the arithmetic)
+        uint32_t raw[HW];
+        tmem_ld_cols<HW>(tmem + lane_base + kColS + h0, raw);
+        tmem_wait_ld();
+        // does any logit exceed its head's reference max by more than 2^8?
+        bool flag = b == 0;
+        if (!flag && valid) {
+          float tmax = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float p0 = fast_exp2(x[i] - mref), p1 = fast_exp2(x[i + 1] - mref);
-            sum += p0 + p1;
-            pk[i >> 1] = p.fp8 ? pack_f16(p0 * pmeta[i], p1 * pmeta[i + 1]) : pack_f16(p0, p1);
+          for (int i = 0; i < HW; ++i) tmax = fmaxf(tmax, fmaf(__uint_as_float(raw[i]), mt.x, -M.m[h0 + i]));
+          flag = tmax > kRescaleLog2;
+        }
+        if (named_bar_or(1, 256, flag)) {
+          // exact per-head maximum of this block's logits
+          {
+            float x[HW];
+#pragma unroll
+            for (int i = 0; i < HW; ++i) x[i] = valid ? __uint_as_float(raw[i]) * mt.x : -INFINITY;
+            const float mx = warp_reduce_scatter<HW>(x, lane, MaxOp());
+            if ((lane & (32 / HW - 1)) == 0) M.red[qd][h0 + lane / (32 / HW)] = mx;
           }
-        };
-        if (!resc) make_p();
-        const bool any = named_bar_or(1, 128, resc);
-        if (any) {
-          // O must hold exactly PV(0..b-1) while it is rescaled. kv_empty[stage]
-          // completes when the PV of that stage's block finishes; for block b-1
-          // it is at most one phase away from this wait (its stage was refilled
-          // for b-1 only after PV(b-3) completed), so the parity is unambiguous.
-          const uint32_t gp = gb - 1;
-          if (!mbar_wait(&M.kv_empty[gp & 1], (gp >> 1) & 1, abort_v, p.status)) { ok = false; break; }
-          const float a = resc ? fast_exp2(m_used - m_new) : 1.0f;
-          if (resc) {
-            m_used = m_new;
-            l *= a;
-            make_p();
+          named_bar_sync(1, 256);
+          bool resc = false;
+          if (tid < H) {
+            const float bm = fmaxf(fmaxf(M.red[0][tid], M.red[1][tid]), fmaxf(M.red[2][tid], M.red[3][tid]));
+            const float mu = b == 0 ? -INFINITY : M.m[tid];
+            float a = 1.0f;
+            if (bm > mu + kRescaleLog2 || (mu == -INFINITY && bm > -INFINITY)) {
+              a = mu == -INFINITY ? 0.0f : fast_exp2(mu - bm);
+              M.m[tid] = bm;
+              resc = b > 0;
+            } else if (b == 0) {
+              M.m[tid] = -INFINITY;
+            }
+            M.alpha[tid] = a;
           }
-          if (half == 0) M.alpha[h] = a;
-          named_bar_sync(1, 128);
-          tc_fence_after();
+          if (named_bar_or(1, 256, resc)) {
+            // this thread's heads of O^T (its lane of every slice) and of its
+            // row's partial sums; slot 4 is the partial sums
 #pragma unroll 1
-          for (int dt = 0; dt < 4; ++dt) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < H; c0 += kColChunk) {
-              uint32_t o[kColChunk];
-              const uint32_t ta = tmem + lane_base + kColO + dt * 64 + c0;
-              tmem_ld_cols<kColChunk>(ta, o);
+            for (int dt = 0; dt < 5; ++dt) {
+              uint32_t o[HW];
+              const uint32_t ta = tmem + lane_base + (dt < 4 ? kColO + dt * 64 : kColL) + h0;
+              tmem_ld_cols<HW>(ta, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < kColChunk; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * M.alpha[c0 + c]);
-              tmem_st_cols<kColChunk>(ta, o);
+              for (int i = 0; i < HW; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * M.alpha[h0 + i]);
+              tmem_st_cols<HW>(ta, o);
             }
+            tmem_wait_st();
           }
-          tmem_wait_st();
-          tc_fence_before();
         }
-        l += sum;
-        uint8_t* prow = stage + s * kTileBytes + kPChunk * kChunkBytes + h * 128;
+        // probabilities, partial sums, P^T row
+        {
+          uint32_t lp[HW];
+          if (b > 0) {
+            tmem_ld_cols<HW>(tmem + lane_base + kColL + h0, lp);
+            tmem_wait_ld();
+          }
+          uint32_t pk[HW / 2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int qq = half * 4 + u;
-          *reinterpret_cast<uint4*>(prow + ((qq ^ (h & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int i = 0; i < HW; i += 2) {
+            float p0 = 0.0f, p1 = 0.0f;
+            if (valid) {
+              p0 = fast_exp2(fmaf(__uint_as_float(raw[i]), mt.x, -M.m[h0 + i]));
+              p1 = fast_exp2(fmaf(__uint_as_float(raw[i + 1]), mt.x, -M.m[h0 + i + 1]));
+            }
+            lp[i] = __float_as_uint(b > 0 ? __uint_as_float(lp[i]) + p0 : p0);
+            lp[i + 1] = __float_as_uint(b > 0 ? __uint_as_float(lp[i + 1]) + p1 : p1);
+            pk[i >> 1] = pack_f16(p0 * mt.y, p1 * mt.y);
+          }
+          tmem_st_cols<HW>(tmem + lane_base + kColL + h0, lp);
+#pragma unroll
+          for (int u = 0; u < HW / 8; ++u)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(p_row + sw_off(rrow, h0 / 8 + u)),
+                         "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                         : "memory");
         }
+        tmem_wait_st();
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&M.p_full[s]);
+        if (lane == 0) mbar_arrive(&M.p_full);
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
       {
-        // last PV of this row done (same reasoning as for the rescale wait)
+        // the last PV of this query row has finished
         const uint32_t gl = g + ri.nb - 1;
-        if (!mbar_wait(&M.kv_empty[gl & 1], (gl >> 1) & 1, abort_v, p.status)) break;
+        if (!mbar_wait(&M.empty[3], gl & 1, abort_v, p.status)) break;
       }
       tc_fence_after();
-      const float lt = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-      if (half == 0 && real) {
-        M.linv[h] = lt > 0.0f ? 1.0f / lt : 0.0f;
-        if (p.lse)
-          p.lse[static_cast<size_t>(row) * H + h] =
-              lt > 0.0f ? (m_used + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      {
+        uint32_t raw[HW];
+        tmem_ld_cols<HW>(tmem + lane_base + kColL + h0, raw);
+        tmem_wait_ld();
+        float x[HW];
+#pragma unroll
+        for (int i = 0; i < HW; ++i) x[i] = __uint_as_float(raw[i]);
+        const float sm = warp_reduce_scatter<HW>(x, lane, AddOp());
+        if ((lane & (32 / HW - 1)) == 0) M.red[qd][h0 + lane / (32 / HW)] = sm;
       }
-      named_bar_sync(1, 128);
-      uint16_t* orow = p.out + static_cast<size_t>(row) * H * kDv;
+      named_bar_sync(1, 256);
+      if (tid < H) {
+        const float lt = (M.red[0][tid] + M.red[1][tid]) + (M.red[2][tid] + M.red[3][tid]);
+        M.linv[tid] = lt > 0.0f ? 1.0f / lt : 0.0f;
+        if (p.lse)
+          p.lse[static_cast<size_t>(row) * H + tid] =
+              lt > 0.0f ? (M.m[tid] + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      }
+      named_bar_sync(1, 256);
       const bool odd = lane & 1;
 #pragma unroll 1
       for (int dt = 0; dt < 4; ++dt) {
         const int d = dt * 128 + qd * 32 + lane;
         const int d_even = d & ~1;
-#pragma unroll 1
-        for (int c0 = 0; c0 < H; c0 += kColChunk) {
-          uint32_t o[kColChunk];
-          tmem_ld_cols<kColChunk>(tmem + lane_base + kColO + dt * 64 + c0, o);
-          tmem_wait_ld();
+        uint32_t o[HW];
+        tmem_ld_cols<HW>(tmem + lane_base + kColO + dt * 64 + h0, o);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kColChunk; c += 2) {
-            const float v0 = __uint_as_float(o[c]) * M.linv[c0 + c];
-            const float v1 = __uint_as_float(o[c + 1]) * M.linv[c0 + c + 1];
-            const float x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? v0 : v1, 1);
-            const uint32_t word = odd ? pack_bf16(x2, v1) : pack_bf16(v0, x2);
-            const int hh = c0 + (odd ? c + 1 : c);
-            *reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(hh) * kDv + d_even) = word;
-          }
+        for (int c = 0; c < HW; c += 2) {
+          const float v0 = __uint_as_float(o[c]) * M.linv[h0 + c];
+          const float v1 = __uint_as_float(o[c + 1]) * M.linv[h0 + c + 1];
+          const float x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? v0 : v1, 1);
+          const uint32_t word = odd ? pack_bf16(x2, v1) : pack_bf16(v0, x2);
+          const int hh = h0 + (odd ? c + 1 : c);
+          *reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(hh) * kDv + d_even) = word;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.o_empty);
       g += ri.nb;
-      ++tok;
     }
   }
 

@@ -59,8 +59,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but the thread may be suspended for up to `ns` nanoseconds while the
+// phase is incomplete (it resumes when the phase completes), so waiting
+// threads do not keep polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // About four seconds of SM clock at GB300 clocks: the limit of every bounded wait.
 constexpr long long kWaitLimitCycles = 8000000000ll;
+// Suspend-time hint of one polling round of a bounded wait.
+constexpr uint32_t kWaitSleepNs = 20000;
 
 // Bounded wait on phase `parity`. Gives up after kWaitLimitCycles SM cycles or
 // when another thread has raised `*abort`; on giving up it records a timeout
@@ -71,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (abort && *abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       if (status) atomicOr(status, kStatusTimeout);

@@ -61,6 +61,7 @@ def test_prefill_argument_checks(L):
     assert _prefill(L, _cache(), T=0) == INVALID
     assert _prefill(L, _cache(), prefix=-1) == INVALID
     assert _prefill(L, _cache(page_size=32)) == UNSUPPORTED
+    assert _prefill(L, _cache(num_pages=(1 << 25) + 1)) == UNSUPPORTED   # pool rows are int32
     assert _prefill(L, _cache(d_idx=64)) == UNSUPPORTED             # e4m3 x 64 = 64-byte rows
     assert _prefill(L, _cache(kv_scale=None)) == INVALID            # FP8 needs scales
     assert _prefill(L, _cache(kv_dtype=7)) == INVALID
