@@ -250,6 +250,54 @@ def run_e2e(args, spec, dev, out, lse, stream, world):
     return ms_e2e, h2d, d2h
 
 
+def measure_decode(args, stream, flush):
+    """The decode workload (64 requests x 2 MTP tokens, 8K-128K keys each, FP8
+    cache in a shuffled pool): one step = smla_sparse_mla_decode (split-key
+    indexer, candidate merge, sparse MLA). Reported next to the headline; its
+    roofline is HBM bandwidth over the algorithmic bytes of the step."""
+    spec = wl.SPECS["decode"]
+    dev = wl.make(spec, "cuda")
+    lens = dev.seq_lens
+    max_len = int(lens.max().item())
+    H, k = spec.n_heads, spec.topk
+    rows = spec.n_seqs * spec.q_per_seq
+    out = torch.empty((rows, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, H), dtype=torch.float32, device="cuda")
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    ws = smla.workspace(smla.decode_workspace_bytes(spec.n_seqs, max_len, spec.q_per_seq, H, spec.h_idx, k))
+
+    def step():
+        smla.sparse_mla_decode(dev.cache, dev.page_table, lens, max_len, spec.q_per_seq, dev.q, dev.q_idx, dev.w,
+                               k, spec.sm_scale, out=out, lse=lse, out_idx=idx, ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert smla.read_status(ws)[0] == 0
+    n = max(5, min(args.steps, 20))
+    ev = []
+    for _ in range(n):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    cnt = counting.decode_counts([int(x) for x in lens.tolist()], spec.q_per_seq, H, spec.h_idx, spec.d_idx, k,
+                                 spec.kv_dtype, 1)
+    alg = cnt["idx_bytes"] + cnt["mla_bytes"]
+    pk = peaks()
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": f"decode: {spec.n_seqs} requests x {spec.q_per_seq} tokens, keys U[{spec.len_min}, "
+                        f"{spec.len_max}], FP8 KV + FP8 indexer, top-{k}, shuffled pages",
+            "ms_per_step": ms, "tokens_per_s": rows / (ms / 1e3), "algorithmic_bytes": alg,
+            "gbs_algorithmic": gbs, "hbm_peak_gbs": pk["hbm"], "frac_of_hbm": gbs / pk["hbm"],
+            "gpu_launches_per_step": 3, "l2": "256 MB buffer written between timed steps"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -263,6 +311,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: use this many query tokens instead of the workload's")
     ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the host-buffer pass")
+    ap.add_argument("--no-decode", action="store_true", help="profiling only: skip the decode measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_setup(args.gpus)
@@ -333,6 +382,8 @@ def main():
     else:
         ms_e2e, h2d, d2h = run_e2e(args, spec, dev, out, lse, stream, world)
 
+    decode = None if args.no_decode else measure_decode(args, stream, flush)
+
     # ------------------------------------------------------------------ roofline
     pk = peaks()
     cnt = counting.prefill_counts(P, T, H, spec.h_idx, spec.d_idx, k, spec.kv_dtype,
@@ -373,6 +424,7 @@ def main():
                 "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse"},
         # per step: indexer_kernel, shadow_convert_kernel (BF16 cache only), mla_kernel
         "gpu_launches": (3 if spec.kv_dtype == "bf16" else 2) * args.steps,
+        "decode": decode,
         "clocks": clk.summary(),
     }
     if rank == 0:

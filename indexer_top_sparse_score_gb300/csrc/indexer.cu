@@ -464,7 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = t * kTileKeys + q * 32 + lane;
         float ks = 1.0f;
         if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
-        uint32_t key[TPW_MAX];
+        // ReLU + head-weighted sum with four independent partial sums per token
+        // (weights read as float4 broadcasts), then the admission test
+        uint32_t key[TPW_MAX], m[TPW_MAX];
         bool adm[TPW_MAX];
 #pragma unroll
         for (int jj = 0; jj < TPW_MAX; ++jj) {
@@ -472,34 +474,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           adm[jj] = false;
           key[jj] = 0;
           if (j < j1) {
-            const float* wr = wbuf + j * HI;
-            float sc = 0.0f;
+            const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-            for (int h = 0; h < HI; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(raw[jj * HI + h]), 0.0f), sc);
-            sc *= ks;
-            key[jj] = score_key(sc);
+            for (int h = 0; h < HI; h += 4) {
+              const float4 wv = w4[h >> 2];
+              a0 = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a0);
+              a1 = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a1);
+              a2 = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a2);
+              a3 = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a3);
+            }
+            key[jj] = score_key(((a0 + a1) + (a2 + a3)) * ks);
             const bool valid = j < it.nrows && s >= it.key_lo && s < it.key_hi && s <= it.pos0 + j;
             adm[jj] = valid && key[jj] > theta[j];
           }
+          m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
         }
         wg_sync();
         for (int j = j0; j < j1; ++j)
           if (cnt[j] > cap - kTileKeys) select_token(j, topk, false, it);
+        // one reservation per warp and token; both issued before either is used
+        int base[TPW_MAX];
+        if (lane == 0) {
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj) base[jj] = m[jj] ? atomicAdd(&cnt[j0 + jj], __popc(m[jj])) : 0;
+        }
 #pragma unroll
         for (int jj = 0; jj < TPW_MAX; ++jj) {
-          const int j = j0 + jj;
-          if (j < j1) {
-            const uint32_t m = __ballot_sync(0xFFFFFFFFu, adm[jj]);
-            if (m) {
-              int base = 0;
-              if (lane == 0) base = atomicAdd(&cnt[j], __popc(m));
-              base = __shfl_sync(0xFFFFFFFFu, base, 0);
-              if (adm[jj]) {
-                const int pos = base + __popc(m & lanemask_lt);
-                ckey[j * cap + pos] = key[jj];
-                cidx[j * cap + pos] = static_cast<uint32_t>(s);
-              }
-            }
+          base[jj] = __shfl_sync(0xFFFFFFFFu, base[jj], 0);
+          if (adm[jj]) {
+            const int j = j0 + jj;
+            const int pos = base[jj] + __popc(m[jj] & lanemask_lt);
+            ckey[j * cap + pos] = key[jj];
+            cidx[j * cap + pos] = static_cast<uint32_t>(s);
           }
         }
       }
