@@ -106,6 +106,13 @@ int smla_version(void);
  *   out_scores  [n_seqs*q_per_seq][topk] fp32 scores of out_idx, or NULL.
  * Supported: h_idx in {4, 8, 16, 32, 64}; 1 <= topk <= 2048. Integer-valued
  * inputs make the selection bit-identical to the exact fp32 definition.
+ * Workspace: the returned size. When several query rows share the key stream
+ * (long per-sequence batches), 256 bytes already suffice and the rest holds
+ * per-row candidate buffers (up to 16384 / rows-per-work-item (key, index)
+ * pairs of 8 bytes, plus a count per row) whose final exact selection then
+ * runs in a separate light kernel instead of stalling the scoring pipeline;
+ * with less room the selection stays in the scoring kernel. For decode-shaped
+ * calls (few rows per sequence) the per-key-block candidate lists are required.
  * ------------------------------------------------------------------------- */
 size_t smla_indexer_topk_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
                                         int32_t h_idx, int32_t topk);
@@ -154,10 +161,13 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
  *   q, q_idx, w, out, lse as above with rows = n_tokens.
  *   out_idx    [n_tokens][topk] int32 selected indices, or NULL to keep them
  *              in the workspace only.
- * Workspace: at least 256 + n_tokens * topk * 4 bytes (rounded to 256); the
- * size returned for kv_dtype = SMLA_BF16 adds an f16 copy of the sequence's
- * prefix_len + n_tokens cache rows, written once per call, which the attention
- * then gathers without per-row conversion (used only when it fits).
+ * Workspace: at least 256 + n_tokens * topk * 4 bytes (rounded to 256). The
+ * returned size lays out, in order: the status word, the index list, for
+ * kv_dtype = SMLA_BF16 an f16 copy of the sequence's prefix_len + n_tokens
+ * cache rows (written once per call and gathered by the attention without
+ * per-row conversion), and the indexer's deferred candidate buffers (see
+ * smla_indexer_topk). Each optional part is used only when the workspace
+ * reaches its end.
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t n_heads,
                                               int32_t h_idx, int32_t topk, int32_t kv_dtype);

@@ -113,7 +113,8 @@ int smla_version(void) { return 100; }
 size_t smla_indexer_topk_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
                                         int32_t h_idx, int32_t topk) {
   if (n_seqs <= 0 || max_seq_len <= 0 || q_per_seq <= 0 || topk <= 0) return kStatusBytes;
-  return round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk));
+  return round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk)) +
+         indexer_group_cand_bytes(n_seqs * q_per_seq, q_per_seq, h_idx, topk);
 }
 
 static int indexer_checks(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
@@ -141,12 +142,16 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
   const bool split = indexer_split_mode(q_per_seq, h_idx);
   if (indexer_tokens_per_cta(h_idx, topk, split, q_per_seq) <= 0) return SMLA_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return SMLA_ERR_WORKSPACE;
-  if (workspace_bytes < smla_indexer_topk_workspace_size(n_seqs, max_seq_len, q_per_seq, h_idx, topk))
-    return SMLA_ERR_WORKSPACE;
+  // required: status word (+ split-mode lists); the group-mode candidate
+  // buffers behind it are used when they fit
+  const size_t ws_min = round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk));
+  if (workspace_bytes < ws_min) return SMLA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((rc = reset_status(workspace, st))) return rc;
   IndexerLaunch L{cache, page_tables, max_pages, n_seqs, q_per_seq, seq_lens, 0, max_seq_len, q_idx, w,
-                  h_idx, topk, out_idx, out_scores, workspace, workspace_bytes, st};
+                  h_idx, topk, out_idx, out_scores, workspace, ws_min, st};
+  L.cand = static_cast<uint8_t*>(workspace) + ws_min;
+  L.cand_bytes = workspace_bytes - ws_min;
   return launch_indexer(L);
 }
 
@@ -199,11 +204,12 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
 }
 
 // ----------------------------------------------------------------- prefill
-size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t, int32_t,
+size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t, int32_t h_idx,
                                               int32_t topk, int32_t kv_dtype) {
   if (prefix_len < 0 || n_tokens <= 0 || topk <= 0) return kStatusBytes;
   return prefill_min_workspace(n_tokens, topk) +
-         (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(prefix_len + n_tokens) : 0);
+         (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(prefix_len + n_tokens) : 0) +
+         indexer_group_cand_bytes(n_tokens, n_tokens, h_idx, topk);
 }
 
 int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_table, int32_t prefix_len,
@@ -231,6 +237,13 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   int32_t* idx = out_idx ? out_idx : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   IndexerLaunch IL{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, static_cast<int32_t>(total), q_idx,
                    w, h_idx, topk, idx, nullptr, workspace, workspace_bytes, st};
+  // layout: status | index list | f16 shadow (BF16 caches) | deferred candidate buffers
+  const size_t cand_off =
+      ws_min + (cache->kv_dtype == SMLA_BF16 ? mla_shadow_bytes(static_cast<int32_t>(total)) : 0);
+  if (workspace_bytes > cand_off) {
+    IL.cand = static_cast<uint8_t*>(workspace) + cand_off;
+    IL.cand_bytes = workspace_bytes - cand_off;
+  }
   if ((rc = launch_indexer(IL))) return rc;
   MlaLaunch ML{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, q, n_heads, idx, topk, sm_scale, out,
                lse, static_cast<uint32_t*>(workspace), st};

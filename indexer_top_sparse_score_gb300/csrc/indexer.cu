@@ -44,6 +44,7 @@ constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
+constexpr int kMaxAcc = 4;                            // TMEM accumulator buffers at most
 
 struct IdxParams {
   const float* k_scale;  // [pool rows] or null
@@ -61,11 +62,13 @@ struct IdxParams {
   int32_t n_kblocks;  // split mode: key blocks per sequence
   int32_t n_items;    // group mode: n_seqs * n_groups; split: n_seqs * n_kblocks
   int32_t tmem_cols;
+  int32_t acc_shift;  // log2 of the TMEM accumulator buffers (1, 2 or 4 buffers)
   int32_t* out_idx;
   float* out_scores;
-  uint32_t* cand_key;
+  uint32_t* cand_key;  // split mode: per (row, key block) lists; group mode: per-row deferred buffers
   uint32_t* cand_idx;
   int32_t* cand_cnt;
+  int32_t defer;       // group mode: hand rows with more than topk candidates to finish_kernel
   uint32_t* status;
 };
 
@@ -73,9 +76,20 @@ struct Item {
   int seq, row0, nrows, pos0;
   int key_lo, key_hi;
   int t0, t1;
+  int rot;  // tiles are streamed from t0 + rot, wrapping: CTAs start at different tiles
   int kb;
   bool trivial;
 };
+
+// Tile streamed at step tt (0 <= tt < t1 - t0) of an item. The top-k does not
+// depend on the key order; rotating it per CTA keeps the CTAs from all reading
+// the same key tile (and the same L2 slices) at the same time.
+__device__ __forceinline__ int tile_at(const Item& it, int tt) {
+  const int nt = it.t1 - it.t0;
+  int u = tt + it.rot;
+  if (u >= nt) u -= nt;
+  return it.t0 + u;
+}
 
 // The k-th item of this CTA. Returns -1 when the CTA has no more items, 0 for
 // an empty slot (skip), 1 for a real item. Every role calls this with the
@@ -119,6 +133,7 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it) {
   if (it.key_hi <= it.key_lo) return 0;
   it.t0 = it.key_lo / kTileKeys;
   it.t1 = (it.key_hi + kTileKeys - 1) / kTileKeys;
+  it.rot = static_cast<int>((blockIdx.x * 97u + static_cast<unsigned>(k) * 31u) % static_cast<unsigned>(it.t1 - it.t0));
   return 1;
 }
 
@@ -167,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = bars;
   uint64_t* a_empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* b_full = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kMaxAcc;
+  uint64_t* b_full = acc_empty + kMaxAcc;
   uint64_t* b_empty = b_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&a_full[i], 1);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiThreads / 32);
     }
@@ -229,13 +244,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       ++bi;
       const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
-      for (int tw = it.t0; tw < it.t1 && ok; tw += 16) {
-        const int lp = 2 * tw + lane;
-        const int pg = lp * kPage < it.key_hi ? page_of(p, pt, lp) : 0;
-        const int tend = min(tw + 16, it.t1);
-        for (int t = tw; t < tend; ++t, ++sc) {
-          const int pg0 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (t - tw));
-          const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (t - tw) + 1);
+      const int nt = it.t1 - it.t0;
+      for (int tw = 0; tw < nt && ok; tw += 16) {
+        // lane l resolves page l & 1 of the tile streamed at step tw + l / 2
+        int pg = 0;
+        if (tw + (lane >> 1) < nt) {
+          const int lp = 2 * tile_at(it, tw + (lane >> 1)) + (lane & 1);
+          pg = lp * kPage < it.key_hi ? page_of(p, pt, lp) : 0;
+        }
+        const int tend = min(tw + 16, nt);
+        for (int tt = tw; tt < tend; ++tt, ++sc) {
+          const int pg0 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (tt - tw));
+          const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (tt - tw) + 1);
+          const int t = tile_at(it, tt);
           if (lane == 0) {
             const int s = sc % kStages;
             ok = mbar_wait(&a_empty[s], ((sc / kStages) & 1) ^ 1, abort_v, p.status);
@@ -271,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = it.t0; t < it.t1; ++t, ++sc, ++ac) {
           const int s = sc % kStages;
-          const int buf = ac & 1;
-          if (!mbar_wait(&a_full[s], (sc / kStages) & 1, abort_v, p.status) ||
-              !mbar_wait(&acc_empty[buf], ((ac >> 1) & 1) ^ 1, abort_v, p.status)) {
+          const int buf = ac & ((1 << p.acc_shift) - 1);
+          if (!mbar_wait_spin(&a_full[s], (sc / kStages) & 1, abort_v, p.status) ||
+              !mbar_wait_spin(&acc_empty[buf], ((ac >> p.acc_shift) & 1) ^ 1, abort_v, p.status)) {
             ok = false;
             break;
           }
@@ -318,6 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = cnt[j];
       uint32_t* kb = ckey + j * cap;
       uint32_t* ib = cidx + j * cap;
+      if (to_output && p.defer && n > keep) {
+        // hand the buffer to finish_kernel: copy it to the row's slot
+        const int row = it.row0 + j;
+        uint4* dk = reinterpret_cast<uint4*>(p.cand_key + static_cast<size_t>(row) * cap);
+        uint4* di = reinterpret_cast<uint4*>(p.cand_idx + static_cast<size_t>(row) * cap);
+        for (int e = 4 * tid_wg; e < n; e += 512) {
+          dk[e >> 2] = *reinterpret_cast<const uint4*>(kb + e);
+          di[e >> 2] = *reinterpret_cast<const uint4*>(ib + e);
+        }
+        if (tid_wg == 0) p.cand_cnt[row] = n;
+        wg_sync();
+        return;
+      }
       uint32_t tk = 0, ti = 0xFFFFFFFFu;
       const bool all = n <= keep;
       bool cut = false;  // mid-stream: keep key >= tk (a superset of the top-k)
@@ -403,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.out_idx[static_cast<size_t>(row) * topk + e] = -1;
             if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + e] = 0.0f;
           }
+          if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;  // row complete
         } else if (tid_wg == 0) {
           p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + it.kb] = base;
         }
@@ -410,9 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       wg_sync();
       if (!to_output && tid_wg == 0) {
         cnt[j] = base;
-        // admit later keys only above the cut (exact: above the k-th key; a
-        // later key equal to it loses the tie to every kept entry)
-        theta[j] = cut ? (tk > 0 ? tk - 1 : 0) : tk;
+        // admit later keys from the cut (or the k-th key) up: keys stream in
+        // a rotated order, so a later key equal to it may have a smaller
+        // index and win the tie
+        theta[j] = tk > 0 ? tk - 1 : 0;
       }
       wg_sync();
     };
@@ -438,14 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int n = it.pos0 + j + 1;
           int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + j) * topk;
           for (int e = tid_wg; e < topk; e += 128) o[e] = e < n ? e : -1;
+          if (p.defer && tid_wg == 0) p.cand_cnt[it.row0 + j] = -1;  // row complete
         }
         continue;
       }
       const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
       bool ok = true;
-      for (int t = it.t0; t < it.t1; ++t, ++ac) {
-        const int buf = ac & 1;
-        if (!mbar_wait(&acc_full[buf], (ac >> 1) & 1, abort_v, p.status)) {
+      for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
+        const int t = tile_at(it, tt);
+        const int buf = ac & ((1 << p.acc_shift) - 1);
+        if (!mbar_wait_spin(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
           ok = false;
           break;
         }
@@ -602,6 +640,82 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Group mode, deferred rows: the exact top-k of one row's candidate buffer
+// (copied out by the indexer when it held more than topk entries). One
+// 128-thread CTA per row; the buffer is staged in shared memory and selected
+// with the same exact radix selection the indexer uses in-kernel.
+struct FinishParams {
+  const uint32_t* cand_key;
+  const uint32_t* cand_idx;
+  const int32_t* cand_cnt;  // > 0: entries to select from; -1: row written by the indexer
+  int32_t cap, topk;
+  int32_t* out_idx;
+  float* out_scores;
+};
+
+constexpr int kFinishThreads = 128;
+
+size_t finish_smem_bytes(int cap) { return (2 * static_cast<size_t>(cap) + 768 + 16 + 4) * 4; }
+
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishParams p) {
+  extern __shared__ __align__(16) uint32_t fsm[];
+  uint32_t* keys = fsm;
+  uint32_t* idxs = fsm + p.cap;
+  uint32_t* hist = idxs + p.cap;  // 3 x 256
+  uint32_t* red = hist + 768;     // 16
+  uint32_t* wsum = red + 16;      // 4
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int n = p.cand_cnt[row];
+  if (n <= 0) return;
+  const uint4* sk = reinterpret_cast<const uint4*>(p.cand_key + static_cast<size_t>(row) * p.cap);
+  const uint4* si = reinterpret_cast<const uint4*>(p.cand_idx + static_cast<size_t>(row) * p.cap);
+  for (int e = 4 * tid; e < n; e += 4 * kFinishThreads) {
+    *reinterpret_cast<uint4*>(keys + e) = __ldg(sk + (e >> 2));
+    *reinterpret_cast<uint4*>(idxs + e) = __ldg(si + (e >> 2));
+  }
+  __syncthreads();
+  auto sync = []() { __syncthreads(); };
+  uint32_t tk = 0, ti = 0xFFFFFFFFu;
+  const bool all = n <= p.topk;
+  if (!all) wg_select(keys, idxs, n, p.topk, tid, hist, red, sync, tk, ti);
+  int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
+  float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
+  const uint32_t lanemask_lt = (1u << lane) - 1u;
+  int base = 0;
+  for (int e0 = 0; e0 < n; e0 += kFinishThreads) {
+    const int e = e0 + tid;
+    uint32_t kk = 0, ii = 0;
+    bool take = false;
+    if (e < n) {
+      kk = keys[e];
+      ii = idxs[e];
+      take = all || selected(kk, ii, tk, ti);
+    }
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+    if (lane == 0) wsum[w] = __popc(m);
+    __syncthreads();
+    int off = base, tot = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kFinishThreads / 32; ++w2) {
+      const int v = static_cast<int>(wsum[w2]);
+      if (w2 < w) off += v;
+      tot += v;
+    }
+    __syncthreads();
+    if (take) {
+      const int pos = off + __popc(m & lanemask_lt);
+      o[pos] = static_cast<int32_t>(ii);
+      if (os) os[pos] = key_score(kk);
+    }
+    base += tot;
+  }
+  for (int e = base + tid; e < p.topk; e += kFinishThreads) {
+    o[e] = -1;
+    if (os) os[e] = 0.0f;
+  }
+}
+
 template <int HI>
 int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
   CUtensorMap map_k, map_q;
@@ -616,7 +730,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + 16 * 8 + 16;
+                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kStages + 2 * kMaxAcc + 2) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -652,6 +766,14 @@ int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_pe
   return kBufEntries / tq - 2 * kTileKeys >= topk ? tq : 0;
 }
 
+size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk) {
+  if (indexer_split_mode(q_per_seq, h_idx) || n_rows <= 0) return 0;
+  const int tq = indexer_tokens_per_cta(h_idx, topk, false, q_per_seq);
+  if (tq <= 0) return 0;
+  const size_t cap = kBufEntries / tq;
+  return static_cast<size_t>(n_rows) * cap * 8 + (static_cast<size_t>(n_rows) * 4 + 255) / 256 * 256;
+}
+
 size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
                                int32_t topk) {
   size_t bytes = kStatusBytes;
@@ -684,8 +806,11 @@ int launch_indexer(const IndexerLaunch& L) {
   prm.is_bf16 = L.cache->idx_dtype == SMLA_BF16;
   prm.split = split;
   const int N = L.h_idx * tq;
+  // as many accumulator buffers as fit in TMEM's 512 columns (at most 4)
+  prm.acc_shift = 0;
+  while (prm.acc_shift < 2 && (N << (prm.acc_shift + 1)) <= 512) ++prm.acc_shift;
   int cols = 32;
-  while (cols < 2 * N) cols <<= 1;
+  while (cols < (N << prm.acc_shift)) cols <<= 1;
   prm.tmem_cols = cols;
   prm.out_idx = L.out_idx;
   prm.out_scores = L.out_scores;
@@ -702,6 +827,13 @@ int launch_indexer(const IndexerLaunch& L) {
   } else {
     prm.n_groups = (L.q_per_seq + tq - 1) / tq;
     prm.n_items = L.n_seqs * prm.n_groups;
+    const size_t cand = indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk);
+    if (L.cand && cand > 0 && L.cand_bytes >= cand && (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
+      prm.defer = 1;
+      prm.cand_key = static_cast<uint32_t*>(L.cand);
+      prm.cand_idx = prm.cand_key + rows * prm.cap;
+      prm.cand_cnt = reinterpret_cast<int32_t*>(prm.cand_idx + rows * prm.cap);
+    }
   }
   int rc;
   switch (L.h_idx) {
@@ -712,7 +844,21 @@ int launch_indexer(const IndexerLaunch& L) {
     case 64: rc = launch_indexer_t<64>(L, prm); break;
     default: return SMLA_ERR_UNSUPPORTED;
   }
-  if (rc != SMLA_OK || !split) return rc;
+  if (rc != SMLA_OK) return rc;
+  if (!split) {
+    if (!prm.defer) return SMLA_OK;
+    FinishParams fp{prm.cand_key, prm.cand_idx, prm.cand_cnt, prm.cap, L.topk, L.out_idx, L.out_scores};
+    const size_t fsmem = finish_smem_bytes(prm.cap);
+    static size_t attr_bytes = 0;
+    if (fsmem > attr_bytes) {
+      if (cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(fsmem)) != cudaSuccess)
+        return SMLA_ERR_CUDA;
+      attr_bytes = fsmem;
+    }
+    finish_kernel<<<prm.n_rows, kFinishThreads, fsmem, L.stream>>>(fp);
+    return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  }
   MergeParams mp{prm.cand_key, prm.cand_idx, prm.cand_cnt, L.seq_lens, L.q_per_seq, prm.n_kblocks, L.topk,
                  L.out_idx, L.out_scores};
   merge_kernel<<<prm.n_rows, kMergeThreads, 0, L.stream>>>(mp);

@@ -34,6 +34,10 @@ struct IndexerLaunch {
   void* workspace;          // status word + candidate lists (split mode)
   size_t workspace_bytes;
   cudaStream_t stream;
+  // group mode: room for the per-row candidate buffers of rows whose final
+  // selection is deferred to finish_kernel (null or too small: select in-kernel)
+  void* cand = nullptr;
+  size_t cand_bytes = 0;
 };
 
 struct MlaLaunch {
@@ -71,6 +75,8 @@ bool indexer_split_mode(int32_t q_per_seq, int32_t h_idx);
 int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_per_seq);
 size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
                                int32_t topk);
+// Group mode: bytes of the deferred per-row candidate buffers (0 if split mode).
+size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk);
 
 int launch_indexer(const IndexerLaunch& L);   // returns smla_status
 int launch_mla(const MlaLaunch& L);           // returns smla_status

@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // About four seconds of SM clock at GB300 clocks: the limit of every bounded wait.
 constexpr long long kWaitLimitCycles = 8000000000ll;
 // Suspend-time hint of one polling round of a bounded wait.
@@ -94,6 +107,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (status) atomicOr(status, kStatusTimeout);
       if (abort) *abort = 1;
       return false;
+    }
+  }
+}
+
+// Bounded wait that polls without suspending: the lowest wake-up latency, for
+// waits on a pipeline's critical path. Same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint32_t* status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        if (status) atomicOr(status, kStatusTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
     }
   }
 }

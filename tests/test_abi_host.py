@@ -90,11 +90,17 @@ def test_decode_and_indexer_argument_checks(L):
 
 
 def test_workspace_sizes(L):
-    # prefill keeps the index list: status word + T x topk int32
-    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4
+    # prefill keeps the index list (status word + T x topk int32) and room for the
+    # candidate buffers of rows whose final selection is deferred: 4 query rows per
+    # indexer work item at 32 heads share 16384 entries, so 4096 (key, index) pairs
+    # per row, plus one count per row
+    cand = 16384 * 4096 * 8 + 16384 * 4
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4 + cand
     # a BF16 cache adds an f16 copy of the sequence's rows (576 values x 2 bytes per key)
     assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 0) == \
-        256 + 16384 * 2048 * 4 + 16384 * 576 * 2
+        256 + 16384 * 2048 * 4 + 16384 * 576 * 2 + cand
+    # the indexer alone: status word + the same candidate buffers
+    assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256 + cand
     # decode: candidate lists of every (row, 8192-key block) + counts + index list
     rows, nkb, k = 128, 16, 2048
     dec = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
