@@ -111,8 +111,10 @@ int smla_version(void);
  * per-row candidate buffers (up to 16384 / rows-per-work-item (key, index)
  * pairs of 8 bytes, plus a count per row) whose final exact selection then
  * runs in a separate light kernel instead of stalling the scoring pipeline;
- * with less room the selection stays in the scoring kernel. For decode-shaped
- * calls (few rows per sequence) the per-key-block candidate lists are required.
+ * with less room the selection stays in the scoring kernel. Decode-shaped
+ * calls (few rows per sequence, whose keys are split across SMs) require a
+ * score array per query row (4 bytes per key up to max_seq_len): the scoring
+ * kernel writes every score and a per-row kernel then selects the exact top-k.
  * ------------------------------------------------------------------------- */
 size_t smla_indexer_topk_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
                                         int32_t h_idx, int32_t topk);

@@ -286,6 +286,136 @@ __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* 
 }
 
 // ---------------------------------------------------------------------------
+// Exact top-k threshold over a dense score array: entry e has key keys[e] and
+// index e, for e in [0, n) (n > k >= 1). NT cooperating threads (a multiple of
+// 128) synchronised by `sync()`; `hist` = 3 x 256 words and `red` =
+// 2 * NT / 32 words of shared scratch; keys must be 16-byte aligned. Returns
+// (thr_key, thr_idx) with the meaning of wg_select. Same method as wg_select
+// (range-adaptive radix passes over the keys, then over the tied indices),
+// reading the keys straight from (global) memory, four per 16-byte load.
+template <int NT, typename Sync>
+__device__ __forceinline__ void dense_select(const uint32_t* keys, int n, int k, int tid, uint32_t* hist,
+                                             uint32_t* red, Sync sync, uint32_t& thr_key, uint32_t& thr_idx) {
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, w = tid >> 5;
+  int hb = 0;
+  // f(key, index) for every entry of this thread (4 consecutive per load,
+  // four loads in flight per thread)
+  auto each4 = [&](auto f) {
+    constexpr int U = 4;
+    for (int b0 = tid * 4; b0 < n; b0 += 4 * NT * U) {
+      uint4 kv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e0 = b0 + u * 4 * NT;
+        kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e0 = b0 + u * 4 * NT;
+        f(kv[u].x, e0 + 0, e0 + 0 < n);
+        f(kv[u].y, e0 + 1, e0 + 1 < n);
+        f(kv[u].z, e0 + 2, e0 + 2 < n);
+        f(kv[u].w, e0 + 3, e0 + 3 < n);
+      }
+    }
+  };
+  auto minmax = [&](bool ties, uint32_t tk, uint32_t& lo, uint32_t& hi) {
+    for (int b = tid; b < 256; b += NT) hist[256 * hb + b] = 0;
+    uint32_t a = 0xFFFFFFFFu, bmax = 0;
+    each4([&](uint32_t kk, int e, bool ok) {
+      if (!ok || (ties && kk != tk)) return;
+      const uint32_t v = ties ? static_cast<uint32_t>(e) : kk;
+      a = min(a, v);
+      bmax = max(bmax, v);
+    });
+    a = __reduce_min_sync(0xFFFFFFFFu, a);
+    bmax = __reduce_max_sync(0xFFFFFFFFu, bmax);
+    if (lane == 0) {
+      red[w] = a;
+      red[NW + w] = bmax;
+    }
+    sync();
+    lo = 0xFFFFFFFFu;
+    hi = 0;
+    for (int i = 0; i < NW; ++i) {
+      lo = min(lo, red[i]);
+      hi = max(hi, red[NW + i]);
+    }
+    sync();  // red is reused by the next min/max
+  };
+  auto refine = [&](bool ties, uint32_t tk, uint32_t lo, uint32_t hi, int& r, uint32_t& value, uint32_t& count) {
+    while (true) {
+      const uint32_t range = hi - lo;
+      const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
+      uint32_t* h = hist + 256 * hb;
+      uint32_t* hn = hist + 256 * ((hb + 1) % 3);
+      for (int b = tid; b < 256; b += NT) hn[b] = 0;
+      each4([&](uint32_t kk, int e, bool ok) {
+        if (!ok) return;
+        const uint32_t v = ties ? static_cast<uint32_t>(e) : kk;
+        if ((ties && kk != tk) || v < lo || v > hi) return;
+        atomicAdd(&h[(v - lo) >> shift], 1u);
+      });
+      sync();
+      hb = (hb + 1) % 3;
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int bin = ties ? 8 * lane + i : 255 - 8 * lane - i;
+        c[i] = h[bin];
+        sum += c[i];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t excl = incl - sum;
+      uint32_t bin_found = 0, r_in = 0, cnt = 0;
+      bool mine = false;
+      if (excl < static_cast<uint32_t>(r) && incl >= static_cast<uint32_t>(r)) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (run + c[i] >= static_cast<uint32_t>(r)) {
+            bin_found = ties ? 8 * lane + i : 255 - 8 * lane - i;
+            r_in = static_cast<uint32_t>(r) - run;
+            cnt = c[i];
+            mine = true;
+            break;
+          }
+          run += c[i];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
+      bin_found = __shfl_sync(0xFFFFFFFFu, bin_found, src);
+      r = static_cast<int>(__shfl_sync(0xFFFFFFFFu, r_in, src));
+      count = __shfl_sync(0xFFFFFFFFu, cnt, src);
+      const uint64_t nlo = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(bin_found) << shift);
+      const uint64_t nhi = nlo + ((1ull << shift) - 1ull);
+      lo = static_cast<uint32_t>(nlo);
+      hi = static_cast<uint32_t>(nhi < hi ? nhi : hi);
+      if (shift == 0) {
+        value = lo;
+        return;
+      }
+    }
+  };
+  uint32_t lo, hi, cnt = 0;
+  int r = k;
+  minmax(false, 0, lo, hi);
+  refine(false, 0, lo, hi, r, thr_key, cnt);
+  if (static_cast<uint32_t>(r) == cnt) {
+    thr_idx = 0xFFFFFFFFu;
+    return;
+  }
+  minmax(true, thr_key, lo, hi);
+  refine(true, thr_key, lo, hi, r, thr_idx, cnt);
+}
+
+// ---------------------------------------------------------------------------
 // Conservative cut for a buffer that only needs shrinking (not the exact top-k):
 // returns the largest L such that at least k entries have key >= L, to bin
 // resolution: one min/max pass and one histogram pass over the live range.

@@ -27,8 +27,8 @@
 // (the i-th cheapest with the i-th most expensive, the "V" pairing of the
 // page's PCP section applied across SMs) so every CTA gets the same mix of
 // short and long causal rows. Decode ("split mode") takes all rows of one
-// sequence against one block of 8192 keys; a merge kernel then selects the
-// exact top-k of the per-block candidate lists.
+// sequence against one block of 8192 keys and writes every score to the
+// row's score array; select_kernel then takes each row's exact top-k.
 #include <algorithm>
 
 #include "common.cuh"
@@ -38,7 +38,8 @@ namespace smla {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;         // key-tile ring in group mode (the candidate buffers need the rest)
+constexpr int kSplitStages = 12;   // split mode keeps no candidates: 8 more stages in their space
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
@@ -65,10 +66,12 @@ struct IdxParams {
   int32_t acc_shift;  // log2 of the TMEM accumulator buffers (1, 2 or 4 buffers)
   int32_t* out_idx;
   float* out_scores;
-  uint32_t* cand_key;  // split mode: per (row, key block) lists; group mode: per-row deferred buffers
+  uint32_t* cand_key;  // group mode: per-row deferred candidate buffers
   uint32_t* cand_idx;
   int32_t* cand_cnt;
   int32_t defer;       // group mode: hand rows with more than topk candidates to finish_kernel
+  uint32_t* scores;    // split mode: score keys [rows][score_stride], written for keys 0..pos
+  int64_t score_stride;
   uint32_t* status;
 };
 
@@ -179,13 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 128);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]
   uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + 16);
-  uint64_t* a_full = bars;
-  uint64_t* a_empty = bars + kStages;
+  // ring barriers of stages 0-3, accumulators, query tile, then the ring
+  // barriers of the split-mode stages 4-11
   uint64_t* acc_full = bars + 2 * kStages;
   uint64_t* acc_empty = acc_full + kMaxAcc;
   uint64_t* b_full = acc_empty + kMaxAcc;
   uint64_t* b_empty = b_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + 1);
+  uint64_t* ring_x = b_empty + 1;  // [2][kSplitStages - kStages]
+  auto full_bar = [&](int st) { return st < kStages ? bars + st : ring_x + (st - kStages); };
+  auto empty_bar = [&](int st) {
+    return st < kStages ? bars + kStages + st : ring_x + (kSplitStages - kStages) + (st - kStages);
+  };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_x + 2 * (kSplitStages - kStages));
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,10 +202,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int N = HI * p.tq;
+  // key-tile ring: stages 0-3 ahead of the query tile; split mode adds stages
+  // 4-11 in the (unused) candidate-buffer space
+  const int nst = p.split ? kSplitStages : kStages;
+  auto stage_off = [](int st) -> uint32_t {
+    return st < kStages ? static_cast<uint32_t>(st * kStageBytes)
+                        : static_cast<uint32_t>(kStages * kStageBytes + kMaxN * kIdxRowBytes +
+                                                (st - kStages) * kStageBytes);
+  };
+  static_assert((kSplitStages - kStages) * kStageBytes <= 2 * kBufEntries * 4, "split stages fit");
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], 1);
+    for (int i = 0; i < kSplitStages; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -258,14 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (tt - tw) + 1);
           const int t = tile_at(it, tt);
           if (lane == 0) {
-            const int s = sc % kStages;
-            ok = mbar_wait(&a_empty[s], ((sc / kStages) & 1) ^ 1, abort_v, p.status);
+            const int s = sc % nst;
+            ok = mbar_wait(empty_bar(s), ((sc / nst) & 1) ^ 1, abort_v, p.status);
             if (ok) {
               const bool has1 = (2 * t + 1) * kPage < it.key_hi;
-              mbar_arrive_expect_tx(&a_full[s], has1 ? kStageBytes : kStageBytes / 2);
-              tma_load_2d(a_tiles + s * kStageBytes, &map_k, &a_full[s], 0, pg0 * kPage);
+              mbar_arrive_expect_tx(full_bar(s), has1 ? kStageBytes : kStageBytes / 2);
+              tma_load_2d(a_tiles + stage_off(s), &map_k, full_bar(s), 0, pg0 * kPage);
               if (has1)
-                tma_load_2d(a_tiles + s * kStageBytes + kStageBytes / 2, &map_k, &a_full[s], 0, pg1 * kPage);
+                tma_load_2d(a_tiles + stage_off(s) + kStageBytes / 2, &map_k, full_bar(s), 0, pg1 * kPage);
             }
           }
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -291,15 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         bool ok = true;
         for (int t = it.t0; t < it.t1; ++t, ++sc, ++ac) {
-          const int s = sc % kStages;
+          const int s = sc % nst;
           const int buf = ac & ((1 << p.acc_shift) - 1);
-          if (!mbar_wait_spin(&a_full[s], (sc / kStages) & 1, abort_v, p.status) ||
+          if (!mbar_wait_spin(full_bar(s), (sc / nst) & 1, abort_v, p.status) ||
               !mbar_wait_spin(&acc_empty[buf], ((ac >> p.acc_shift) & 1) ^ 1, abort_v, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * kStageBytes) >> 4);
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage_off(s) >> 4);
           const uint32_t d = tmem + buf * N;
 #pragma unroll
           for (int kk = 0; kk < kIdxRowBytes / 32; ++kk) {
@@ -307,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.is_bf16) mma_f16(d, ad + off, b_desc0 + off, idesc, kk > 0);
             else mma_f8(d, ad + off, b_desc0 + off, idesc, kk > 0);
           }
-          mma_commit(&a_empty[s]);
+          mma_commit(empty_bar(s));
           mma_commit(&acc_full[buf]);
         }
         if (!ok) break;
@@ -419,28 +436,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!to_output) {
             kb[off] = kk[q4];
             ib[off] = ii[q4];
-          } else if (!p.split) {
+          } else {
             p.out_idx[static_cast<size_t>(row) * topk + off] = static_cast<int32_t>(ii[q4]);
             if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + off] = key_score(kk[q4]);
-          } else {
-            const size_t slot = (static_cast<size_t>(row) * p.n_kblocks + it.kb) * topk + off;
-            p.cand_key[slot] = kk[q4];
-            p.cand_idx[slot] = ii[q4];
           }
           ++off;
         }
         base += total;
       }
       if (to_output) {
-        if (!p.split) {
-          for (int e = base + tid_wg; e < topk; e += 128) {
-            p.out_idx[static_cast<size_t>(row) * topk + e] = -1;
-            if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + e] = 0.0f;
-          }
-          if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;  // row complete
-        } else if (tid_wg == 0) {
-          p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + it.kb] = base;
+        for (int e = base + tid_wg; e < topk; e += 128) {
+          p.out_idx[static_cast<size_t>(row) * topk + e] = -1;
+          if (p.out_scores) p.out_scores[static_cast<size_t>(row) * topk + e] = 0.0f;
         }
+        if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;  // row complete
       }
       wg_sync();
       if (!to_output && tid_wg == 0) {
@@ -528,6 +537,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
         }
+        if (p.split) {
+          // decode: every score goes to the row's score array; select_kernel
+          // takes the exact top-k of each row afterwards
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj) {
+            const int j = j0 + jj;
+            if (j < j1 && j < it.nrows && s < it.key_hi && s <= it.pos0 + j)
+              p.scores[static_cast<int64_t>(it.row0 + j) * p.score_stride + s] = key[jj];
+          }
+          continue;
+        }
         wg_sync();
         for (int j = j0; j < j1; ++j)
           if (cnt[j] > cap - kTileKeys) select_token(j, topk, false, it);
@@ -549,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      if (p.split) continue;
       wg_sync();
       for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
     }
@@ -560,81 +581,88 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Decode merge: exact top-k of the per-key-block candidate lists of one row.
-struct MergeParams {
-  const uint32_t* cand_key;
-  const uint32_t* cand_idx;
-  const int32_t* cand_cnt;
+// Split mode (decode), step 2: the exact top-k of one row's dense score array
+// (written by the scoring kernel for keys 0..pos). One CTA of 1024 threads
+// per row; scores are read from global memory (they stay in L2).
+struct SelectParams {
+  const uint32_t* scores;
+  int64_t score_stride;
   const int32_t* seq_lens;
-  int32_t q_per_seq, n_kblocks, topk;
+  int32_t q_per_seq, topk;
   int32_t* out_idx;
   float* out_scores;
 };
 
-constexpr int kMergeThreads = 512;
+constexpr int kSelThreads = 1024;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t scratch[8];
-  __shared__ uint32_t wsum[kMergeThreads / 32];
-  __shared__ int32_t counts[256];
-  const int row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
+  __shared__ uint32_t hist[768];
+  __shared__ uint32_t red[2 * kSelThreads / 32];
+  __shared__ uint32_t wsum[kSelThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int seq = row / p.q_per_seq;
-  const int nb = min((p.seq_lens[seq] + kKeyBlock - 1) / kKeyBlock, p.n_kblocks);
-  int total = 0;
-  for (int b = 0; b < nb; ++b) total += p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + b];
-  if (tid < 256) counts[tid] = 0;
-  __syncthreads();
-  for (int b = tid; b < nb && b < 256; b += kMergeThreads) counts[b] = p.cand_cnt[static_cast<size_t>(row) * p.n_kblocks + b];
-  __syncthreads();
-  const size_t base_row = static_cast<size_t>(row) * p.n_kblocks;
-  auto blk_cnt = [&](int b) { return b < 256 ? counts[b] : p.cand_cnt[base_row + b]; };
-  auto each = [&](auto f) {
-    for (int b = 0; b < nb; ++b) {
-      const int c = blk_cnt(b);
-      const size_t off = (base_row + b) * p.topk;
-      for (int i = tid; i < c; i += kMergeThreads) f(p.cand_key[off + i], p.cand_idx[off + i]);
-    }
-  };
-  auto sync = [&]() { __syncthreads(); };
-  uint32_t tk = 0, ti = 0xFFFFFFFFu;
-  const bool all = total <= p.topk;
-  if (!all) radix_select<kMergeThreads>(p.topk, tid, hist, scratch, each, sync, tk, ti);
+  const int pos = p.seq_lens[seq] - p.q_per_seq + (row - seq * p.q_per_seq);
+  const int n = pos + 1;  // keys 0..pos
+  const uint32_t* keys = p.scores + static_cast<int64_t>(row) * p.score_stride;
   int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
   float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
-  int outn = 0;
-  const uint32_t lanemask_lt = (1u << lane) - 1u;
-  for (int b = 0; b < nb; ++b) {
-    const int c = blk_cnt(b);
-    const size_t off = (base_row + b) * p.topk;
-    for (int c0 = 0; c0 < c; c0 += kMergeThreads) {
-      const int i = c0 + tid;
-      uint32_t key = 0, idx = 0;
-      bool take = false;
-      if (i < c) {
-        key = p.cand_key[off + i];
-        idx = p.cand_idx[off + i];
-        take = all || selected(key, idx, tk, ti);
-      }
-      const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
-      if (lane == 0) wsum[warp] = __popc(m);
-      __syncthreads();
-      int pos = outn, tot = 0;
-      for (int w2 = 0; w2 < kMergeThreads / 32; ++w2) {
-        if (w2 < warp) pos += wsum[w2];
-        tot += wsum[w2];
-      }
-      pos += __popc(m & lanemask_lt);
-      __syncthreads();
-      if (take) {
-        o[pos] = static_cast<int32_t>(idx);
-        if (os) os[pos] = key_score(key);
-      }
-      outn += tot;
-    }
+  auto sync = []() { __syncthreads(); };
+  uint32_t tk = 0, ti = 0xFFFFFFFFu;
+  const bool all = n <= p.topk;
+  if (n > 0 && !all) dense_select<kSelThreads>(keys, n, p.topk, tid, hist, red, sync, tk, ti);
+  // output in a fixed order: warp w takes the 128-entry segments w, w + 32, ...
+  // (lane l holds entries 4l..4l+3 of a segment); pass 1 counts each warp's
+  // selected entries, pass 2 writes them after the earlier warps' ones
+  constexpr int kW = kSelThreads / 32;
+  const int nseg = (n + 127) / 128;
+  auto seg_take = [&](int sg, uint32_t (&kk)[4], bool (&tk4)[4]) {
+    const int e0 = sg * 128 + 4 * lane;
+    const uint4 v = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+    kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      tk4[q] = e0 + q < n && (all || selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti));
+  };
+  int mine = 0;
+  for (int sg = w; sg < nseg; sg += kW) {
+    uint32_t kk[4];
+    bool tk4[4];
+    seg_take(sg, kk, tk4);
+    mine += tk4[0] + tk4[1] + tk4[2] + tk4[3];
   }
-  for (int e = outn + tid; e < p.topk; e += kMergeThreads) {
+  mine = __reduce_add_sync(0xFFFFFFFFu, mine);
+  if (lane == 0) wsum[w] = mine;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w2 = 0; w2 < kW; ++w2) {
+    const int v = static_cast<int>(wsum[w2]);
+    if (w2 < w) base += v;
+    total += v;
+  }
+  for (int sg = w; sg < nseg; sg += kW) {
+    uint32_t kk[4];
+    bool tk4[4];
+    seg_take(sg, kk, tk4);
+    const int c = tk4[0] + tk4[1] + tk4[2] + tk4[3];
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += t2;
+    }
+    int q0 = base + incl - c;
+    const int e0 = sg * 128 + 4 * lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (!tk4[q]) continue;
+      o[q0] = e0 + q;
+      if (os) os[q0] = key_score(kk[q]);
+      ++q0;
+    }
+    base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  base = total;
+  for (int e = base + tid; e < p.topk; e += kSelThreads) {
     o[e] = -1;
     if (os) os[e] = 0.0f;
   }
@@ -730,7 +758,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kStages + 2 * kMaxAcc + 2) * 8 + 16;
+                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 2) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -778,9 +806,9 @@ size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_pe
                                int32_t topk) {
   size_t bytes = kStatusBytes;
   if (indexer_split_mode(q_per_seq, h_idx)) {
-    const size_t nkb = (static_cast<size_t>(max_seq_len) + kKeyBlock - 1) / kKeyBlock;
+    // one score key per (row, key): rows x max_seq_len rounded up to 4
     const size_t rows = static_cast<size_t>(n_seqs) * q_per_seq;
-    bytes += rows * nkb * topk * 8 + ((rows * nkb * 4 + 255) / 256) * 256;
+    bytes += rows * ((static_cast<size_t>(max_seq_len) + 3) / 4 * 4) * 4;
   }
   return bytes;
 }
@@ -820,10 +848,8 @@ int launch_indexer(const IndexerLaunch& L) {
   if (split) {
     prm.n_kblocks = (L.max_seq_len + kKeyBlock - 1) / kKeyBlock;
     prm.n_items = L.n_seqs * prm.n_kblocks;
-    const size_t nk = static_cast<size_t>(prm.n_kblocks);
-    prm.cand_key = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-    prm.cand_idx = prm.cand_key + rows * nk * L.topk;
-    prm.cand_cnt = reinterpret_cast<int32_t*>(prm.cand_idx + rows * nk * L.topk);
+    prm.scores = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+    prm.score_stride = (static_cast<int64_t>(L.max_seq_len) + 3) / 4 * 4;
   } else {
     prm.n_groups = (L.q_per_seq + tq - 1) / tq;
     prm.n_items = L.n_seqs * prm.n_groups;
@@ -859,9 +885,8 @@ int launch_indexer(const IndexerLaunch& L) {
     finish_kernel<<<prm.n_rows, kFinishThreads, fsmem, L.stream>>>(fp);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
   }
-  MergeParams mp{prm.cand_key, prm.cand_idx, prm.cand_cnt, L.seq_lens, L.q_per_seq, prm.n_kblocks, L.topk,
-                 L.out_idx, L.out_scores};
-  merge_kernel<<<prm.n_rows, kMergeThreads, 0, L.stream>>>(mp);
+  SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.q_per_seq, L.topk, L.out_idx, L.out_scores};
+  select_kernel<<<prm.n_rows, kSelThreads, 0, L.stream>>>(sp);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
