@@ -184,6 +184,11 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
  * q_per_seq new tokens each (1 for plain decode, 2 for one MTP draft), over a
  * paged cache with one page table per request. Arguments as in
  * smla_indexer_topk and smla_sparse_mla_fwd. q_per_seq must be in [1, 8].
+ * Workspace: the returned size holds, in order, the indexer's part (see
+ * smla_indexer_topk), the index list, and room for fp32 partial outputs: with
+ * fewer query rows than SMs each row's selection is cut into up to 4 parts
+ * attended on different SMs and merged by their log-sum-exp (used only when
+ * the workspace reaches its end).
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_decode_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
                                              int32_t n_heads, int32_t h_idx, int32_t topk);

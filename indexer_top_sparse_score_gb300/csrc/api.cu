@@ -257,11 +257,12 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
 }
 
 // ----------------------------------------------------------------- decode
-size_t smla_sparse_mla_decode_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t,
-                                             int32_t h_idx, int32_t topk) {
+size_t smla_sparse_mla_decode_workspace_size(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq,
+                                             int32_t n_heads, int32_t h_idx, int32_t topk) {
   if (n_seqs <= 0 || max_seq_len <= 0 || q_per_seq <= 0 || topk <= 0) return kStatusBytes;
   return round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk)) +
-         round256(static_cast<size_t>(n_seqs) * q_per_seq * topk * 4);
+         round256(static_cast<size_t>(n_seqs) * q_per_seq * topk * 4) +
+         (n_heads > 0 ? mla_partial_bytes(n_seqs * q_per_seq, n_heads) : 0);
 }
 
 int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
@@ -291,6 +292,12 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
   if ((rc = launch_indexer(IL))) return rc;
   MlaLaunch ML{cache, page_tables, max_pages, n_seqs, q_per_seq, seq_lens, 0, q, n_heads, idx, topk, sm_scale, out,
                lse, static_cast<uint32_t*>(workspace), st};
+  // layout: indexer part | index list | partial outputs of split rows (if it fits)
+  const size_t part_off = idx_ws + round256(static_cast<size_t>(n_seqs) * q_per_seq * topk * 4);
+  if (workspace_bytes > part_off) {
+    ML.partials = static_cast<uint8_t*>(workspace) + part_off;
+    ML.partial_bytes = workspace_bytes - part_off;
+  }
   return launch_mla(ML);
 }
 

@@ -165,7 +165,9 @@ __device__ __forceinline__ void tmem_ld_heads(uint32_t taddr, uint32_t* r) {
   }
 }
 
-template <int HI>
+// SPLIT: decode shape (compile-time, so the decode kernel carries none of the
+// candidate-selection code)
+template <int HI, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IdxParams p) {
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = HI * p.tq;
   // key-tile ring: stages 0-3 ahead of the query tile; split mode adds stages
   // 4-11 in the (unused) candidate-buffer space
-  const int nst = p.split ? kSplitStages : kStages;
+  const int nst = SPLIT ? kSplitStages : kStages;
   auto stage_off = [](int st) -> uint32_t {
     return st < kStages ? static_cast<uint32_t>(st * kStageBytes)
                         : static_cast<uint32_t>(kStages * kStageBytes + kMaxN * kIdxRowBytes +
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
         const int t = tile_at(it, tt);
         const int buf = ac & ((1 << p.acc_shift) - 1);
-        if (!mbar_wait_spin(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
+        if (!mbar_wait_backoff(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
           ok = false;
           break;
         }
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
         }
-        if (p.split) {
+        if constexpr (SPLIT) {
           // decode: every score goes to the row's score array; select_kernel
           // takes the exact top-k of each row afterwards
 #pragma unroll
@@ -569,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (p.split) continue;
+      if constexpr (SPLIT) continue;
       wg_sync();
       for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
     }
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
   }
 }
 
-template <int HI>
+template <int HI, bool SPLIT>
 int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
   CUtensorMap map_k, map_q;
   const CUtensorMapDataType dt = prm.is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -761,14 +763,14 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                       1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 2) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     attr_done = true;
   }
   const int grid_items = prm.split ? prm.n_items : (prm.n_items + 1) / 2;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
-  indexer_kernel<HI><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  indexer_kernel<HI, SPLIT><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
@@ -863,11 +865,11 @@ int launch_indexer(const IndexerLaunch& L) {
   }
   int rc;
   switch (L.h_idx) {
-    case 4: rc = launch_indexer_t<4>(L, prm); break;
-    case 8: rc = launch_indexer_t<8>(L, prm); break;
-    case 16: rc = launch_indexer_t<16>(L, prm); break;
-    case 32: rc = launch_indexer_t<32>(L, prm); break;
-    case 64: rc = launch_indexer_t<64>(L, prm); break;
+    case 4: rc = split ? launch_indexer_t<4, true>(L, prm) : launch_indexer_t<4, false>(L, prm); break;
+    case 8: rc = split ? launch_indexer_t<8, true>(L, prm) : launch_indexer_t<8, false>(L, prm); break;
+    case 16: rc = split ? launch_indexer_t<16, true>(L, prm) : launch_indexer_t<16, false>(L, prm); break;
+    case 32: rc = split ? launch_indexer_t<32, true>(L, prm) : launch_indexer_t<32, false>(L, prm); break;
+    case 64: rc = split ? launch_indexer_t<64, true>(L, prm) : launch_indexer_t<64, false>(L, prm); break;
     default: return SMLA_ERR_UNSUPPORTED;
   }
   if (rc != SMLA_OK) return rc;

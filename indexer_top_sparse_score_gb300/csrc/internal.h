@@ -60,7 +60,17 @@ struct MlaLaunch {
   // of a single sequence), or null to gather and widen the pool rows in-kernel
   void* shadow = nullptr;
   int32_t shadow_rows = 0;
+  // room for the partial outputs of split rows (few rows: each row's
+  // selection is cut into parts spread over SMs and merged by lse), or null
+  void* partials = nullptr;
+  size_t partial_bytes = 0;
 };
+
+// Parts a row is split into when there are few rows (at most kMaxParts).
+constexpr int kMaxParts = 4;
+int mla_parts(int32_t n_rows, int32_t topk);
+// Workspace bytes for the partial outputs of n_rows split rows.
+size_t mla_partial_bytes(int32_t n_rows, int32_t n_heads);
 
 // Workspace of a prefill without the optional f16 shadow (status + index list).
 size_t prefill_min_workspace(int32_t n_tokens, int32_t topk);

@@ -76,6 +76,11 @@ struct MlaParams {
   uint32_t* status;
   const uint16_t* shadow;  // f16 rows by logical position, or null
   int32_t shadow_rows;
+  // split rows: each row's blocks are cut into n_parts items of part_blocks
+  // blocks; each item writes a normalised fp32 partial output and its lse
+  int32_t n_parts, part_blocks;
+  float* part_o;    // [rows * n_parts][H][512]
+  float* part_lse;  // [rows * n_parts][H]
 };
 
 struct SmemMeta {
@@ -94,28 +99,34 @@ struct SmemMeta {
 constexpr size_t kSmemBytes = kQBytes + kStageBytes + sizeof(SmemMeta);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// k-th row of this CTA: head/tail pairs. -1 done, 0 skip, 1 row.
-__device__ __forceinline__ int next_row(int n_rows, int k, int& row) {
-  const int P = (n_rows + 1) / 2;
+// k-th work item of this CTA (a query row, or one part of a split row):
+// head/tail pairs over the items. -1 done, 0 skip, 1 item.
+__device__ __forceinline__ int next_row(int n_items, int k, int& item) {
+  const int P = (n_items + 1) / 2;
   const int pair = blockIdx.x + (k >> 1) * gridDim.x;
   if (pair >= P) return -1;
-  row = (k & 1) ? (n_rows - 1 - pair) : pair;
-  if ((k & 1) && row == pair) return 0;
+  item = (k & 1) ? (n_items - 1 - pair) : pair;
+  if ((k & 1) && item == pair) return 0;
   return 1;
 }
 
 struct RowInfo {
-  int seq, pos, nvalid, nb;
+  int row, seq, pos, nvalid;
+  int b0, nb;  // the item's blocks: b0 .. b0 + nb - 1 of the row's selection
 };
 
-__device__ __forceinline__ RowInfo row_info(const MlaParams& p, int row) {
+__device__ __forceinline__ RowInfo row_info(const MlaParams& p, int item) {
   RowInfo r;
-  r.seq = row / p.q_per_seq;
-  const int j = row - r.seq * p.q_per_seq;
+  r.row = item / p.n_parts;
+  const int part = item - r.row * p.n_parts;
+  r.seq = r.row / p.q_per_seq;
+  const int j = r.row - r.seq * p.q_per_seq;
   const int L = p.seq_lens ? p.seq_lens[r.seq] : p.prefix_len + p.q_per_seq;
   r.pos = L - p.q_per_seq + j;
   r.nvalid = max(0, min(p.topk, r.pos + 1));
-  r.nb = (r.nvalid + kBlk - 1) / kBlk;
+  const int nb_row = (r.nvalid + kBlk - 1) / kBlk;
+  r.b0 = part * p.part_blocks;
+  r.nb = max(0, min(nb_row - r.b0, p.part_blocks));
   return r;
 }
 
@@ -288,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         int row;
-        const int r = next_row(p.n_rows, k, row);
+        const int r = next_row(p.n_rows * p.n_parts, k, row);
         if (r < 0) break;
         if (r == 0) continue;
         const RowInfo ri = row_info(p, row);
@@ -348,15 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool over = false;
     for (int k = 0; ok; ++k) {
       int row;
-      const int r = next_row(p.n_rows, k, row);
+      const int r = next_row(p.n_rows * p.n_parts, k, row);
       if (r < 0) break;
       if (r == 0) continue;
       const RowInfo ri = row_info(p, row);
       if (ri.nb == 0) continue;
+      row = ri.row;
       const int32_t* pt = p.page_tables + static_cast<size_t>(ri.seq) * p.max_pages;
       const int32_t* ir = p.idx + static_cast<size_t>(row) * p.topk;
       auto fetch_key = [&](int b) -> int {
-        const int e = b * kBlk + 32 * pw + lane;
+        const int e = (ri.b0 + b) * kBlk + 32 * pw + lane;
         return (b < ri.nb && e < ri.nvalid) ? __ldg(ir + e) : -1;
       };
       auto fetch_page = [&](int key) -> int {
@@ -410,14 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(2, kProducers);
         if (tid == 0) mbar_arrive(&M.q_full);
       }
-      int key0 = fetch_key(0), key1 = fetch_key(1);
-      int pg0 = fetch_page(key0);
+      // keys three blocks ahead and page ids two ahead (each consumed a block
+      // after it was requested); the pool rows of the next block are
+      // prefetched into L2 while this block is copied
+      const int key0 = fetch_key(0);
+      int key1 = fetch_key(1), key2 = fetch_key(2);
+      int loc = locate(key0, fetch_page(key0));
+      int pg1 = fetch_page(key1);
+      const uint32_t row_bytes = p.fp8 ? kDqk : 2 * kDqk;
       for (int b = 0; b < ri.nb && ok; ++b, ++g) {
-        const int loc = locate(key0, pg0);
         float ks = 1.0f;
         if (p.fp8 && loc >= 0) ks = __ldg(p.kv_scale + loc);
-        const int key2 = fetch_key(b + 2);
-        const int pg1 = fetch_page(key1);
+        const int key3 = fetch_key(b + 3);
+        const int loc1 = locate(key1, pg1);
+        if (!p.shadow && loc1 >= 0) prefetch_l2_bulk(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
+        const int pg2 = fetch_page(key2);
         int rl[8];  // pool rows of this lane's copy passes
 #pragma unroll
         for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
@@ -506,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        key0 = key1;
+        loc = loc1;
         key1 = key2;
-        pg0 = pg1;
+        key2 = key3;
+        pg1 = pg2;
       }
       ++tok;
     }
@@ -529,14 +549,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     for (int k = 0;; ++k) {
       int row;
-      const int r = next_row(p.n_rows, k, row);
+      const int r = next_row(p.n_rows * p.n_parts, k, row);
       if (r < 0) break;
       if (r == 0) continue;
       const RowInfo ri = row_info(p, row);
+      const int item = row;
+      row = ri.row;
       uint16_t* orow = p.out + static_cast<size_t>(row) * H * kDv;
       if (ri.nb == 0) {
-        for (int i = tid; i < H * kDv / 8; i += 256) reinterpret_cast<uint4*>(orow)[i] = make_uint4(0, 0, 0, 0);
-        if (p.lse && tid < H) p.lse[static_cast<size_t>(row) * H + tid] = -INFINITY;
+        if (p.n_parts > 1) {
+          if (tid < H) p.part_lse[static_cast<size_t>(item) * H + tid] = -INFINITY;
+        } else {
+          for (int i = tid; i < H * kDv / 8; i += 256) reinterpret_cast<uint4*>(orow)[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse && tid < H) p.lse[static_cast<size_t>(row) * H + tid] = -INFINITY;
+        }
         continue;
       }
       bool ok = true;
@@ -656,14 +682,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < H) {
         const float lt = (M.red[0][tid] + M.red[1][tid]) + (M.red[2][tid] + M.red[3][tid]);
         M.linv[tid] = lt > 0.0f ? 1.0f / lt : 0.0f;
-        if (p.lse)
-          p.lse[static_cast<size_t>(row) * H + tid] =
-              lt > 0.0f ? (M.m[tid] + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        const float lse = lt > 0.0f ? (M.m[tid] + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        if (p.n_parts > 1) p.part_lse[static_cast<size_t>(item) * H + tid] = lse;
+        else if (p.lse) p.lse[static_cast<size_t>(row) * H + tid] = lse;
       }
       named_bar_sync(1, 256);
       const bool odd = lane & 1;
+      if (p.n_parts > 1) {
+        // normalised fp32 partial output of this part: [H][512]
+        float* po = p.part_o + static_cast<size_t>(item) * H * kDv;
 #pragma unroll 1
-      for (int dt = 0; dt < 4; ++dt) {
+        for (int dt = 0; dt < 4; ++dt) {
+          const int d = dt * 128 + qd * 32 + lane;
+          uint32_t o[HW];
+          tmem_ld_cols<HW>(tmem + lane_base + kColO + dt * 64 + h0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HW; ++c) po[static_cast<size_t>(h0 + c) * kDv + d] = __uint_as_float(o[c]) * M.linv[h0 + c];
+        }
+      }
+#pragma unroll 1
+      for (int dt = 0; dt < (p.n_parts > 1 ? 0 : 4); ++dt) {
         const int d = dt * 128 + qd * 32 + lane;
         const int d_even = d & ~1;
         uint32_t o[HW];
@@ -691,6 +730,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Merge of split rows: out = sum_s w_s * o_s with w_s = exp(lse_s - lse) and
+// lse = log sum_s exp(lse_s) (the partial attentions of disjoint key sets,
+// each normalised over its own keys). One CTA per row.
+__global__ void __launch_bounds__(256) part_merge_kernel(const float* __restrict__ part_o,
+                                                         const float* __restrict__ part_lse, int n_parts,
+                                                         int n_heads, uint16_t* __restrict__ out, float* lse) {
+  __shared__ float wgt[kMaxParts][64];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const size_t item0 = static_cast<size_t>(row) * n_parts;
+  if (tid < n_heads) {
+    float m = -INFINITY;
+    for (int s = 0; s < n_parts; ++s) m = fmaxf(m, part_lse[(item0 + s) * n_heads + tid]);
+    float sum = 0.0f;
+    float e[kMaxParts];
+    for (int s = 0; s < n_parts; ++s) {
+      const float l = part_lse[(item0 + s) * n_heads + tid];
+      e[s] = (m == -INFINITY || l == -INFINITY) ? 0.0f : __expf(l - m);
+      sum += e[s];
+    }
+    for (int s = 0; s < n_parts; ++s) wgt[s][tid] = sum > 0.0f ? e[s] / sum : 0.0f;
+    if (lse) lse[static_cast<size_t>(row) * n_heads + tid] = sum > 0.0f ? m + __logf(sum) : -INFINITY;
+  }
+  __syncthreads();
+  for (int i = tid; i < n_heads * kDv / 2; i += 256) {
+    const int h = i / (kDv / 2), d = 2 * (i - h * (kDv / 2));
+    float v0 = 0.0f, v1 = 0.0f;
+    for (int s = 0; s < n_parts; ++s) {
+      const float ws = wgt[s][h];
+      if (ws == 0.0f) continue;  // empty part: its output was never written
+      const float2 o = *reinterpret_cast<const float2*>(part_o + ((item0 + s) * n_heads + h) * kDv + d);
+      v0 = fmaf(ws, o.x, v0);
+      v1 = fmaf(ws, o.y, v1);
+    }
+    *reinterpret_cast<uint32_t*>(out + (static_cast<size_t>(row) * n_heads + h) * kDv + d) = pack_bf16(v0, v1);
+  }
+}
+
 template <int H>
 int launch_t(const MlaLaunch& L, const MlaParams& prm) {
   static bool attr_done = false;
@@ -700,9 +776,14 @@ int launch_t(const MlaLaunch& L, const MlaParams& prm) {
       return SMLA_ERR_CUDA;
     attr_done = true;
   }
-  const int grid = std::max(1, std::min(num_sms(), (prm.n_rows + 1) / 2));
+  const int grid = std::max(1, std::min(num_sms(), (prm.n_rows * prm.n_parts + 1) / 2));
   mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  if (prm.n_parts > 1) {
+    part_merge_kernel<<<prm.n_rows, 256, 0, L.stream>>>(prm.part_o, prm.part_lse, prm.n_parts, H, prm.out,
+                                                        prm.lse);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  }
   return SMLA_OK;
 }
 
@@ -741,6 +822,19 @@ __global__ void __launch_bounds__(256) shadow_convert_kernel(const uint16_t* __r
 
 }  // namespace
 
+int mla_parts(int32_t n_rows, int32_t topk) {
+  const int nb_row = (topk + kBlk - 1) / kBlk;
+  const int sms = num_sms();
+  if (n_rows <= 0 || n_rows >= sms || nb_row < 2) return 1;
+  // about four work items per SM
+  return std::max(1, std::min({kMaxParts, nb_row, (4 * sms + n_rows - 1) / n_rows}));
+}
+
+size_t mla_partial_bytes(int32_t n_rows, int32_t n_heads) {
+  const size_t items = static_cast<size_t>(n_rows) * kMaxParts;
+  return items * n_heads * kDv * 4 + (items * n_heads * 4 + 255) / 256 * 256;
+}
+
 size_t mla_shadow_bytes(int32_t n_keys) {
   return n_keys > 0 ? (static_cast<size_t>(n_keys) * kDqk * 2 + 255) / 256 * 256 : 0;
 }
@@ -777,7 +871,18 @@ int launch_mla(const MlaLaunch& L) {
   prm.status = L.status;
   prm.shadow = static_cast<const uint16_t*>(L.shadow);
   prm.shadow_rows = L.shadow_rows;
+  prm.n_parts = 1;
+  prm.part_blocks = (L.topk + kBlk - 1) / kBlk;
   if (prm.n_rows == 0) return SMLA_OK;
+  const int parts = mla_parts(prm.n_rows, L.topk);
+  if (parts > 1 && L.partials && L.partial_bytes >= mla_partial_bytes(prm.n_rows, L.n_heads) &&
+      (reinterpret_cast<uintptr_t>(L.partials) & 15u) == 0) {
+    const int nb_row = (L.topk + kBlk - 1) / kBlk;
+    prm.part_blocks = (nb_row + parts - 1) / parts;
+    prm.n_parts = (nb_row + prm.part_blocks - 1) / prm.part_blocks;
+    prm.part_o = static_cast<float*>(L.partials);
+    prm.part_lse = prm.part_o + static_cast<size_t>(prm.n_rows) * kMaxParts * L.n_heads * kDv;
+  }
   switch (L.n_heads) {
     case 16: return launch_t<16>(L, prm);
     case 64: return launch_t<64>(L, prm);

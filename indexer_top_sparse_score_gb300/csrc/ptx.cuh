@@ -130,6 +130,27 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, v
   }
 }
 
+// Bounded wait that polls with a short sleep between tests: for waits that
+// usually last long while other warps of the SM need the issue slots (the
+// sleeping warp is not eligible). Same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t* status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (abort && *abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        if (status) atomicOr(status, kStatusTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // --------------------------------------------------------------------------
 // proxy fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -144,6 +165,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

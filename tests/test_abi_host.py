@@ -101,10 +101,11 @@ def test_workspace_sizes(L):
         256 + 16384 * 2048 * 4 + 16384 * 576 * 2 + cand
     # the indexer alone: status word + the same candidate buffers
     assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256 + cand
-    # decode: a score per (row, key) up to max_seq_len, then the index list
+    # decode: a score per (row, key) up to max_seq_len, the index list, then
+    # room for the fp32 partial outputs (and lse) of rows split into up to 4 parts
     rows, k = 128, 2048
     dec = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
-    assert dec == 256 + rows * 131072 * 4 + rows * k * 4
+    assert dec == 256 + rows * 131072 * 4 + rows * k * 4 + rows * 4 * 64 * 512 * 4 + rows * 4 * 64 * 4
     assert L.smla_sparse_mla_fwd_workspace_size(0, 100, 64, 2048, 0) == 256
     assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 1) == 256
     assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 0) == 256 + 1000 * 1152
