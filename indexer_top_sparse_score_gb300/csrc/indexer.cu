@@ -97,7 +97,12 @@ __device__ __forceinline__ int tile_at(const Item& it, int tt) {
 // The k-th item of this CTA. Returns -1 when the CTA has no more items, 0 for
 // an empty slot (skip), 1 for a real item. Every role calls this with the
 // same k sequence, so all roles agree on the schedule.
-__device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it) {
+// kMaxPrefix: split mode enumerates only the non-empty (sequence, key block)
+// items through a per-CTA prefix sum of the sequences' block counts held in
+// the (otherwise unused) histogram scratch, for up to this many sequences.
+constexpr int kMaxPrefixSeqs = 1535;
+
+__device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, const uint32_t* pref) {
   if (!p.split) {
     const int G = p.n_items;
     const int P = (G + 1) / 2;
@@ -119,9 +124,23 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it) {
     it.trivial = it.key_hi <= p.topk && p.out_scores == nullptr;
   } else {
     const int i = blockIdx.x + k * gridDim.x;
-    if (i >= p.n_items) return -1;
-    const int seq = i / p.n_kblocks;
-    const int kb = i - seq * p.n_kblocks;
+    int seq, kb;
+    if (pref) {
+      // i-th non-empty item: the sequence whose block range holds i
+      if (i >= static_cast<int>(pref[p.n_seqs])) return -1;
+      int lo = 0, hi = p.n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int>(pref[mid]) <= i) lo = mid;
+        else hi = mid - 1;
+      }
+      seq = lo;
+      kb = i - static_cast<int>(pref[seq]);
+    } else {
+      if (i >= p.n_items) return -1;
+      seq = i / p.n_kblocks;
+      kb = i - seq * p.n_kblocks;
+    }
     const int L = p.seq_lens[seq];
     if (kb * kKeyBlock >= L) return 0;
     it.seq = seq;
@@ -231,6 +250,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
+  // split mode: prefix sums of the sequences' key-block counts (hist is unused there)
+  const uint32_t* pref = nullptr;
+  if constexpr (SPLIT) {
+    if (p.n_seqs <= kMaxPrefixSeqs) {
+      if (threadIdx.x == 0) {
+        uint32_t acc = 0;
+        for (int b = 0; b < p.n_seqs; ++b) {
+          hist[b] = acc;
+          const int L = min(p.seq_lens[b], p.n_kblocks * kKeyBlock);
+          acc += static_cast<uint32_t>(max(0, (L + kKeyBlock - 1) / kKeyBlock));
+        }
+        hist[p.n_seqs] = acc;
+      }
+      pref = hist;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -250,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Item it;
-      const int r = next_item(p, k, it);
+      const int r = next_item(p, k, it, pref);
       if (r < 0) break;
       if (r == 0 || it.trivial) continue;
       if (lane == 0) {
@@ -302,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = smem_desc(smem_u32(b_tile), 16, 1024);
       for (int k = 0;; ++k) {
         Item it;
-        const int r = next_item(p, k, it);
+        const int r = next_item(p, k, it, pref);
         if (r < 0) break;
         if (r == 0 || it.trivial) continue;
         if (!mbar_wait(b_full, bi & 1, abort_v, p.status)) break;
@@ -466,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int k = 0;; ++k) {
       Item it;
-      const int r = next_item(p, k, it);
+      const int r = next_item(p, k, it, pref);
       if (r < 0) break;
       if (r == 0) continue;
       named_bar_sync(3, kEpiThreads);

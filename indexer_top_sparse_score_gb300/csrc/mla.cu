@@ -437,15 +437,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int loc1 = locate(key1, pg1);
         if (!p.shadow && loc1 >= 0) prefetch_l2_bulk(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
         const int pg2 = fetch_page(key2);
-        int rl[8];  // pool rows of this lane's copy passes
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
         const uint32_t ph_e = (g & 1) ^ 1;  // slot of block g free: PV of block g-1 done
         auto meta = [&]() {
           M.row[g & 1][32 * pw + lane] =
               loc >= 0 ? make_float4(ks * p.scale_log2, ks, 1.0f, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
         };
         if (p.shadow) {
+          int rl[8];  // pool rows of this lane's copy passes
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
 #pragma unroll
           for (int grp = 0; grp < kGroups; ++grp) {
             if (!mbar_wait(&M.empty[grp < 4 ? grp : 3], ph_e, abort_v, p.status)) { ok = false; break; }
@@ -470,9 +470,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           meta();
           fence_proxy_async_smem();
           mbar_arrive(&M.full[kGroups - 1]);
+        } else if (p.fp8) {
+          // e4m3 rows: one chunk (64 values = 64 bytes per row) per unit; lane l
+          // takes 16 bytes (q = l & 3) of row 32pw + (l >> 2) + 8i in pass i and
+          // widens them into f16 pieces 2q and 2q+1; units u+1 and u+2 are in
+          // flight while unit u is stored
+          const int rs8 = lane >> 2, q4 = lane & 3;
+          int rl8[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rl8[i] = __shfl_sync(0xFFFFFFFFu, loc, rs8 + 8 * i);
+          uint4 st8[3][4];
+          auto load8 = [&](int c, uint4* dst) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = rl8[i] < 0 ? make_uint4(0, 0, 0, 0)
+                                  : ldg_stream(p.kv + static_cast<int64_t>(rl8[i]) * kDqk + c * 64 + q4 * 16);
+          };
+          load8(0, st8[0]);
+          load8(1, st8[1]);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const int grp = c < 8 ? c >> 1 : 4;
+            if (c + 2 < kChunks) load8(c + 2, st8[(c + 2) % 3]);
+            if ((c & 1) == 0 && !mbar_wait(&M.empty[grp < 4 ? grp : 3], ph_e, abort_v, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* cp = stage + c * kChunkBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 w = st8[c % 3][i];
+              const int rw = 32 * pw + rs8 + 8 * i;
+              *reinterpret_cast<uint4*>(cp + sw_off(rw, 2 * q4)) =
+                  make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xFFFFu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+              *reinterpret_cast<uint4*>(cp + sw_off(rw, 2 * q4 + 1)) =
+                  make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z & 0xFFFFu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.w & 0xFFFFu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
+            }
+            if ((c & 1) == 1 || c == kChunks - 1) {
+              if (c == kChunks - 1) meta();
+              fence_proxy_async_smem();
+              mbar_arrive(&M.full[grp]);
+            }
+          }
         } else {
-          // load + widen in units of half a chunk (4 of the 8 passes); unit
-          // u+1 is loaded before unit u is stored
+          // bf16 rows: load + widen in units of half a chunk (4 of the 8
+          // passes); unit u+1 is loaded before unit u is stored
+          int rl[8];  // pool rows of this lane's copy passes
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
           constexpr int kUnits = 2 * kChunks;
           uint4 st[2][4];
           auto load = [&](int u, uint4* dst) {
@@ -480,16 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int rw = rl[4 * (u & 1) + i];
-              if (rw < 0) {
-                dst[i] = make_uint4(0, 0, 0, 0);
-              } else if (!p.fp8) {
-                dst[i] = ldg_stream(reinterpret_cast<const uint16_t*>(p.kv) + static_cast<int64_t>(rw) * kDqk +
-                                    c * 64 + pj * 8);
-              } else {
-                const uint2 w =
-                    *reinterpret_cast<const uint2*>(p.kv + static_cast<int64_t>(rw) * kDqk + c * 64 + pj * 8);
-                dst[i] = make_uint4(w.x, w.y, 0, 0);
-              }
+              dst[i] = rw < 0 ? make_uint4(0, 0, 0, 0)
+                              : ldg_stream(reinterpret_cast<const uint16_t*>(p.kv) + static_cast<int64_t>(rw) * kDqk +
+                                           c * 64 + pj * 8);
             }
           };
           load(0, st[0]);
@@ -505,18 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint4 w = st[u & 1][i];
-              uint4 o;
-              if (!p.fp8) {
-                over |= bf16x2_over_f16(w.x) | bf16x2_over_f16(w.y) | bf16x2_over_f16(w.z) | bf16x2_over_f16(w.w);
-                o = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                               bf16x2_to_f16x2(w.w));
-              } else {
-                o = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xFFFFu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
-              }
-              *reinterpret_cast<uint4*>(stage + c * kChunkBytes + sw_off(32 * pw + psub + 4 * (4 * (u & 1) + i), pj)) = o;
+              over |= bf16x2_over_f16(w.x) | bf16x2_over_f16(w.y) | bf16x2_over_f16(w.z) | bf16x2_over_f16(w.w);
+              *reinterpret_cast<uint4*>(stage + c * kChunkBytes + sw_off(32 * pw + psub + 4 * (4 * (u & 1) + i), pj)) =
+                  make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
             }
             if ((u & 3) == 3 || u == kUnits - 1) {
               if (u == kUnits - 1) meta();
