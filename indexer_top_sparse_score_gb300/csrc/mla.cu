@@ -386,6 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return pg * kPage + (key & 63);
       };
+      // the next item's query into L2 while this one runs (H * 1152 bytes,
+      // split evenly over the gather threads)
+      {
+        int nrow;
+        if (next_row(p.n_rows * p.n_parts, k + 1, nrow) > 0) {
+          constexpr uint32_t kQSlice = H * kDqk * 2 / kProducers;
+          static_assert(kQSlice % 16 == 0, "prefetch slices are 16-byte multiples");
+          const uint8_t* nq = reinterpret_cast<const uint8_t*>(p.q + static_cast<size_t>(nrow / p.n_parts) * H * kDqk);
+          prefetch_l2_bulk(nq + tid * kQSlice, kQSlice);
+        }
+      }
       // widen the BF16 query to f16 into the swizzled Q tile
       {
         const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
@@ -767,38 +778,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge of split rows: out = sum_s w_s * o_s with w_s = exp(lse_s - lse) and
 // lse = log sum_s exp(lse_s) (the partial attentions of disjoint key sets,
-// each normalised over its own keys). One CTA per row.
+// each normalised over its own keys). One CTA per (row, group of 8 heads);
+// each thread combines 4 consecutive values of one head with 16-byte loads.
+constexpr int kMergeHeads = 8;
+
 __global__ void __launch_bounds__(256) part_merge_kernel(const float* __restrict__ part_o,
                                                          const float* __restrict__ part_lse, int n_parts,
                                                          int n_heads, uint16_t* __restrict__ out, float* lse) {
-  __shared__ float wgt[kMaxParts][64];
-  const int row = blockIdx.x, tid = threadIdx.x;
+  __shared__ float wgt[kMaxParts][kMergeHeads];
+  const int row = blockIdx.x, h0 = blockIdx.y * kMergeHeads, tid = threadIdx.x;
   const size_t item0 = static_cast<size_t>(row) * n_parts;
-  if (tid < n_heads) {
+  if (tid < kMergeHeads && h0 + tid < n_heads) {
+    const int h = h0 + tid;
     float m = -INFINITY;
-    for (int s = 0; s < n_parts; ++s) m = fmaxf(m, part_lse[(item0 + s) * n_heads + tid]);
+    for (int s = 0; s < n_parts; ++s) m = fmaxf(m, part_lse[(item0 + s) * n_heads + h]);
     float sum = 0.0f;
     float e[kMaxParts];
     for (int s = 0; s < n_parts; ++s) {
-      const float l = part_lse[(item0 + s) * n_heads + tid];
+      const float l = part_lse[(item0 + s) * n_heads + h];
       e[s] = (m == -INFINITY || l == -INFINITY) ? 0.0f : __expf(l - m);
       sum += e[s];
     }
     for (int s = 0; s < n_parts; ++s) wgt[s][tid] = sum > 0.0f ? e[s] / sum : 0.0f;
-    if (lse) lse[static_cast<size_t>(row) * n_heads + tid] = sum > 0.0f ? m + __logf(sum) : -INFINITY;
+    if (lse) lse[static_cast<size_t>(row) * n_heads + h] = sum > 0.0f ? m + __logf(sum) : -INFINITY;
   }
   __syncthreads();
-  for (int i = tid; i < n_heads * kDv / 2; i += 256) {
-    const int h = i / (kDv / 2), d = 2 * (i - h * (kDv / 2));
-    float v0 = 0.0f, v1 = 0.0f;
+  // 8 heads x 512 values = 1024 float4 per CTA: 4 per thread
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = tid + u * 256;
+    const int hl = i >> 7, d = (i & 127) * 4;
+    const int h = h0 + hl;
+    if (h >= n_heads) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < n_parts; ++s) {
-      const float ws = wgt[s][h];
+      const float ws = wgt[s][hl];
       if (ws == 0.0f) continue;  // empty part: its output was never written
-      const float2 o = *reinterpret_cast<const float2*>(part_o + ((item0 + s) * n_heads + h) * kDv + d);
-      v0 = fmaf(ws, o.x, v0);
-      v1 = fmaf(ws, o.y, v1);
+      const float4 o = __ldg(reinterpret_cast<const float4*>(part_o + ((item0 + s) * n_heads + h) * kDv + d));
+      acc.x = fmaf(ws, o.x, acc.x);
+      acc.y = fmaf(ws, o.y, acc.y);
+      acc.z = fmaf(ws, o.z, acc.z);
+      acc.w = fmaf(ws, o.w, acc.w);
     }
-    *reinterpret_cast<uint32_t*>(out + (static_cast<size_t>(row) * n_heads + h) * kDv + d) = pack_bf16(v0, v1);
+    *reinterpret_cast<uint2*>(out + (static_cast<size_t>(row) * n_heads + h) * kDv + d) =
+        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
   }
 }
 
@@ -815,8 +838,8 @@ int launch_t(const MlaLaunch& L, const MlaParams& prm) {
   mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   if (prm.n_parts > 1) {
-    part_merge_kernel<<<prm.n_rows, 256, 0, L.stream>>>(prm.part_o, prm.part_lse, prm.n_parts, H, prm.out,
-                                                        prm.lse);
+    part_merge_kernel<<<dim3(prm.n_rows, (H + kMergeHeads - 1) / kMergeHeads), 256, 0, L.stream>>>(
+        prm.part_o, prm.part_lse, prm.n_parts, H, prm.out, prm.lse);
     if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   }
   return SMLA_OK;
