@@ -9,12 +9,13 @@
 //
 // One CTA per SM (persistent). A work item is TQ query rows against a key
 // range, streamed in tiles of 128 keys:
-//   warp 0      TMA producer: q_I tile once per item, k_I tiles (two 64-row
-//               pages each, page table resolved here) into a 4-stage ring;
-//   warp 1      MMA issuer: D[128 keys x (TQ*H_I)] = k_I_tile . q_I^T with
-//               tcgen05 (kind::f8f6f4 for e4m3, kind::f16 for bf16), fp32
-//               accumulators double-buffered in TMEM;
-//   warp 2      TMEM allocator;
+//   warps 0, 3  TMA producers, taking the tiles in turn: k_I tiles (two
+//               64-row pages each, page table resolved here) into a ring of
+//               stages; warp 0 also loads the q_I tile once per item;
+//   warps 1-2   MMA issuers, taking the tiles in turn: D[128 keys x (TQ*H_I)]
+//               = k_I_tile . q_I^T with tcgen05 (kind::f8f6f4 for e4m3,
+//               kind::f16 for bf16), fp32 accumulators in a ring of up to
+//               four TMEM buffers (warp 2 also allocates TMEM);
 //   warps 4-11  two epilogue warpgroups; each thread owns one key (TMEM lane)
 //               and computes the ReLU + head-weighted sum in registers, then
 //               streams the keys that beat the token's threshold into a
@@ -39,13 +40,18 @@ namespace smla {
 namespace {
 
 constexpr int kStages = 4;         // key-tile ring in group mode (the candidate buffers need the rest)
-constexpr int kSplitStages = 12;   // split mode keeps no candidates: 8 more stages in their space
+constexpr int kSplitStages = 10;   // split mode keeps no candidates: 6 more stages and a second
+                                   // query tile in their space
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
 constexpr int kMaxAcc = 4;                            // TMEM accumulator buffers at most
+constexpr int kIssuers = 2;                           // MMA issuer warps
+static_assert(kStages % kIssuers == 0 && kSplitStages % kIssuers == 0 && kMaxAcc % kIssuers == 0,
+              "each ring barrier belongs to one issuer");
+static_assert(kStages % 2 == 0 && kSplitStages % 2 == 0, "each stage belongs to one of the two producers");
 
 struct IdxParams {
   const float* k_scale;  // [pool rows] or null
@@ -97,10 +103,16 @@ __device__ __forceinline__ int tile_at(const Item& it, int tt) {
 // The k-th item of this CTA. Returns -1 when the CTA has no more items, 0 for
 // an empty slot (skip), 1 for a real item. Every role calls this with the
 // same k sequence, so all roles agree on the schedule.
-// kMaxPrefix: split mode enumerates only the non-empty (sequence, key block)
-// items through a per-CTA prefix sum of the sequences' block counts held in
-// the (otherwise unused) histogram scratch, for up to this many sequences.
+// Split mode, for up to kMaxPrefixSeqs sequences: the sequences' key tiles are
+// laid end to end (a per-CTA prefix sum of the tile counts, held in the
+// otherwise unused histogram scratch) and CTA b takes the b-th of gridDim.x
+// equal contiguous ranges; its k-th item is the k-th sequence piece of that
+// range. More sequences fall back to fixed blocks of kKeyBlock keys.
 constexpr int kMaxPrefixSeqs = 1535;
+
+__device__ __forceinline__ int split_len(const IdxParams& p, int seq) {
+  return min(p.seq_lens[seq], static_cast<int>(p.score_stride));  // keys with a score slot
+}
 
 __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, const uint32_t* pref) {
   if (!p.split) {
@@ -123,33 +135,40 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, co
     it.kb = 0;
     it.trivial = it.key_hi <= p.topk && p.out_scores == nullptr;
   } else {
-    const int i = blockIdx.x + k * gridDim.x;
-    int seq, kb;
+    int seq;
     if (pref) {
-      // i-th non-empty item: the sequence whose block range holds i
-      if (i >= static_cast<int>(pref[p.n_seqs])) return -1;
-      int lo = 0, hi = p.n_seqs - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int>(pref[mid]) <= i) lo = mid;
-        else hi = mid - 1;
+      const uint32_t total = pref[p.n_seqs];
+      const uint32_t lo = static_cast<uint32_t>(static_cast<uint64_t>(total) * blockIdx.x / gridDim.x);
+      const uint32_t hi = static_cast<uint32_t>(static_cast<uint64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+      if (lo >= hi) return -1;
+      int a = 0, b = p.n_seqs - 1;  // the last sequence starting at or before tile lo
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (pref[mid] <= lo) a = mid;
+        else b = mid - 1;
       }
-      seq = lo;
-      kb = i - static_cast<int>(pref[seq]);
+      seq = a + k;
+      if (seq >= p.n_seqs || pref[seq] >= hi) return -1;
+      const uint32_t s0 = max(lo, pref[seq]), s1 = min(hi, pref[seq + 1]);
+      if (s1 <= s0) return 0;
+      it.key_lo = static_cast<int>(s0 - pref[seq]) * kTileKeys;
+      it.key_hi = min(split_len(p, seq), static_cast<int>(s1 - pref[seq]) * kTileKeys);
+      it.kb = 0;
     } else {
+      const int i = blockIdx.x + k * gridDim.x;
       if (i >= p.n_items) return -1;
       seq = i / p.n_kblocks;
-      kb = i - seq * p.n_kblocks;
+      const int kb = i - seq * p.n_kblocks;
+      const int L = split_len(p, seq);
+      if (kb * kKeyBlock >= L) return 0;
+      it.key_lo = kb * kKeyBlock;
+      it.key_hi = min(L, it.key_lo + kKeyBlock);
+      it.kb = kb;
     }
-    const int L = p.seq_lens[seq];
-    if (kb * kKeyBlock >= L) return 0;
     it.seq = seq;
     it.row0 = seq * p.q_per_seq;
     it.nrows = p.q_per_seq;
-    it.pos0 = L - p.q_per_seq;
-    it.key_lo = kb * kKeyBlock;
-    it.key_hi = min(L, it.key_lo + kKeyBlock);
-    it.kb = kb;
+    it.pos0 = p.seq_lens[seq] - p.q_per_seq;
     it.trivial = false;
   }
   if (it.key_hi <= it.key_lo) return 0;
@@ -214,7 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty_bar = [&](int st) {
     return st < kStages ? bars + kStages + st : ring_x + (kSplitStages - kStages) + (st - kStages);
   };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_x + 2 * (kSplitStages - kStages));
+  // query-tile barriers: buffer 0 as above, buffer 1 (split mode) after the ring
+  uint64_t* qb_x = ring_x + 2 * (kSplitStages - kStages);  // [full, empty] of query buffer 1
+  auto q_full = [&](int qb) { return qb == 0 ? b_full : qb_x; };
+  auto q_empty = [&](int qb) { return qb == 0 ? b_empty : qb_x + 1; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qb_x + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -231,7 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : static_cast<uint32_t>(kStages * kStageBytes + kMaxN * kIdxRowBytes +
                                                 (st - kStages) * kStageBytes);
   };
-  static_assert((kSplitStages - kStages) * kStageBytes <= 2 * kBufEntries * 4, "split stages fit");
+  static_assert((kSplitStages - kStages + 1) * kStageBytes <= 2 * kBufEntries * 4, "split stages and query tile fit");
+  static_assert(kMaxN * kIdxRowBytes <= kStageBytes, "a query tile fits a stage slot");
+  // query tile buffers: split mode alternates two (the next item's tile loads
+  // while the current one is in use), group mode uses the first
+  auto q_tile = [&](int qb) { return qb == 0 ? b_tile : smem + stage_off(kSplitStages); };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSplitStages; ++i) {
       mbar_init(full_bar(i), 1);
@@ -239,10 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiThreads / 32);
+      mbar_init(&acc_empty[i], SPLIT ? 4 : kEpiThreads / 32);  // split: one warpgroup per buffer
     }
     mbar_init(b_full, 1);
-    mbar_init(b_empty, 1);
+    mbar_init(b_empty, kIssuers);
+    mbar_init(q_full(1), 1);
+    mbar_init(q_empty(1), kIssuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -258,13 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc = 0;
         for (int b = 0; b < p.n_seqs; ++b) {
           hist[b] = acc;
-          const int L = min(p.seq_lens[b], p.n_kblocks * kKeyBlock);
-          acc += static_cast<uint32_t>(max(0, (L + kKeyBlock - 1) / kKeyBlock));
+          const int L = split_len(p, b);
+          acc += static_cast<uint32_t>(max(0, (L + kTileKeys - 1) / kTileKeys));
         }
         hist[p.n_seqs] = acc;
       }
       pref = hist;
     }
+    if (threadIdx.x == 0)
+      for (int b = 0; b < p.n_seqs; ++b)
+        if (p.seq_lens[b] > p.score_stride) set_status(p.status, kStatusBounds);  // keys past the score row skipped
   }
   tc_fence_before();
   __syncthreads();
@@ -272,11 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   volatile int* abort_v = abort_flag;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // The whole warp walks the items; each lane fetches one page id of the
-    // next 32 pages (16 tiles) so page-table latency is paid once per 16
-    // tiles, and lane 0 issues the copies.
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // Two producer warps take the key tiles in turn (tile counter parity);
+    // the stage counts are even, so each stage's barriers belong to one
+    // producer, which waits on their phases in order. Warp 0 also loads the
+    // query tile of every item. In each warp every lane fetches one page id
+    // of the warp's next 16 tiles (32 pages), so page-table latency is paid
+    // once per 16 tiles, and lane 0 issues the copies.
+    const int pw = warp == 0 ? 0 : 1;
     if (lane == 0) {
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_q);
@@ -288,32 +324,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = next_item(p, k, it, pref);
       if (r < 0) break;
       if (r == 0 || it.trivial) continue;
-      if (lane == 0) {
-        ok = mbar_wait(b_empty, (bi & 1) ^ 1, abort_v, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(b_full, N * kIdxRowBytes);
-          tma_load_2d(b_tile, &map_q, b_full, 0, it.row0 * HI);
+      if (pw == 0) {
+        if (lane == 0) {
+          const int qb = SPLIT ? static_cast<int>(bi & 1) : 0;
+          const uint32_t use = SPLIT ? bi >> 1 : bi;  // earlier uses of this buffer
+          ok = mbar_wait(q_empty(qb), (use & 1) ^ 1, abort_v, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(q_full(qb), N * kIdxRowBytes);
+            tma_load_2d(q_tile(qb), &map_q, q_full(qb), 0, it.row0 * HI);
+          }
         }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        ++bi;
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      ++bi;
       const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
       const int nt = it.t1 - it.t0;
-      for (int tw = 0; tw < nt && ok; tw += 16) {
-        // lane l resolves page l & 1 of the tile streamed at step tw + l / 2
+      const uint32_t sc0 = sc;
+      for (int tw = (pw - static_cast<int>(sc0 & 1u) + 2) & 1; tw < nt && ok; tw += 32) {
+        // lane l resolves page l & 1 of the tile streamed at step tw + 2 * (l / 2)
         int pg = 0;
-        if (tw + (lane >> 1) < nt) {
-          const int lp = 2 * tile_at(it, tw + (lane >> 1)) + (lane & 1);
+        if (tw + 2 * (lane >> 1) < nt) {
+          const int lp = 2 * tile_at(it, tw + 2 * (lane >> 1)) + (lane & 1);
           pg = lp * kPage < it.key_hi ? page_of(p, pt, lp) : 0;
         }
-        const int tend = min(tw + 16, nt);
-        for (int tt = tw; tt < tend; ++tt, ++sc) {
-          const int pg0 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (tt - tw));
-          const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, 2 * (tt - tw) + 1);
-          const int t = tile_at(it, tt);
+        const int tend = min(tw + 32, nt);
+        for (int tt = tw; tt < tend; tt += 2) {
+          const int pg0 = __shfl_sync(0xFFFFFFFFu, pg, tt - tw);
+          const int pg1 = __shfl_sync(0xFFFFFFFFu, pg, tt - tw + 1);
           if (lane == 0) {
-            const int s = sc % nst;
-            ok = mbar_wait(empty_bar(s), ((sc / nst) & 1) ^ 1, abort_v, p.status);
+            const uint32_t g = sc0 + tt;
+            const int t = tile_at(it, tt);
+            const int s = g % nst;
+            ok = mbar_wait(empty_bar(s), ((g / nst) & 1) ^ 1, abort_v, p.status);
             if (ok) {
               const bool has1 = (2 * t + 1) * kPage < it.key_hi;
               mbar_arrive_expect_tx(full_bar(s), has1 ? kStageBytes : kStageBytes / 2);
@@ -326,47 +368,69 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
       }
+      sc = sc0 + nt;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = p.is_bf16 ? instr_desc(128, N, kFmtBF16, kFmtBF16, false, false)
-                                       : instr_desc(128, N, kFmtE4M3, kFmtE4M3, false, false);
-      uint32_t sc = 0, bi = 0, ac = 0;
-      const uint64_t a_desc0 = smem_desc(smem_u32(a_tiles), 16, 1024);
-      const uint64_t b_desc0 = smem_desc(smem_u32(b_tile), 16, 1024);
-      for (int k = 0;; ++k) {
-        Item it;
-        const int r = next_item(p, k, it, pref);
-        if (r < 0) break;
-        if (r == 0 || it.trivial) continue;
-        if (!mbar_wait(b_full, bi & 1, abort_v, p.status)) break;
-        ++bi;
-        tc_fence_after();
-        bool ok = true;
-        for (int t = it.t0; t < it.t1; ++t, ++sc, ++ac) {
-          const int s = sc % nst;
-          const int buf = ac & ((1 << p.acc_shift) - 1);
-          if (!mbar_wait_spin(full_bar(s), (sc / nst) & 1, abort_v, p.status) ||
-              !mbar_wait_spin(&acc_empty[buf], ((ac >> p.acc_shift) & 1) ^ 1, abort_v, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage_off(s) >> 4);
-          const uint32_t d = tmem + buf * N;
-#pragma unroll
-          for (int kk = 0; kk < kIdxRowBytes / 32; ++kk) {
-            const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
-            if (p.is_bf16) mma_f16(d, ad + off, b_desc0 + off, idesc, kk > 0);
-            else mma_f8(d, ad + off, b_desc0 + off, idesc, kk > 0);
-          }
-          mma_commit(empty_bar(s));
-          mma_commit(&acc_full[buf]);
+  } else if (warp >= 1 && warp <= kIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    // The tiles go round-robin (CTA tile counter modulo kIssuers) to the
+    // issuer warps. One thread's chain of waits, MMAs and commits pays a long
+    // issue latency per operation; several chains overlap it. All of a tile's
+    // MMAs and commits come from one warp (a commit tracks its own thread's
+    // MMAs), and every issuer releases the query tile once per item.
+    // kIssuers divides the stage count and the accumulator count, so each
+    // stage and accumulator barrier has a single issuer that waits on its
+    // phases in order (a parity wait cannot tell phase n from phase n - 2).
+    const int iw = warp - 1;
+    const uint32_t idesc = p.is_bf16 ? instr_desc(128, N, kFmtBF16, kFmtBF16, false, false)
+                                     : instr_desc(128, N, kFmtE4M3, kFmtE4M3, false, false);
+    // Operands broadcast from lane 0 are warp-uniform to the compiler, which
+    // can then keep the MMA descriptors in uniform registers instead of
+    // re-checking per MMA that every lane holds the same value.
+    uint32_t sc = 0, bi = 0;
+    const uint32_t tmem_u = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    const uint32_t a_base = __shfl_sync(0xFFFFFFFFu, smem_u32(a_tiles), 0);
+    const uint32_t q_base0 = __shfl_sync(0xFFFFFFFFu, smem_u32(q_tile(0)), 0);
+    const uint32_t q_base1 = __shfl_sync(0xFFFFFFFFu, smem_u32(q_tile(1)), 0);
+    for (int k = 0;; ++k) {
+      Item it;
+      const int r = next_item(p, k, it, pref);
+      if (r < 0) break;
+      if (r == 0 || it.trivial) continue;
+      const int qb = SPLIT ? static_cast<int>(bi & 1) : 0;
+      const uint32_t use = SPLIT ? bi >> 1 : bi;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(q_full(qb), use & 1, abort_v, p.status))) break;
+      ++bi;
+      const uint64_t b_desc0 = smem_desc(qb == 0 ? q_base0 : q_base1, 16, 1024);
+      tc_fence_after();
+      bool ok = true;
+      const uint32_t sc0 = sc;
+      const int nt = it.t1 - it.t0;
+      for (int tt = (iw - static_cast<int>(sc0 % kIssuers) + kIssuers) % kIssuers; tt < nt; tt += kIssuers) {
+        // CTA tile counter: stage ring and accumulator ring position
+        const uint32_t g = __shfl_sync(0xFFFFFFFFu, sc0 + tt, 0);
+        const int s = g % nst;
+        const int buf = g & ((1u << p.acc_shift) - 1);
+        ok = mbar_wait_spin(full_bar(s), (g / nst) & 1, abort_v, p.status) &&
+             mbar_wait_spin(&acc_empty[buf], ((g >> p.acc_shift) & 1) ^ 1, abort_v, p.status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        mma_commit(b_empty);
+        tc_fence_after();
+        const uint64_t ad = smem_desc(a_base + stage_off(s), 16, 1024);
+        const uint32_t d = tmem_u + buf * N;
+#pragma unroll
+        for (int kk = 0; kk < kIdxRowBytes / 32; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+          if (p.is_bf16) mma_f16_warp(d, ad + off, b_desc0 + off, idesc, kk > 0);
+          else mma_f8_warp(d, ad + off, b_desc0 + off, idesc, kk > 0);
+        }
+        mma_commit_warp(empty_bar(s));
+        mma_commit_warp(&acc_full[buf]);
       }
+      if (!ok) break;
+      sc = sc0 + nt;
+      mma_commit_warp(q_empty(qb));
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
@@ -526,89 +590,143 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
       bool ok = true;
-      for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
-        const int t = tile_at(it, tt);
-        const int buf = ac & ((1 << p.acc_shift) - 1);
-        if (!mbar_wait_backoff(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t raw[TPW_MAX * HI];
-#pragma unroll
-        for (int jj = 0; jj < TPW_MAX; ++jj)
-          if (j0 + jj < j1)
-            tmem_ld_heads<HI>(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N + (j0 + jj) * HI,
-                              raw + jj * HI);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-
-        const int s = t * kTileKeys + q * 32 + lane;
-        float ks = 1.0f;
-        if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
-        // ReLU + head-weighted sum with four independent partial sums per token
-        // (weights read as float4 broadcasts), then the admission test
-        uint32_t key[TPW_MAX], m[TPW_MAX];
-        bool adm[TPW_MAX];
-#pragma unroll
-        for (int jj = 0; jj < TPW_MAX; ++jj) {
-          const int j = j0 + jj;
-          adm[jj] = false;
-          key[jj] = 0;
-          if (j < j1) {
-            const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
-            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-            for (int h = 0; h < HI; h += 4) {
-              const float4 wv = w4[h >> 2];
-              a0 = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a0);
-              a1 = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a1);
-              a2 = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a2);
-              a3 = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a3);
-            }
-            key[jj] = score_key(((a0 + a1) + (a2 + a3)) * ks);
-            const bool valid = j < it.nrows && s >= it.key_lo && s < it.key_hi && s <= it.pos0 + j;
-            adm[jj] = valid && key[jj] > theta[j];
+      if constexpr (SPLIT) {
+        // decode: the two warpgroups take the tiles in turn (each accumulator
+        // buffer belongs to one warpgroup) and each covers every query row of
+        // its tile, TPW_MAX rows per pass; every score goes to the row's
+        // score array, and select_kernel takes the exact top-k afterwards
+        const uint32_t ac0 = ac;
+        const int nt = it.t1 - it.t0;
+        for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt; tt += 2) {
+          const uint32_t g = ac0 + tt;
+          const int t = tile_at(it, tt);
+          const int buf = g & ((1u << p.acc_shift) - 1);
+          if (!mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status)) {
+            ok = false;
+            break;
           }
-          m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
+          tc_fence_after();
+          const int s = t * kTileKeys + q * 32 + lane;
+          float ks = 1.0f;
+          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          for (int jb = 0; jb < p.tq; jb += TPW_MAX) {
+            uint32_t raw[TPW_MAX * HI];
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj)
+              if (jb + jj < p.tq)
+                tmem_ld_heads<HI>(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N + (jb + jj) * HI,
+                                  raw + jj * HI);
+            tmem_wait_ld();
+            if (jb + TPW_MAX >= p.tq) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj) {
+              const int j = jb + jj;
+              if (j < it.nrows && s < it.key_hi && s <= it.pos0 + j) {
+                const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+                for (int h = 0; h < HI; h += 4) {
+                  const float4 wv = w4[h >> 2];
+                  a0 = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a0);
+                  a1 = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a1);
+                  a2 = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a2);
+                  a3 = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a3);
+                }
+                p.scores[static_cast<int64_t>(it.row0 + j) * p.score_stride + s] =
+                    score_key(((a0 + a1) + (a2 + a3)) * ks);
+              }
+            }
+          }
         }
-        if constexpr (SPLIT) {
-          // decode: every score goes to the row's score array; select_kernel
-          // takes the exact top-k of each row afterwards
+        ac = ac0 + nt;
+        if (!ok) break;
+      } else {
+        // prefill: both warpgroups take every tile, each for its own query rows
+        for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
+          const int t = tile_at(it, tt);
+          const int buf = ac & ((1 << p.acc_shift) - 1);
+          if (!mbar_wait_backoff(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t raw[TPW_MAX * HI];
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj)
+            if (j0 + jj < j1)
+              tmem_ld_heads<HI>(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N + (j0 + jj) * HI,
+                                raw + jj * HI);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+
+          const int s = t * kTileKeys + q * 32 + lane;
+          float ks = 1.0f;
+          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          // ReLU + head-weighted sum with four independent partial sums per token
+          // (weights read as float4 broadcasts), then the admission test
+          uint32_t key[TPW_MAX], m[TPW_MAX];
+          bool adm[TPW_MAX];
 #pragma unroll
           for (int jj = 0; jj < TPW_MAX; ++jj) {
             const int j = j0 + jj;
-            if (j < j1 && j < it.nrows && s < it.key_hi && s <= it.pos0 + j)
-              p.scores[static_cast<int64_t>(it.row0 + j) * p.score_stride + s] = key[jj];
+            adm[jj] = false;
+            key[jj] = 0;
+            if (j < j1) {
+              const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
+              float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+              for (int h = 0; h < HI; h += 4) {
+                const float4 wv = w4[h >> 2];
+                a0 = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a0);
+                a1 = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a1);
+                a2 = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a2);
+                a3 = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a3);
+              }
+              key[jj] = score_key(((a0 + a1) + (a2 + a3)) * ks);
+              const bool valid = j < it.nrows && s >= it.key_lo && s < it.key_hi && s <= it.pos0 + j;
+              adm[jj] = valid && key[jj] > theta[j];
+            }
+            m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
           }
-          continue;
+          // every warp reads the token counts (the last tile's reservations
+          // are done), and only then may any warp reserve again: a warp that
+          // read a count after another's reservation could take a different
+          // branch and miss the selection's barriers
+          wg_sync();
+          bool over[TPW_MAX];
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj) over[jj] = j0 + jj < j1 && cnt[j0 + jj] > cap - kTileKeys;
+          wg_sync();
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj)
+            if (over[jj]) select_token(j0 + jj, topk, false, it);
+          // one reservation per warp and token; both issued before either is used
+          int base[TPW_MAX];
+          if (lane == 0) {
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj) base[jj] = m[jj] ? atomicAdd(&cnt[j0 + jj], __popc(m[jj])) : 0;
+          }
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj) {
+            base[jj] = __shfl_sync(0xFFFFFFFFu, base[jj], 0);
+            if (adm[jj]) {
+              const int j = j0 + jj;
+              const int pos = base[jj] + __popc(m[jj] & lanemask_lt);
+              ckey[j * cap + pos] = key[jj];
+              cidx[j * cap + pos] = static_cast<uint32_t>(s);
+            }
+          }
         }
+        if (!ok) break;
         wg_sync();
-        for (int j = j0; j < j1; ++j)
-          if (cnt[j] > cap - kTileKeys) select_token(j, topk, false, it);
-        // one reservation per warp and token; both issued before either is used
-        int base[TPW_MAX];
-        if (lane == 0) {
-#pragma unroll
-          for (int jj = 0; jj < TPW_MAX; ++jj) base[jj] = m[jj] ? atomicAdd(&cnt[j0 + jj], __popc(m[jj])) : 0;
-        }
-#pragma unroll
-        for (int jj = 0; jj < TPW_MAX; ++jj) {
-          base[jj] = __shfl_sync(0xFFFFFFFFu, base[jj], 0);
-          if (adm[jj]) {
-            const int j = j0 + jj;
-            const int pos = base[jj] + __popc(m[jj] & lanemask_lt);
-            ckey[j * cap + pos] = key[jj];
-            cidx[j * cap + pos] = static_cast<uint32_t>(s);
-          }
-        }
+        for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
       }
-      if (!ok) break;
-      if constexpr (SPLIT) continue;
-      wg_sync();
-      for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
     }
   }
 
@@ -639,7 +757,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int seq = row / p.q_per_seq;
   const int pos = p.seq_lens[seq] - p.q_per_seq + (row - seq * p.q_per_seq);
-  const int n = pos + 1;  // keys 0..pos
+  const int n = min(pos + 1, static_cast<int>(p.score_stride));  // keys 0..pos (with a score slot)
   const uint32_t* keys = p.scores + static_cast<int64_t>(row) * p.score_stride;
   int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
   float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
@@ -795,7 +913,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 2) * 8 + 16;
+                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -803,7 +921,11 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
       return SMLA_ERR_CUDA;
     attr_done = true;
   }
-  const int grid_items = prm.split ? prm.n_items : (prm.n_items + 1) / 2;
+  // split mode with the balanced tile ranges: up to one CTA per key tile
+  const int64_t split_tiles = static_cast<int64_t>(prm.n_seqs) * ((prm.score_stride + kTileKeys - 1) / kTileKeys);
+  const int grid_items = !prm.split ? (prm.n_items + 1) / 2
+                         : prm.n_seqs <= kMaxPrefixSeqs ? static_cast<int>(std::min<int64_t>(split_tiles, 1 << 30))
+                                                        : prm.n_items;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
   indexer_kernel<HI, SPLIT><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
@@ -874,6 +996,7 @@ int launch_indexer(const IndexerLaunch& L) {
   // as many accumulator buffers as fit in TMEM's 512 columns (at most 4)
   prm.acc_shift = 0;
   while (prm.acc_shift < 2 && (N << (prm.acc_shift + 1)) <= 512) ++prm.acc_shift;
+  if ((1 << prm.acc_shift) % kIssuers != 0) return SMLA_ERR_UNSUPPORTED;  // N <= 128 always gives 4 buffers
   int cols = 32;
   while (cols < (N << prm.acc_shift)) cols <<= 1;
   prm.tmem_cols = cols;
