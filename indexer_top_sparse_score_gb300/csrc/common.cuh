@@ -286,46 +286,51 @@ __device__ __forceinline__ void wg_select(const uint32_t* keys, const uint32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Exact top-k threshold over a dense score array: entry e has key keys[e] and
-// index e, for e in [0, n) (n > k >= 1). NT cooperating threads (a multiple of
-// 128) synchronised by `sync()`; `hist` = 3 x 256 words and `red` =
-// 2 * NT / 32 words of shared scratch; keys must be 16-byte aligned. Returns
-// (thr_key, thr_idx) with the meaning of wg_select. Same method as wg_select
-// (range-adaptive radix passes over the keys, then over the tied indices),
-// reading the keys straight from (global) memory, four per 16-byte load.
+// Exact top-k threshold over an array of entries: entry e has key keys[e] and
+// index idxs[e] (or e when idxs is null), for e in [0, n) (n > k >= 1). NT
+// cooperating threads (a multiple of 128) synchronised by `sync()`; `hist` =
+// 3 x 256 words and `red` = 2 * NT / 32 words of shared scratch; keys (and
+// idxs) must be 16-byte aligned. Returns (thr_key, thr_idx) with the meaning
+// of wg_select. Same method as wg_select (range-adaptive radix passes over the
+// keys, then over the tied indices), reading the entries straight from
+// (global or shared) memory, four per 16-byte load.
 template <int NT, typename Sync>
-__device__ __forceinline__ void dense_select(const uint32_t* keys, int n, int k, int tid, uint32_t* hist,
-                                             uint32_t* red, Sync sync, uint32_t& thr_key, uint32_t& thr_idx) {
+__device__ __forceinline__ void dense_select(const uint32_t* keys, const uint32_t* idxs, int n, int k, int tid,
+                                             uint32_t* hist, uint32_t* red, Sync sync, uint32_t& thr_key,
+                                             uint32_t& thr_idx) {
   constexpr int NW = NT / 32;
   const int lane = tid & 31, w = tid >> 5;
   int hb = 0;
-  // f(key, index) for every entry of this thread (4 consecutive per load,
-  // four loads in flight per thread)
+  // f(key, index, valid) for every entry of this thread (4 consecutive per
+  // load, four loads in flight per thread); the index is idxs[e] when idxs is
+  // given, else the position e
   auto each4 = [&](auto f) {
     constexpr int U = 4;
     for (int b0 = tid * 4; b0 < n; b0 += 4 * NT * U) {
-      uint4 kv[U];
+      uint4 kv[U], iv[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int e0 = b0 + u * 4 * NT;
         kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+        iv[u] = make_uint4(e0, e0 + 1, e0 + 2, e0 + 3);
+        if (idxs && e0 < n) iv[u] = *reinterpret_cast<const uint4*>(idxs + e0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int e0 = b0 + u * 4 * NT;
-        f(kv[u].x, e0 + 0, e0 + 0 < n);
-        f(kv[u].y, e0 + 1, e0 + 1 < n);
-        f(kv[u].z, e0 + 2, e0 + 2 < n);
-        f(kv[u].w, e0 + 3, e0 + 3 < n);
+        f(kv[u].x, iv[u].x, e0 + 0 < n);
+        f(kv[u].y, iv[u].y, e0 + 1 < n);
+        f(kv[u].z, iv[u].z, e0 + 2 < n);
+        f(kv[u].w, iv[u].w, e0 + 3 < n);
       }
     }
   };
   auto minmax = [&](bool ties, uint32_t tk, uint32_t& lo, uint32_t& hi) {
     for (int b = tid; b < 256; b += NT) hist[256 * hb + b] = 0;
     uint32_t a = 0xFFFFFFFFu, bmax = 0;
-    each4([&](uint32_t kk, int e, bool ok) {
+    each4([&](uint32_t kk, uint32_t e, bool ok) {
       if (!ok || (ties && kk != tk)) return;
-      const uint32_t v = ties ? static_cast<uint32_t>(e) : kk;
+      const uint32_t v = ties ? e : kk;
       a = min(a, v);
       bmax = max(bmax, v);
     });
@@ -351,9 +356,9 @@ __device__ __forceinline__ void dense_select(const uint32_t* keys, int n, int k,
       uint32_t* h = hist + 256 * hb;
       uint32_t* hn = hist + 256 * ((hb + 1) % 3);
       for (int b = tid; b < 256; b += NT) hn[b] = 0;
-      each4([&](uint32_t kk, int e, bool ok) {
+      each4([&](uint32_t kk, uint32_t e, bool ok) {
         if (!ok) return;
-        const uint32_t v = ties ? static_cast<uint32_t>(e) : kk;
+        const uint32_t v = ties ? e : kk;
         if ((ties && kk != tk) || v < lo || v > hi) return;
         atomicAdd(&h[(v - lo) >> shift], 1u);
       });

@@ -736,9 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Split mode (decode), step 2: the exact top-k of one row's dense score array
-// (written by the scoring kernel for keys 0..pos). One CTA of 1024 threads
-// per row; scores are read from global memory (they stay in L2).
+// Parameters of select_kernel (split mode, step 2).
 struct SelectParams {
   const uint32_t* scores;
   int64_t score_stride;
@@ -749,11 +747,96 @@ struct SelectParams {
 };
 
 constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelShift = 20;                  // first radix digit: key bits 31..20
+constexpr int kSelBins = 1 << (32 - kSelShift);
+constexpr int kSelCand = 8192;                 // first-digit bin entries held in shared memory
+constexpr int kSelTies = 1024;                 // equal keys ranked by index in shared memory
+constexpr int kSelBmBits = 1 << 18;            // rows up to this many keys mark their selection in a bitmap
 
+// shared memory of select_kernel (dynamic)
+struct SelSmem {
+  uint32_t hist[kSelBins];
+  uint32_t bm[kSelBmBits / 32];  // selected positions of the row
+  uint32_t cand_key[kSelCand], cand_idx[kSelCand];
+  uint32_t tie[kSelTies];
+  uint32_t hist3[768];
+  uint32_t red[2 * kSelWarps];
+  uint32_t wsum[kSelWarps];
+  uint32_t n_cand, bin, above, thr_idx;
+};
+
+// Every entry of the row, a warp-uniform number of times per warp: warp w
+// takes 128-entry segments (lane l entries 4l..4l+3, one bitmap word per 8
+// lanes), four segments in flight. f(k4, e0) gets the lane's four keys.
+template <typename F>
+__device__ __forceinline__ void sel_each(const uint32_t* keys, int n, int w, int lane, F f) {
+  constexpr int U = 4;
+  for (int s0 = w * 128; s0 < n; s0 += U * kSelThreads * 4) {
+    uint4 kv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e0 = s0 + u * kSelThreads * 4 + 4 * lane;
+      kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) f(kv[u], s0 + u * kSelThreads * 4 + 4 * lane);
+  }
+}
+
+// Top-down scan of a histogram of nbins (a multiple of kSelThreads or at most
+// kSelThreads) bins: the bin holding the k-th largest entry and the number of
+// entries in higher bins, left in S.bin / S.above. All threads call it.
+__device__ __forceinline__ void sel_top_scan(SelSmem& S, const uint32_t* hist, int nbins, uint32_t k, int tid) {
+  const int lane = tid & 31, w = tid >> 5;
+  const int per = nbins >= kSelThreads ? nbins / kSelThreads : 1;
+  uint32_t c[4] = {0, 0, 0, 0}, sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = per * tid + i;
+    if (i < per && j < nbins) c[i] = hist[nbins - 1 - j];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) S.wsum[w] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum;
+  for (int w2 = 0; w2 < w; ++w2) run += S.wsum[w2];
+  if (run < k && run + sum >= k) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (run + c[i] >= k) {
+        S.bin = static_cast<uint32_t>(nbins - 1 - (per * tid + i));
+        S.above = run;
+        break;
+      }
+      run += c[i];
+    }
+  }
+  __syncthreads();
+}
+
+// Split mode (decode), step 2: the exact top-k of one row's dense score array
+// (written by the scoring kernel for keys 0..pos). One CTA of 1024 threads per
+// row; scores are read from global memory (they stay in L2).
+//  1. histogram of the top 12 key bits: the bin B holding the k-th best key
+//     splits the row into entries sure to be selected (higher bins),
+//     candidates (bin B) and the rest;
+//  2. one pass marks the sure entries in a bitmap of the row's positions and
+//     stages the candidates (key, index) in shared memory;
+//  3. two more digits (bits 19..8, 7..0) over the candidates give the exact
+//     k-th key; among equal keys the lower indices win, ranked by counting;
+//  4. the bitmap is written out as the ascending list of selected positions.
+// Rows too long for the bitmap, or whose bin B is too crowded to stage, take
+// the exact radix selection over the whole row instead (dense_select).
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
-  __shared__ uint32_t hist[768];
-  __shared__ uint32_t red[2 * kSelThreads / 32];
-  __shared__ uint32_t wsum[kSelThreads / 32];
+  extern __shared__ __align__(16) uint8_t sel_raw[];
+  SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int seq = row / p.q_per_seq;
   const int pos = p.seq_lens[seq] - p.q_per_seq + (row - seq * p.q_per_seq);
@@ -761,66 +844,216 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const uint32_t* keys = p.scores + static_cast<int64_t>(row) * p.score_stride;
   int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
   float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
+  const int k = p.topk;
+  if (n <= k) {
+    // every key is selected: 0..n-1 in order, then -1
+    for (int e = tid; e < k; e += kSelThreads) {
+      o[e] = e < n ? e : -1;
+      if (os) os[e] = e < n ? key_score(keys[e]) : 0.0f;
+    }
+    return;
+  }
   auto sync = []() { __syncthreads(); };
-  uint32_t tk = 0, ti = 0xFFFFFFFFu;
-  const bool all = n <= p.topk;
-  if (n > 0 && !all) dense_select<kSelThreads>(keys, n, p.topk, tid, hist, red, sync, tk, ti);
-  // output in a fixed order: warp w takes the 128-entry segments w, w + 32, ...
-  // (lane l holds entries 4l..4l+3 of a segment); pass 1 counts each warp's
-  // selected entries, pass 2 writes them after the earlier warps' ones
-  constexpr int kW = kSelThreads / 32;
-  const int nseg = (n + 127) / 128;
-  auto seg_take = [&](int sg, uint32_t (&kk)[4], bool (&tk4)[4]) {
-    const int e0 = sg * 128 + 4 * lane;
-    const uint4 v = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
-    kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
+  const bool use_bm = n <= kSelBmBits;
+  // 1. first-digit histogram
+  for (int b = tid; b < kSelBins; b += kSelThreads) S.hist[b] = 0;
+  if (use_bm)
+    for (int b = tid; b < (n + 31) / 32; b += kSelThreads) S.bm[b] = 0;
+  if (tid == 0) S.n_cand = 0;
+  __syncthreads();
+  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
+    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      tk4[q] = e0 + q < n && (all || selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti));
-  };
-  int mine = 0;
-  for (int sg = w; sg < nseg; sg += kW) {
-    uint32_t kk[4];
-    bool tk4[4];
-    seg_take(sg, kk, tk4);
-    mine += tk4[0] + tk4[1] + tk4[2] + tk4[3];
-  }
-  mine = __reduce_add_sync(0xFFFFFFFFu, mine);
-  if (lane == 0) wsum[w] = mine;
+      if (e0 + q < n) atomicAdd(&S.hist[kk[q] >> kSelShift], 1u);
+  });
   __syncthreads();
-  int base = 0, total = 0;
-  for (int w2 = 0; w2 < kW; ++w2) {
-    const int v = static_cast<int>(wsum[w2]);
-    if (w2 < w) base += v;
-    total += v;
-  }
-  for (int sg = w; sg < nseg; sg += kW) {
-    uint32_t kk[4];
-    bool tk4[4];
-    seg_take(sg, kk, tk4);
-    const int c = tk4[0] + tk4[1] + tk4[2] + tk4[3];
-    int incl = c;
+  sel_top_scan(S, S.hist, kSelBins, static_cast<uint32_t>(k), tid);
+  const uint32_t b1 = S.bin;
+  const uint32_t n_b1 = S.hist[b1];
+  const int r1 = k - static_cast<int>(S.above);  // rank (1-based) of the k-th best inside bin b1
+  int r = r1;
+  uint32_t tk = 0, ti = 0xFFFFFFFFu;
+  bool staged = use_bm && n_b1 <= static_cast<uint32_t>(kSelCand);
+  if (staged) {
+    // 2. sure entries into the bitmap (each word belongs to one warp segment),
+    //    candidates into shared memory
+    sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      uint32_t bits = 0, nc = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += t2;
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t b = kk[q] >> kSelShift;
+        if (e0 + q < n) {
+          bits |= (b > b1 ? 1u : 0u) << ((e0 + q) & 31);
+          nc += b == b1;
+        }
+      }
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
+      if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
+      if (__ballot_sync(0xFFFFFFFFu, nc != 0)) {
+        uint32_t incl = nc;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += t2;
+        }
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&S.n_cand, incl);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - nc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (e0 + q < n && (kk[q] >> kSelShift) == b1) {
+            S.cand_key[base] = kk[q];
+            S.cand_idx[base] = static_cast<uint32_t>(e0 + q);
+            ++base;
+          }
+      }
+    });
+    __syncthreads();
+    // 3. exact k-th key among the candidates: digits 19..8, then 7..0
+    const int nc = static_cast<int>(n_b1);
+    uint32_t prefix = b1 << kSelShift;
+    for (int d = 0; d < 2; ++d) {
+      const int shift = d == 0 ? 8 : 0;
+      const int nb = d == 0 ? 4096 : 256;
+      const uint32_t pmask = d == 0 ? 0xFFF00000u : 0xFFFFFF00u;
+      for (int b = tid; b < nb; b += kSelThreads) S.hist[b] = 0;
+      __syncthreads();
+      for (int e = tid; e < nc; e += kSelThreads) {
+        const uint32_t kk = S.cand_key[e];
+        if ((kk & pmask) == prefix) atomicAdd(&S.hist[(kk >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      sel_top_scan(S, S.hist, nb, static_cast<uint32_t>(r), tid);
+      prefix |= S.bin << shift;
+      r -= static_cast<int>(S.above);
     }
-    int q0 = base + incl - c;
-    const int e0 = sg * 128 + 4 * lane;
+    tk = prefix;
+    const int m = static_cast<int>(S.hist[tk & 255u]);  // entries with key == tk; the r lowest indices win
+    if (r < m) {
+      if (m <= kSelTies) {
+        if (tid == 0) S.n_cand = 0;
+        __syncthreads();
+        for (int e0 = 0; e0 < nc; e0 += kSelThreads) {
+          const int e = e0 + tid;
+          const bool eq = e < nc && S.cand_key[e] == tk;
+          const uint32_t mb = __ballot_sync(0xFFFFFFFFu, eq);
+          uint32_t base = 0;
+          if (mb && lane == 0) base = atomicAdd(&S.n_cand, static_cast<uint32_t>(__popc(mb)));
+          base = __shfl_sync(0xFFFFFFFFu, base, 0);
+          if (eq) S.tie[base + __popc(mb & ((1u << lane) - 1u))] = S.cand_idx[e];
+        }
+        __syncthreads();
+        if (tid < m) {
+          const uint32_t mine = S.tie[tid];
+          int below = 0;
+          for (int j = 0; j < m; ++j) below += S.tie[j] < mine;
+          if (below == r - 1) S.thr_idx = mine;
+        }
+        __syncthreads();
+        ti = S.thr_idx;
+      } else {
+        // many equal keys: exact selection over all candidates (r1 < nc)
+        for (int e = nc + tid; e < (nc + 3) / 4 * 4; e += kSelThreads) S.cand_key[e] = 0;  // 16-byte tail
+        __syncthreads();
+        dense_select<kSelThreads>(S.cand_key, S.cand_idx, nc, r1, tid, S.hist3, S.red, sync, tk, ti);
+      }
+    }
+    for (int e = tid; e < nc; e += kSelThreads) {
+      const uint32_t i = S.cand_idx[e];
+      if (selected(S.cand_key[e], i, tk, ti)) atomicOr(&S.bm[i >> 5], 1u << (i & 31));
+    }
+  } else {
+    // the whole row: exact radix selection from global memory
+    dense_select<kSelThreads>(keys, nullptr, n, k, tid, S.hist3, S.red, sync, tk, ti);
+    if (use_bm)
+      sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
+        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        uint32_t bits = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti)) bits |= 1u << ((e0 + q) & 31);
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
+        if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
+      });
+  }
+  __syncthreads();
+  if (use_bm) {
+    // 4. ascending positions: thread t owns a run of bitmap words
+    const int nw = (n + 31) / 32;
+    const int per = (nw + kSelThreads - 1) / kSelThreads;
+    const int w0 = tid * per, w1 = min(nw, w0 + per);
+    uint32_t cnt = 0;
+    for (int i = w0; i < w1; ++i) cnt += __popc(S.bm[i]);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+      if (lane >= o2) incl += t2;
+    }
+    if (lane == 31) S.wsum[w] = incl;
+    __syncthreads();
+    uint32_t at = incl - cnt;
+    for (int w2 = 0; w2 < w; ++w2) at += S.wsum[w2];
+    for (int i = w0; i < w1; ++i) {
+      uint32_t bits = S.bm[i];
+      while (bits) {
+        const int e = i * 32 + __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (at < static_cast<uint32_t>(k)) {
+          o[at] = e;
+          if (os) os[at] = key_score(keys[e]);
+        }
+        ++at;
+      }
+    }
+    return;
+  }
+  // rows longer than the bitmap: selected entries in a fixed order (warp w
+  // takes the 128-entry segments w, w + 32, ...): count, then write
+  int mine = 0;
+  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
+    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mine += e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti);
+  });
+  mine = __reduce_add_sync(0xFFFFFFFFu, mine);
+  if (lane == 0) S.wsum[w] = mine;
+  __syncthreads();
+  int base = 0;
+  for (int w2 = 0; w2 < w; ++w2) base += static_cast<int>(S.wsum[w2]);
+  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
+    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+    bool t4[4];
+    int c = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if (!tk4[q]) continue;
-      o[q0] = e0 + q;
-      if (os) os[q0] = key_score(kk[q]);
-      ++q0;
+      t4[q] = e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti);
+      c += t4[q];
     }
+    int incl = c;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+      if (lane >= o2) incl += t2;
+    }
+    int q0 = base + incl - c;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (t4[q]) {
+        if (q0 < k) {
+          o[q0] = e0 + q;
+          if (os) os[q0] = key_score(kk[q]);
+        }
+        ++q0;
+      }
     base += __shfl_sync(0xFFFFFFFFu, incl, 31);
-  }
-  base = total;
-  for (int e = base + tid; e < p.topk; e += kSelThreads) {
-    o[e] = -1;
-    if (os) os[e] = 0.0f;
-  }
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -1046,7 +1279,14 @@ int launch_indexer(const IndexerLaunch& L) {
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
   }
   SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.q_per_seq, L.topk, L.out_idx, L.out_scores};
-  select_kernel<<<prm.n_rows, kSelThreads, 0, L.stream>>>(sp);
+  static bool sel_attr = false;
+  if (!sel_attr) {
+    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    sel_attr = true;
+  }
+  select_kernel<<<prm.n_rows, kSelThreads, sizeof(SelSmem), L.stream>>>(sp);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }

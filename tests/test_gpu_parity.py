@@ -226,3 +226,30 @@ def test_indexer_heavy_ties(mode):
     compare_idx(_host(gidx)[rows], ridx)
     if mode == "constant":
         assert (np.sort(_host(gidx)[rows], axis=1) == np.arange(spec.topk)[None, :]).all()
+
+
+@pytest.mark.parametrize("mode", ["constant", "binary"])
+def test_decode_indexer_heavy_ties(mode):
+    """Decode shape (split mode) with ties everywhere, rows from 2.5K to 20K keys:
+    the dense per-row selection must keep the lowest indices among equal scores
+    whether the threshold bin is staged in shared memory or not."""
+    spec = wl.scaled(wl.SPECS["decode"], n_seqs=5, len_min=2500, len_max=20000, seed=91)
+    prob = wl.make(spec, "cpu")
+    k = prob.cache.k_idx
+    if mode == "constant":
+        row = k.view(-1, spec.d_idx)[0].clone()
+        k.view(-1, spec.d_idx)[:] = row
+    else:
+        g = torch.Generator().manual_seed(5)
+        v = torch.randint(0, 2, k.shape, generator=g).to(torch.float32)
+        k.copy_(v.to(torch.float8_e4m3fn).view(torch.uint8))
+    dev = prob.to("cuda")
+    max_len = int(dev.seq_lens.max())
+    gidx, ws = smla.indexer_topk(dev.cache, dev.page_table, dev.seq_lens, max_len, spec.q_per_seq, dev.q_idx,
+                                 dev.w, spec.topk)
+    assert smla.read_status(ws)[0] == 0
+    rows = np.arange(spec.n_seqs * spec.q_per_seq)
+    ridx, *_ = oracle.Oracle(prob).rows(rows, attend=False)
+    compare_idx(_host(gidx), ridx)
+    if mode == "constant":
+        assert (np.sort(_host(gidx), axis=1) == np.arange(spec.topk)[None, :]).all()
