@@ -282,67 +282,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA
     // Per block: QK^T chunk group by chunk group as the groups arrive, then
     // (after the softmax) PV slice by slice, each slice's commit freeing the
-    // chunks it read. The tensor pipe runs them in issue order.
-    if (lane == 0) {
-      const uint32_t idesc_qk = instr_desc(128, H, fmt, fmt, false, false);
-      const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, true);
-      const uint32_t q0 = smem_u32(q_tile), st0 = smem_u32(stage);
-      // K-major operands (rows of 128 bytes, 8-row groups 1024 bytes apart):
-      // the gathered rows (A of QK) and the query (B of QK). MN-major operands:
-      // the same rows read as V^T (A of PV; the two 64-value chunks of a
-      // 128-value slice are one chunk apart) and P^T (B of PV).
-      const uint64_t k_desc = smem_desc(st0, 16, 1024);
-      const uint64_t q_desc = smem_desc(q0, 16, 1024);
-      const uint64_t vt_desc = smem_desc(st0, kChunkBytes, 1024);
-      const uint64_t p_desc = smem_desc(st0 + kPChunk * kChunkBytes, kChunkBytes, 1024);
-      uint32_t g = 0, tok = 0;
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        int row;
-        const int r = next_row(p.n_rows * p.n_parts, k, row);
-        if (r < 0) break;
-        if (r == 0) continue;
-        const RowInfo ri = row_info(p, row);
-        if (ri.nb == 0) continue;
-        if (!mbar_wait(&M.q_full, tok & 1, abort_v, p.status)) break;
-        for (int b = 0; b < ri.nb; ++b, ++g) {
-          const uint32_t ph = g & 1;
+    // chunks it read. The tensor pipe runs them in issue order. The whole warp
+    // runs the loop with warp-uniform operands (broadcast from lane 0) and one
+    // elected lane issues each MMA and commit.
+    const uint32_t idesc_qk = instr_desc(128, H, fmt, fmt, false, false);
+    const uint32_t idesc_pv = instr_desc(128, H, fmt, fmt, true, true);
+    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, smem_u32(q_tile), 0);
+    const uint32_t st0 = __shfl_sync(0xFFFFFFFFu, smem_u32(stage), 0);
+    const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    // K-major operands (rows of 128 bytes, 8-row groups 1024 bytes apart):
+    // the gathered rows (A of QK) and the query (B of QK). MN-major operands:
+    // the same rows read as V^T (A of PV; the two 64-value chunks of a
+    // 128-value slice are one chunk apart) and P^T (B of PV).
+    const uint64_t k_desc = smem_desc(st0, 16, 1024);
+    const uint64_t q_desc = smem_desc(q0, 16, 1024);
+    const uint64_t vt_desc = smem_desc(st0, kChunkBytes, 1024);
+    const uint64_t p_desc = smem_desc(st0 + kPChunk * kChunkBytes, kChunkBytes, 1024);
+    uint32_t g = 0, tok = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int row;
+      const int r = next_row(p.n_rows * p.n_parts, k, row);
+      if (r < 0) break;
+      if (r == 0) continue;
+      const RowInfo ri = row_info(p, row);
+      const int nb = __shfl_sync(0xFFFFFFFFu, ri.nb, 0);
+      if (nb == 0) continue;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&M.q_full, tok & 1, abort_v, p.status))) break;
+      for (int b = 0; b < nb; ++b, ++g) {
+        const uint32_t ph = g & 1;
 #pragma unroll 1
-          for (int grp = 0; grp < kGroups; ++grp) {
-            if (!mbar_wait(&M.full[grp], ph, abort_v, p.status)) { ok = false; break; }
-            tc_fence_after();
-            const int c1 = grp < 4 ? 2 * grp + 2 : kChunks;
-#pragma unroll 1
-            for (int c = 2 * grp; c < c1; ++c) {
-              const uint64_t ka = k_desc + static_cast<uint64_t>((c * kChunkBytes) >> 4);
-              const uint64_t qb = q_desc + static_cast<uint64_t>((c * kQChunkBytes) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16(tmem + kColS, ka + static_cast<uint64_t>(kk * 2), qb + static_cast<uint64_t>(kk * 2),
-                        idesc_qk, (c | kk) != 0);
-            }
-          }
-          if (!ok) break;
-          mma_commit(&M.s_full);
-          if (b == ri.nb - 1) mma_commit(&M.q_empty);  // Q may be replaced once these finish
-          if (!mbar_wait(&M.p_full, ph, abort_v, p.status) ||
-              (b == 0 && !mbar_wait(&M.o_empty, (tok & 1) ^ 1, abort_v, p.status))) {
-            ok = false;
-            break;
-          }
+        for (int grp = 0; grp < kGroups; ++grp) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&M.full[grp], ph, abort_v, p.status))) { ok = false; break; }
           tc_fence_after();
+          const int c1 = grp < 4 ? 2 * grp + 2 : kChunks;
 #pragma unroll 1
-          for (int dt = 0; dt < 4; ++dt) {
+          for (int c = 2 * grp; c < c1; ++c) {
+            const uint64_t ka = k_desc + static_cast<uint64_t>((c * kChunkBytes) >> 4);
+            const uint64_t qb = q_desc + static_cast<uint64_t>((c * kQChunkBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16(tmem + kColO + dt * 64,
-                      vt_desc + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
-                      p_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (b | kk) != 0);
-            mma_commit(&M.empty[dt]);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_warp(tm + kColS, ka + static_cast<uint64_t>(kk * 2), qb + static_cast<uint64_t>(kk * 2),
+                           idesc_qk, (c | kk) != 0);
           }
         }
-        ++tok;
+        if (!ok) break;
+        mma_commit_warp(&M.s_full);
+        if (b == nb - 1) mma_commit_warp(&M.q_empty);  // Q may be replaced once these finish
+        const bool w_ok = mbar_wait(&M.p_full, ph, abort_v, p.status) &&
+                          (b != 0 || mbar_wait(&M.o_empty, (tok & 1) ^ 1, abort_v, p.status));
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_warp(tm + kColO + dt * 64,
+                         vt_desc + static_cast<uint64_t>((dt * 2 * kChunkBytes + kk * 2048) >> 4),
+                         p_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (b | kk) != 0);
+          mma_commit_warp(&M.empty[dt]);
+        }
       }
+      ++tok;
     }
   } else if (warp >= 12) {
     // ---------------------------------------------------------------- gather producers
