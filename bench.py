@@ -326,6 +326,8 @@ def main():
                     help="profiling only: use this many query tokens instead of the workload's")
     ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the host-buffer pass")
     ap.add_argument("--no-decode", action="store_true", help="profiling only: skip the decode measurement")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="profiling only: run and print the decode measurement alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_setup(args.gpus)
@@ -337,6 +339,12 @@ def main():
         smla.build()
     barrier(world)
     L = smla.lib()
+    if args.decode_only:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        d = measure_decode(args, torch.cuda.current_stream(), flush)
+        if rank == 0:
+            print(json.dumps({"decode": d}))
+        return
     spec = wl.SPECS[args.workload]
     if args.tokens:
         spec = wl.scaled(spec, n_tokens=args.tokens)

@@ -218,10 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]
   uint32_t* scratch = hist + 1536;                              // [2][16]
-  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [128]
-  uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 128);     // [128]
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [2 tile parities][128 tokens]
+  uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 256);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + 16);
+  uint32_t* wcnt = wsum + 16;                                   // [2 wg][2 parities][16 tokens][4 warps]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wcnt + 256);
   // ring barriers of stages 0-3, accumulators, query tile, then the ring
   // barriers of the split-mode stages 4-11
   uint64_t* acc_full = bars + 2 * kStages;
@@ -453,8 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Select the best `keep` of token j's buffer. If `to_output`, write the
     // selection to the output row (or the split-mode candidate slot); else
     // compact the buffer in place (stable) and raise the token's threshold.
-    auto select_token = [&](int j, int keep, bool to_output, const Item& it) {
-      const int n = cnt[j];
+    auto select_token = [&](int j, int n, int keep, bool to_output, const Item& it) -> int {
       uint32_t* kb = ckey + j * cap;
       uint32_t* ib = cidx + j * cap;
       if (to_output && p.defer && n > keep) {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid_wg == 0) p.cand_cnt[row] = n;
         wg_sync();
-        return;
+        return n;
       }
       uint32_t tk = 0, ti = 0xFFFFFFFFu;
       const bool all = n <= keep;
@@ -554,13 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       wg_sync();
       if (!to_output && tid_wg == 0) {
-        cnt[j] = base;
         // admit later keys from the cut (or the k-th key) up: keys stream in
         // a rotated order, so a later key equal to it may have a smaller
         // index and win the tie
         theta[j] = tk > 0 ? tk - 1 : 0;
       }
       wg_sync();
+      return base;
     };
 
     for (int k = 0;; ++k) {
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wbuf[i] = gi < p.n_rows * HI ? __ldg(p.w + gi) : 0.0f;
       }
       for (int j = threadIdx.x - 128; j < p.tq; j += kEpiThreads) {
-        cnt[j] = 0;
+        cnt[(ac & 1u) * 128 + j] = 0;
         theta[j] = 0;
       }
       named_bar_sync(3, kEpiThreads);
@@ -668,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = t * kTileKeys + q * 32 + lane;
           float ks = 1.0f;
           if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
-          // ReLU + head-weighted sum with four independent partial sums per token
-          // (weights read as float4 broadcasts), then the admission test
+          // ReLU + head-weighted sum with eight independent partial sums per
+          // token (weights read as float4 broadcasts), then the admission test
           uint32_t key[TPW_MAX], m[TPW_MAX];
           bool adm[TPW_MAX];
 #pragma unroll
@@ -679,53 +679,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             key[jj] = 0;
             if (j < j1) {
               const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
-              float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+              float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
               for (int h = 0; h < HI; h += 4) {
                 const float4 wv = w4[h >> 2];
-                a0 = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a0);
-                a1 = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a1);
-                a2 = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a2);
-                a3 = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a3);
+                const int o = (h >> 2) & 1 ? 4 : 0;
+                a[o + 0] = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a[o + 0]);
+                a[o + 1] = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a[o + 1]);
+                a[o + 2] = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a[o + 2]);
+                a[o + 3] = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a[o + 3]);
               }
-              key[jj] = score_key(((a0 + a1) + (a2 + a3)) * ks);
+              key[jj] = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
               const bool valid = j < it.nrows && s >= it.key_lo && s < it.key_hi && s <= it.pos0 + j;
               adm[jj] = valid && key[jj] > theta[j];
             }
             m[jj] = __ballot_sync(0xFFFFFFFFu, adm[jj]);
           }
-          // every warp reads the token counts (the last tile's reservations
-          // are done), and only then may any warp reserve again: a warp that
-          // read a count after another's reservation could take a different
-          // branch and miss the selection's barriers
-          wg_sync();
-          bool over[TPW_MAX];
-#pragma unroll
-          for (int jj = 0; jj < TPW_MAX; ++jj) over[jj] = j0 + jj < j1 && cnt[j0 + jj] > cap - kTileKeys;
-          wg_sync();
-#pragma unroll
-          for (int jj = 0; jj < TPW_MAX; ++jj)
-            if (over[jj]) select_token(j0 + jj, topk, false, it);
-          // one reservation per warp and token; both issued before either is used
-          int base[TPW_MAX];
+          // The warps post their admitted counts and meet once: every warp
+          // then knows each token's count before the tile (double-buffered by
+          // tile parity, so the update below cannot race a slower warp's
+          // read), the tile's total and its own offset, and all take the
+          // same decision to compact a buffer the tile would overflow.
+          const int par = static_cast<int>(ac & 1u);
+          uint32_t* wc = wcnt + (wg * 2 + par) * 64;
           if (lane == 0) {
 #pragma unroll
-            for (int jj = 0; jj < TPW_MAX; ++jj) base[jj] = m[jj] ? atomicAdd(&cnt[j0 + jj], __popc(m[jj])) : 0;
+            for (int jj = 0; jj < TPW_MAX; ++jj) wc[jj * 4 + (ew & 3)] = static_cast<uint32_t>(__popc(m[jj]));
           }
+          wg_sync();
 #pragma unroll
           for (int jj = 0; jj < TPW_MAX; ++jj) {
-            base[jj] = __shfl_sync(0xFFFFFFFFu, base[jj], 0);
+            const int j = j0 + jj;
+            if (j >= j1) continue;
+            int pre = 0, tot = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < 4; ++w2) {
+              const int v = static_cast<int>(wc[jj * 4 + w2]);
+              if (w2 < (ew & 3)) pre += v;
+              tot += v;
+            }
+            int cb = cnt[par * 128 + j];
+            if (cb + tot > cap) cb = select_token(j, cb, topk, false, it);
             if (adm[jj]) {
-              const int j = j0 + jj;
-              const int pos = base[jj] + __popc(m[jj] & lanemask_lt);
+              const int pos = cb + pre + __popc(m[jj] & lanemask_lt);
               ckey[j * cap + pos] = key[jj];
               cidx[j * cap + pos] = static_cast<uint32_t>(s);
             }
+            if (tid_wg == 0) cnt[(par ^ 1) * 128 + j] = cb + tot;
           }
         }
         if (!ok) break;
         wg_sync();
-        for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, topk, true, it);
+        for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, cnt[(ac & 1u) * 128 + j], topk, true, it);
       }
     }
   }
@@ -1146,7 +1151,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      1536 * 4 + 32 * 4 + 128 * 4 + 128 * 4 + 16 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
+                      1536 * 4 + 32 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -170,6 +170,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+// L2 prefetch of the 128-byte lines covering [p, p + bytes): plain per-line
+// prefetches, which do not occupy the bulk-copy unit (one bulk prefetch per
+// thread and row stalled the issuing warp for ~100 cycles each).
+__device__ __forceinline__ void prefetch_l2_lines(const void* p, uint32_t bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
+  for (uintptr_t a = a0; a < a1; a += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
