@@ -396,43 +396,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nrow;
         if (next_row(p.n_rows * p.n_parts, k + 1, nrow) > 0) {
           constexpr uint32_t kQSlice = H * kDqk * 2 / kProducers;
-          static_assert(kQSlice % 16 == 0, "prefetch slices are 16-byte multiples");
           const uint8_t* nq = reinterpret_cast<const uint8_t*>(p.q + static_cast<size_t>(nrow / p.n_parts) * H * kDqk);
-          prefetch_l2_bulk(nq + tid * kQSlice, kQSlice);
+          prefetch_l2_lines(nq + tid * kQSlice, kQSlice);
         }
       }
-      // widen the BF16 query to f16 into the swizzled Q tile
+      // the BF16 query: its 16-byte pieces are copied asynchronously straight
+      // into the swizzled Q tile, then each thread widens the pieces it copied
+      // to f16 in place
       {
         const uint16_t* qr = p.q + static_cast<size_t>(row) * H * kDqk;
         constexpr int kQPieces = (H * 72 + kProducers - 1) / kProducers;
-        constexpr int kQBatch = 12;
-#pragma unroll 1
-        for (int u0 = 0; u0 < kQPieces; u0 += kQBatch) {
-          uint4 vq[kQBatch];
-#pragma unroll
-          for (int u = 0; u < kQBatch; ++u) {
-            const int pc = tid + (u0 + u) * kProducers;
-            const int h = pc / 72, pp = pc - h * 72;
-            if (u0 + u < kQPieces && pc < H * 72) vq[u] = ldg_stream(qr + h * kDqk + pp * 8);
-          }
-          if (u0 == 0 && !mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) { ok = false; break; }
-#pragma unroll
-          for (int u = 0; u < kQBatch; ++u) {
-            const int pc = tid + (u0 + u) * kProducers;
-            if (u0 + u >= kQPieces || pc >= H * 72) break;
-            const int h = pc / 72, pp = pc - h * 72;
-            const uint32_t in[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              over |= bf16x2_over_f16(in[t]);
-              o[t] = bf16x2_to_f16x2(in[t]);
-            }
-            *reinterpret_cast<uint4*>(q_tile + (pp >> 3) * kQChunkBytes + sw_off(h, pp & 7)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-          }
+        if (!mbar_wait(&M.q_empty, (tok & 1) ^ 1, abort_v, p.status)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        const uint32_t q_u32 = smem_u32(q_tile);
+#pragma unroll 4
+        for (int u = 0; u < kQPieces; ++u) {
+          const int pc = tid + u * kProducers;
+          if (pc >= H * 72) break;
+          const int h = pc / 72, pp = pc - h * 72;
+          cp_async_16(q_u32 + (pp >> 3) * kQChunkBytes + sw_off(h, pp & 7), qr + h * kDqk + pp * 8, 16u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+#pragma unroll 4
+        for (int u = 0; u < kQPieces; ++u) {
+          const int pc = tid + u * kProducers;
+          if (pc >= H * 72) break;
+          const int h = pc / 72, pp = pc - h * 72;
+          uint4* qp = reinterpret_cast<uint4*>(q_tile + (pp >> 3) * kQChunkBytes + sw_off(h, pp & 7));
+          const uint4 v = *qp;
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            over |= bf16x2_over_f16(in[t]);
+            o[t] = bf16x2_to_f16x2(in[t]);
+          }
+          *qp = make_uint4(o[0], o[1], o[2], o[3]);
+        }
         fence_proxy_async_smem();
         named_bar_sync(2, kProducers);
         if (tid == 0) mbar_arrive(&M.q_full);
@@ -630,12 +633,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t raw[HW];
         tmem_ld_cols<HW>(tmem + lane_base + kColS + h0, raw);
         tmem_wait_ld();
+        // this thread's heads' reference maxima (16-byte broadcast loads)
+        float mh[HW];
+        auto load_m = [&]() {
+#pragma unroll
+          for (int i = 0; i < HW; i += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(&M.m[h0 + i]);
+            mh[i] = v.x;
+            mh[i + 1] = v.y;
+            mh[i + 2] = v.z;
+            mh[i + 3] = v.w;
+          }
+        };
+        load_m();
         // does any logit exceed its head's reference max by more than 2^8?
         bool flag = b == 0;
         if (!flag && valid) {
           float tmax = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < HW; ++i) tmax = fmaxf(tmax, fmaf(__uint_as_float(raw[i]), mt.x, -M.m[h0 + i]));
+          for (int i = 0; i < HW; ++i) tmax = fmaxf(tmax, fmaf(__uint_as_float(raw[i]), mt.x, -mh[i]));
           flag = tmax > kRescaleLog2;
         }
         if (named_bar_or(1, 256, flag)) {
@@ -677,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
           }
+          load_m();  // the maxima may have been raised
         }
         // probabilities, partial sums, P^T row
         {
@@ -690,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < HW; i += 2) {
             float p0 = 0.0f, p1 = 0.0f;
             if (valid) {
-              p0 = fast_exp2(fmaf(__uint_as_float(raw[i]), mt.x, -M.m[h0 + i]));
-              p1 = fast_exp2(fmaf(__uint_as_float(raw[i + 1]), mt.x, -M.m[h0 + i + 1]));
+              p0 = fast_exp2(fmaf(__uint_as_float(raw[i]), mt.x, -mh[i]));
+              p1 = fast_exp2(fmaf(__uint_as_float(raw[i + 1]), mt.x, -mh[i + 1]));
             }
             lp[i] = __float_as_uint(b > 0 ? __uint_as_float(lp[i]) + p0 : p0);
             lp[i + 1] = __float_as_uint(b > 0 ? __uint_as_float(lp[i + 1]) + p1 : p1);
@@ -738,6 +755,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar_sync(1, 256);
       const bool odd = lane & 1;
+      float li[HW];  // this thread's heads' 1 / l
+#pragma unroll
+      for (int i = 0; i < HW; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&M.linv[h0 + i]);
+        li[i] = v.x;
+        li[i + 1] = v.y;
+        li[i + 2] = v.z;
+        li[i + 3] = v.w;
+      }
       if (p.n_parts > 1) {
         // normalised fp32 partial output of this part: [H][512]
         float* po = p.part_o + static_cast<size_t>(item) * H * kDv;
@@ -748,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_cols<HW>(tmem + lane_base + kColO + dt * 64 + h0, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < HW; ++c) po[static_cast<size_t>(h0 + c) * kDv + d] = __uint_as_float(o[c]) * M.linv[h0 + c];
+          for (int c = 0; c < HW; ++c) po[static_cast<size_t>(h0 + c) * kDv + d] = __uint_as_float(o[c]) * li[c];
         }
       }
 #pragma unroll 1
@@ -760,8 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < HW; c += 2) {
-          const float v0 = __uint_as_float(o[c]) * M.linv[h0 + c];
-          const float v1 = __uint_as_float(o[c + 1]) * M.linv[h0 + c + 1];
+          const float v0 = __uint_as_float(o[c]) * li[c];
+          const float v1 = __uint_as_float(o[c + 1]) * li[c + 1];
           const float x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? v0 : v1, 1);
           const uint32_t word = odd ? pack_bf16(x2, v1) : pack_bf16(v0, x2);
           const int hh = h0 + (odd ? c + 1 : c);
