@@ -27,9 +27,14 @@
 // sequence against all their keys; items are handed out in head/tail pairs
 // (the i-th cheapest with the i-th most expensive, the "V" pairing of the
 // page's PCP section applied across SMs) so every CTA gets the same mix of
-// short and long causal rows. Decode ("split mode") takes all rows of one
-// sequence against one block of 8192 keys and writes every score to the
-// row's score array; select_kernel then takes each row's exact top-k.
+// short and long causal rows. When every row has at most 16,384 keys
+// ("dense" group mode, two rows per item) the candidate space holds each
+// row's full score array instead of a candidate buffer: scores are stored at
+// their key's position, with no admission test or compaction while the tiles
+// stream, and the exact top-k of each row is taken from shared memory at the
+// end of the item. Decode ("split mode") takes all rows of one sequence
+// against one block of 8192 keys and writes every score to the row's score
+// array; select_kernel then takes each row's exact top-k.
 #include <algorithm>
 
 #include "common.cuh"
@@ -204,8 +209,9 @@ __device__ __forceinline__ void tmem_ld_heads(uint32_t taddr, uint32_t* r) {
 }
 
 // SPLIT: decode shape (compile-time, so the decode kernel carries none of the
-// candidate-selection code)
-template <int HI, bool SPLIT>
+// candidate-selection code). DENSE: prefill rows short enough that every
+// score of a work item fits in shared memory (see the epilogue).
+template <int HI, bool SPLIT, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IdxParams p) {
@@ -216,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* ckey = reinterpret_cast<uint32_t*>(b_tile + kMaxN * kIdxRowBytes);
   uint32_t* cidx = ckey + kBufEntries;
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]
-  uint32_t* scratch = hist + 1536;                              // [2][16]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]; dense mode [2][4][256]
+  uint32_t* scratch = hist + 2048;                              // [2][16]
   int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [2 tile parities][128 tokens]
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 256);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], SPLIT ? 4 : kEpiThreads / 32);  // split: one warpgroup per buffer
+      mbar_init(&acc_empty[i], (SPLIT || DENSE) ? 4 : kEpiThreads / 32);  // one warpgroup per buffer
     }
     mbar_init(b_full, 1);
     mbar_init(b_empty, kIssuers);
@@ -411,8 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t g = __shfl_sync(0xFFFFFFFFu, sc0 + tt, 0);
         const int s = g % nst;
         const int buf = g & ((1u << p.acc_shift) - 1);
+        // a free accumulator can take long (the epilogue is the slower side):
+        // wait suspended so the spin does not take issue slots from the
+        // epilogue warps on this SM sub-partition
         ok = mbar_wait_spin(full_bar(s), (g / nst) & 1, abort_v, p.status) &&
-             mbar_wait_spin(&acc_empty[buf], ((g >> p.acc_shift) & 1) ^ 1, abort_v, p.status);
+             mbar_wait(&acc_empty[buf], ((g >> p.acc_shift) & 1) ^ 1, abort_v, p.status);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
@@ -563,6 +572,269 @@ __global__ void __launch_bounds__(kThreads, 1)
       return base;
     };
 
+    // Dense mode: the exact top-k of token j from its full score array
+    // (position = key index, keys 0..pos). Warp w of the warpgroup owns a
+    // contiguous quarter of the row (a multiple of 512 entries).
+    //  1. Each warp histograms its quarter into its own 256 bins of the score
+    //     VALUE over the row's [min, max] (found while the tiles streamed):
+    //     value bins spread a row far better than the float's top bits, so
+    //     the shared-memory counters rarely collide.
+    //  2. Every warp sums the four histograms and finds the bin b holding the
+    //     k-th best, how many of it are needed (r) and each warp's count of
+    //     entries above b.
+    //  3. One pass (16 entries per lane and step, one scan of packed counts)
+    //     writes each warp's entries above b at its offset, in a fixed order,
+    //     and stages the warp's entries of b (key, index) in its quarter of
+    //     the query tile's unused rows.
+    //  4. The staged entries are ranked exactly (key descending, index
+    //     ascending); the best r follow the others, in rank order.
+    // A bin too full to stage (heavy ties) falls back to the range-adaptive
+    // radix selection over the whole row and an ordered count-and-write. The
+    // order of a row's indices is deterministic but not ascending.
+    const int stage_cap = ((kMaxN - N) * kIdxRowBytes / 16) & ~15;  // staged (key, index) pairs per warpgroup
+    uint32_t* stg = reinterpret_cast<uint32_t*>(b_tile + N * kIdxRowBytes) + wg * 2 * stage_cap;
+    uint32_t* dsv = wcnt + 64 + 32 * wg;  // [0] staged, [1,2] threshold, [4..7] per-warp counts above b
+    auto dense_token = [&](int j, const Item& it) {
+      int n = it.pos0 + j + 1;
+      if (n > cap) {  // a sequence longer than the host's bound: keys past the score slots are skipped
+        if (tid_wg == 0) set_status(p.status, kStatusBounds);
+        n = cap;
+      }
+      const uint32_t* kb = ckey + j * cap;
+      const int row = it.row0 + j;
+      int32_t* o = p.out_idx + static_cast<size_t>(row) * topk;
+      float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * topk : nullptr;
+      if (n <= topk) {  // every key is kept
+        for (int e = tid_wg; e < topk; e += 128) {
+          o[e] = e < n ? e : -1;
+          if (os) os[e] = e < n ? key_score(kb[e]) : 0.0f;
+        }
+        return;
+      }
+      const int w4 = tid_wg >> 5;
+      const int cw = (n + 2047) / 2048 * 512;  // entries per warp
+      const int b0 = w4 * cw, b1 = min(n, b0 + cw);
+      uint32_t* dh = hist + 1024 * wg;          // [4 warps][256 bins]
+      uint32_t* hw = dh + 256 * w4;
+      const float vlo = key_score(wcnt[j]), vhi = key_score(wcnt[4 + j]);
+      float vinv = vhi > vlo ? 256.0f / (vhi - vlo) : 0.0f;
+      if (!(vinv <= 1.0e30f)) vinv = 0.0f;  // a degenerate range: one bin
+      auto bin_of = [&](uint32_t key) -> int { return min(255, static_cast<int>((key_score(key) - vlo) * vinv)); };
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hw[lane + 32 * i] = 0;
+      if (tid_wg == 0) dsv[0] = 0;
+      __syncwarp();
+      for (int b = b0; b < b1; b += 512) {
+        uint4 kv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const uint4*>(kb + b + 128 * u + 4 * lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e0 = b + 128 * u + 4 * lane;
+          const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            if (e0 + q4 < n) atomicAdd(&hw[bin_of(k4[q4])], 1u);
+        }
+      }
+      wg_sync();
+      // lane l owns bins 255-8l down to 248-8l: totals over the four warps
+      uint32_t c[8], mine[8];
+      {
+        const uint4* h4 = reinterpret_cast<const uint4*>(dh + 248 - 8 * lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+          const uint4 lo4 = h4[64 * w2], hi4 = h4[64 * w2 + 1];  // bins 248-8l .. 255-8l of warp w2
+          const uint32_t v8[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            c[i] += v8[i];
+            if (w2 == w4) mine[i] = v8[i];
+          }
+        }
+      }
+      uint32_t sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += c[i];
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+        if (lane >= o2) incl += t2;
+      }
+      const uint32_t excl = incl - sum;
+      uint32_t found = 0, r_in = 0, m_in = 0;
+      if (excl < static_cast<uint32_t>(topk) && incl >= static_cast<uint32_t>(topk)) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (found == 0 && run + c[i] >= static_cast<uint32_t>(topk)) {
+            found = 0x80000000u | static_cast<uint32_t>(255 - 8 * lane - i);
+            r_in = static_cast<uint32_t>(topk) - run;
+            m_in = c[i];
+          }
+          run += c[i];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xFFFFFFFFu, found != 0)) - 1;
+      const int bstar = static_cast<int>(__shfl_sync(0xFFFFFFFFu, found, src) & 0xFFu);
+      const int r = static_cast<int>(__shfl_sync(0xFFFFFFFFu, r_in, src));
+      const int m = static_cast<int>(__shfl_sync(0xFFFFFFFFu, m_in, src));
+      // each warp's entries in the bin (staged in its own quarter of the room)
+      const int wcap = stage_cap / 4;
+      const uint32_t m0 = dh[bstar], m1 = dh[256 + bstar], m2 = dh[512 + bstar], m3 = dh[768 + bstar];
+      if (max(max(m0, m1), max(m2, m3)) <= static_cast<uint32_t>(wcap)) {
+        // this warp's entries above the bin, and the warps' before it
+        uint32_t above = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (255 - 8 * lane - i > bstar) above += mine[i];
+        above = __reduce_add_sync(0xFFFFFFFFu, above);
+        if (lane == 0) dsv[4 + w4] = above;
+        wg_sync();
+        int base = 0;
+        for (int w2 = 0; w2 < w4; ++w2) base += static_cast<int>(dsv[4 + w2]);
+        const int n_above = static_cast<int>(dsv[4] + dsv[5] + dsv[6] + dsv[7]);
+        uint32_t* sk = stg + w4 * wcap;              // this warp's staged keys
+        uint32_t* si = stg + stage_cap + w4 * wcap;  // and their indices
+        int sbase = 0;
+        // 16 entries per lane and step (lane l: 4 consecutive entries in each
+        // 128-entry quarter); one scan of the packed (above, in-bin) counts
+        for (int b = b0; b < b1; b += 512) {
+          uint4 kv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const uint4*>(kb + b + 128 * u + 4 * lane);
+          int bb[16];
+          int cnt2 = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int e = b + 128 * u + 4 * lane + q4;
+              bb[4 * u + q4] = e < n ? bin_of(k4[q4]) : -1;
+              cnt2 += bb[4 * u + q4] > bstar ? 1 : (bb[4 * u + q4] == bstar ? 0x10000 : 0);
+            }
+          }
+          int incl2 = cnt2;
+#pragma unroll
+          for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl2, o2);
+            if (lane >= o2) incl2 += v;
+          }
+          const int ex = incl2 - cnt2;
+          int off = base + (ex & 0xFFFF), soff = sbase + (ex >> 16);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int e = b + 128 * u + 4 * lane + q4;
+              if (bb[4 * u + q4] > bstar) {
+                if (off < topk) {
+                  o[off] = e;
+                  if (os) os[off] = key_score(k4[q4]);
+                }
+                ++off;
+              } else if (bb[4 * u + q4] == bstar) {
+                if (soff < wcap) {
+                  sk[soff] = k4[q4];
+                  si[soff] = static_cast<uint32_t>(e);
+                }
+                ++soff;
+              }
+            }
+          }
+          const int tot = __shfl_sync(0xFFFFFFFFu, incl2, 31);
+          base += tot & 0xFFFF;
+          sbase += tot >> 16;
+        }
+        wg_sync();
+        // the r best staged entries (key descending, index ascending) follow
+        // the others, in that order
+        const int mw[4] = {static_cast<int>(m0), static_cast<int>(m1), static_cast<int>(m2), static_cast<int>(m3)};
+        for (int a = tid_wg; a < m; a += 128) {
+          int wa = 0, ia = a;
+#pragma unroll
+          for (int w2 = 0; w2 < 3; ++w2)
+            if (wa == w2 && ia >= mw[w2]) {
+              ia -= mw[w2];
+              wa = w2 + 1;
+            }
+          const uint32_t ka = stg[wa * wcap + ia], xa = stg[stage_cap + wa * wcap + ia];
+          int rank = 0;
+#pragma unroll
+          for (int w2 = 0; w2 < 4; ++w2) {
+            const uint32_t* fk = stg + w2 * wcap;
+            const uint32_t* fi = stg + stage_cap + w2 * wcap;
+            const int mf = mw[w2];
+            int f = 0;
+            for (; f + 4 <= mf; f += 4) {
+              const uint4 k4 = *reinterpret_cast<const uint4*>(fk + f);
+              const uint4 i4 = *reinterpret_cast<const uint4*>(fi + f);
+              rank += (k4.x > ka || (k4.x == ka && i4.x < xa)) + (k4.y > ka || (k4.y == ka && i4.y < xa)) +
+                      (k4.z > ka || (k4.z == ka && i4.z < xa)) + (k4.w > ka || (k4.w == ka && i4.w < xa));
+            }
+            for (; f < mf; ++f) rank += fk[f] > ka || (fk[f] == ka && fi[f] < xa);
+          }
+          if (rank < r && n_above + rank < topk) {
+            o[n_above + rank] = static_cast<int32_t>(xa);
+            if (os) os[n_above + rank] = key_score(ka);
+          }
+        }
+      } else {
+        uint32_t tk = 0, ti = 0xFFFFFFFFu;
+        wg_sync();  // every warp has read the histograms
+        dense_select<128>(kb, nullptr, n, topk, tid_wg, dh, scr_wg, wg_sync, tk, ti);
+        int cnt_w = 0;
+        for (int b = b0; b < b1; b += 128) {
+          const int e0 = b + 4 * lane;
+          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+          const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            cnt_w += e0 + q4 < n && selected(k4[q4], static_cast<uint32_t>(e0 + q4), tk, ti);
+        }
+        cnt_w = __reduce_add_sync(0xFFFFFFFFu, cnt_w);
+        if (lane == 0) dsv[4 + w4] = static_cast<uint32_t>(cnt_w);
+        wg_sync();
+        int base = 0;
+        for (int w2 = 0; w2 < w4; ++w2) base += static_cast<int>(dsv[4 + w2]);
+        for (int b = b0; b < b1; b += 128) {
+          const int e0 = b + 4 * lane;
+          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+          const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+          bool t[4];
+          int cl = 0;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            t[q4] = e0 + q4 < n && selected(k4[q4], static_cast<uint32_t>(e0 + q4), tk, ti);
+            cl += t[q4];
+          }
+          int incl2 = cl;
+#pragma unroll
+          for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl2, o2);
+            if (lane >= o2) incl2 += v;
+          }
+          int off = base + incl2 - cl;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (!t[q4]) continue;
+            if (off < topk) {
+              o[off] = e0 + q4;
+              if (os) os[off] = key_score(k4[q4]);
+            }
+            ++off;
+          }
+          base += __shfl_sync(0xFFFFFFFFu, incl2, 31);
+        }
+      }
+      wg_sync();  // histograms, counts and staging are reused by the next row
+    };
+
     for (int k = 0;; ++k) {
       Item it;
       const int r = next_item(p, k, it, pref);
@@ -576,6 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = threadIdx.x - 128; j < p.tq; j += kEpiThreads) {
         cnt[(ac & 1u) * 128 + j] = 0;
         theta[j] = 0;
+        if constexpr (DENSE) {
+          wcnt[j] = 0xFFFFFFFFu;  // the row's smallest and largest score key
+          wcnt[4 + j] = 0;
+        }
       }
       named_bar_sync(3, kEpiThreads);
       if (it.trivial) {
@@ -644,6 +920,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ac = ac0 + nt;
         if (!ok) break;
+      } else if constexpr (DENSE) {
+        // prefill, rows of at most `cap` keys: every score goes to the token's
+        // array in shared memory at its key's position, so a tile needs no
+        // coordination between warps; the two warpgroups take the tiles in
+        // turn (each accumulator buffer belongs to one warpgroup), each
+        // covering every row of its tile. Once the item's tiles are all in,
+        // each warpgroup selects its rows' exact top-k.
+        const uint32_t ac0 = ac;
+        const int nt = it.t1 - it.t0;
+        // each row's smallest and largest score key, kept per thread over the
+        // item's tiles (rows jb + jj of a single pass) and merged at its end
+        constexpr bool kOnePass = TPW_MAX >= 2;  // every row's scores in one pass of TPW_MAX rows
+        uint32_t rmin[TPW_MAX], rmax[TPW_MAX];
+#pragma unroll
+        for (int jj = 0; jj < TPW_MAX; ++jj) {
+          rmin[jj] = 0xFFFFFFFFu;
+          rmax[jj] = 0;
+        }
+        for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt; tt += 2) {
+          const uint32_t g = ac0 + tt;
+          const int t = tile_at(it, tt);
+          const int buf = g & ((1u << p.acc_shift) - 1);
+          if (!mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int s = t * kTileKeys + q * 32 + lane;
+          float ks = 1.0f;
+          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          for (int jb = 0; jb < p.tq; jb += TPW_MAX) {
+            uint32_t raw[TPW_MAX * HI];
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj)
+              if (jb + jj < p.tq)
+                tmem_ld_heads<HI>(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N + (jb + jj) * HI,
+                                  raw + jj * HI);
+            tmem_wait_ld();
+            if (jb + TPW_MAX >= p.tq) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj) {
+              const int j = jb + jj;
+              if (j >= p.tq) break;
+              uint32_t key = 0, kmin = 0xFFFFFFFFu, kmax = 0;
+              if (j < it.nrows && s < it.key_hi && s <= it.pos0 + j && s < cap) {
+                const float4* w4 = reinterpret_cast<const float4*>(wbuf + j * HI);
+                float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int h = 0; h < HI; h += 4) {
+                  const float4 wv = w4[h >> 2];
+                  const int o = (h >> 2) & 1 ? 4 : 0;
+                  a[o + 0] = fmaf(wv.x, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f), a[o + 0]);
+                  a[o + 1] = fmaf(wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f), a[o + 1]);
+                  a[o + 2] = fmaf(wv.z, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f), a[o + 2]);
+                  a[o + 3] = fmaf(wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f), a[o + 3]);
+                }
+                key = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+                ckey[j * cap + s] = key;
+                kmin = key;
+                kmax = key;
+              }
+              if constexpr (kOnePass) {
+                rmin[jj] = min(rmin[jj], kmin);
+                rmax[jj] = max(rmax[jj], kmax);
+              } else {
+                kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+                kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+                if (lane == 0 && j < it.nrows) {
+                  atomicMin(&wcnt[j], kmin);
+                  atomicMax(&wcnt[4 + j], kmax);
+                }
+              }
+            }
+          }
+        }
+        if constexpr (kOnePass) {
+#pragma unroll
+          for (int jj = 0; jj < TPW_MAX; ++jj) {
+            if (jj >= p.tq) break;
+            const uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, rmin[jj]);
+            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, rmax[jj]);
+            if (lane == 0 && jj < it.nrows) {
+              atomicMin(&wcnt[jj], kmin);
+              atomicMax(&wcnt[4 + jj], kmax);
+            }
+          }
+        }
+        ac = ac0 + nt;
+        if (!ok) break;
+        named_bar_sync(3, kEpiThreads);  // every score of the item is in shared memory
+        for (int j = wg; j < it.nrows; j += 2) dense_token(j, it);
       } else {
         // prefill: both warpgroups take every tile, each for its own query rows
         for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
@@ -1137,7 +1508,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
   }
 }
 
-template <int HI, bool SPLIT>
+template <int HI, bool SPLIT, bool DENSE>
 int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
   CUtensorMap map_k, map_q;
   const CUtensorMapDataType dt = prm.is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -1151,10 +1522,10 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      1536 * 4 + 32 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
+                      2048 * 4 + 32 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     attr_done = true;
@@ -1165,7 +1536,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                          : prm.n_seqs <= kMaxPrefixSeqs ? static_cast<int>(std::min<int64_t>(split_tiles, 1 << 30))
                                                         : prm.n_items;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
-  indexer_kernel<HI, SPLIT><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  indexer_kernel<HI, SPLIT, DENSE><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
@@ -1191,6 +1562,15 @@ int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_pe
   return kBufEntries / tq - 2 * kTileKeys >= topk ? tq : 0;
 }
 
+int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len) {
+  // two query rows per work item (four at 4 heads, so the MMA has N >= 16):
+  // each row's scores of keys 0..pos fill half of the candidate space
+  const int tq = h_idx >= 8 ? 2 : 16 / h_idx;
+  if (tq * h_idx > kMaxN) return 0;
+  const int cap = 2 * kBufEntries / tq;
+  return (max_seq_len <= cap && topk <= cap) ? tq : 0;
+}
+
 size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk) {
   if (indexer_split_mode(q_per_seq, h_idx) || n_rows <= 0) return 0;
   const int tq = indexer_tokens_per_cta(h_idx, topk, false, q_per_seq);
@@ -1212,7 +1592,9 @@ size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_pe
 
 int launch_indexer(const IndexerLaunch& L) {
   const bool split = indexer_split_mode(L.q_per_seq, L.h_idx);
-  const int tq = indexer_tokens_per_cta(L.h_idx, L.topk, split, L.q_per_seq);
+  const int dense_tq = split ? 0 : indexer_dense_tokens(L.h_idx, L.topk, L.max_seq_len);
+  const bool dense = dense_tq > 0;
+  const int tq = dense ? dense_tq : indexer_tokens_per_cta(L.h_idx, L.topk, split, L.q_per_seq);
   if (tq <= 0) return SMLA_ERR_UNSUPPORTED;
   IdxParams prm{};
   prm.k_scale = L.cache->k_idx_scale;
@@ -1227,7 +1609,7 @@ int launch_indexer(const IndexerLaunch& L) {
   prm.w = L.w;
   prm.topk = L.topk;
   prm.tq = tq;
-  prm.cap = kBufEntries / tq;
+  prm.cap = (dense ? 2 * kBufEntries : kBufEntries) / tq;  // dense: score slots per row
   prm.is_bf16 = L.cache->idx_dtype == SMLA_BF16;
   prm.split = split;
   const int N = L.h_idx * tq;
@@ -1251,7 +1633,7 @@ int launch_indexer(const IndexerLaunch& L) {
   } else {
     prm.n_groups = (L.q_per_seq + tq - 1) / tq;
     prm.n_items = L.n_seqs * prm.n_groups;
-    const size_t cand = indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk);
+    const size_t cand = dense ? 0 : indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk);
     if (L.cand && cand > 0 && L.cand_bytes >= cand && (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
       prm.defer = 1;
       prm.cand_key = static_cast<uint32_t*>(L.cand);
@@ -1261,11 +1643,26 @@ int launch_indexer(const IndexerLaunch& L) {
   }
   int rc;
   switch (L.h_idx) {
-    case 4: rc = split ? launch_indexer_t<4, true>(L, prm) : launch_indexer_t<4, false>(L, prm); break;
-    case 8: rc = split ? launch_indexer_t<8, true>(L, prm) : launch_indexer_t<8, false>(L, prm); break;
-    case 16: rc = split ? launch_indexer_t<16, true>(L, prm) : launch_indexer_t<16, false>(L, prm); break;
-    case 32: rc = split ? launch_indexer_t<32, true>(L, prm) : launch_indexer_t<32, false>(L, prm); break;
-    case 64: rc = split ? launch_indexer_t<64, true>(L, prm) : launch_indexer_t<64, false>(L, prm); break;
+    case 4:
+      rc = dense ? launch_indexer_t<4, false, true>(L, prm)
+           : split ? launch_indexer_t<4, true, false>(L, prm) : launch_indexer_t<4, false, false>(L, prm);
+      break;
+    case 8:
+      rc = dense ? launch_indexer_t<8, false, true>(L, prm)
+           : split ? launch_indexer_t<8, true, false>(L, prm) : launch_indexer_t<8, false, false>(L, prm);
+      break;
+    case 16:
+      rc = dense ? launch_indexer_t<16, false, true>(L, prm)
+           : split ? launch_indexer_t<16, true, false>(L, prm) : launch_indexer_t<16, false, false>(L, prm);
+      break;
+    case 32:
+      rc = dense ? launch_indexer_t<32, false, true>(L, prm)
+           : split ? launch_indexer_t<32, true, false>(L, prm) : launch_indexer_t<32, false, false>(L, prm);
+      break;
+    case 64:
+      rc = dense ? launch_indexer_t<64, false, true>(L, prm)
+           : split ? launch_indexer_t<64, true, false>(L, prm) : launch_indexer_t<64, false, false>(L, prm);
+      break;
     default: return SMLA_ERR_UNSUPPORTED;
   }
   if (rc != SMLA_OK) return rc;

@@ -83,6 +83,9 @@ int launch_shadow_convert(const MlaLaunch& L);
 // splits each sequence's keys into blocks merged afterwards (decode).
 bool indexer_split_mode(int32_t q_per_seq, int32_t h_idx);
 int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_per_seq);
+// Rows per work item of dense group mode (every row's scores held in shared
+// memory), or 0 when the rows are too long for it.
+int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len);
 size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
                                int32_t topk);
 // Group mode: bytes of the deferred per-row candidate buffers (0 if split mode).

@@ -201,11 +201,14 @@ def test_repeat_calls_same_sets():
     assert (oa.float() - ob.float()).abs().max().item() < 1e-2
 
 
+@pytest.mark.parametrize("prefix", [6000, 17000], ids=["dense", "streaming"])
 @pytest.mark.parametrize("mode", ["constant", "binary"])
-def test_indexer_heavy_ties(mode):
+def test_indexer_heavy_ties(mode, prefix):
     """Ties everywhere: constant keys (all scores equal -> the lowest k indices) and
-    keys in {0,1} (few distinct scores); the lower index must win every tie."""
-    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=700, prefix_len=6000, shuffled=True)
+    keys in {0,1} (few distinct scores); the lower index must win every tie. Rows
+    of at most 16,384 keys take the dense group mode (every score in shared
+    memory), longer rows the streaming candidate buffers."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=700, prefix_len=prefix, shuffled=True)
     prob = wl.make(spec, "cpu")
     k = prob.cache.k_idx
     if mode == "constant":
