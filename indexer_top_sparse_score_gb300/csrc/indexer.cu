@@ -208,6 +208,19 @@ __device__ __forceinline__ void tmem_ld_heads(uint32_t taddr, uint32_t* r) {
   }
 }
 
+// (d0, d1) += (a0, a1) * (b0, b1), both lanes rounded as fmaf (one packed FMA)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\tfma.rn.f32x2 rd, ra, rb, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// shared-memory counter increment whose old value is not needed
+__device__ __forceinline__ void smem_inc(uint32_t* p) {
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(smem_u32(p)) : "memory");
+}
+
 // SPLIT: decode shape (compile-time, so the decode kernel carries none of the
 // candidate-selection code). DENSE: prefill rows short enough that every
 // score of a work item fits in shared memory (see the epilogue).
@@ -625,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid_wg == 0) dsv[0] = 0;
       __syncwarp();
       for (int b = b0; b < b1; b += 512) {
+        const bool full = b + 512 <= n;
         uint4 kv[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const uint4*>(kb + b + 128 * u + 4 * lane);
@@ -634,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            if (e0 + q4 < n) atomicAdd(&hw[bin_of(k4[q4])], 1u);
+            if (full || e0 + q4 < n) smem_inc(&hw[bin_of(k4[q4])]);
         }
       }
       wg_sync();
@@ -703,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16 entries per lane and step (lane l: 4 consecutive entries in each
         // 128-entry quarter); one scan of the packed (above, in-bin) counts
         for (int b = b0; b < b1; b += 512) {
+          const bool full = b + 512 <= n;
           uint4 kv[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const uint4*>(kb + b + 128 * u + 4 * lane);
@@ -714,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int e = b + 128 * u + 4 * lane + q4;
-              bb[4 * u + q4] = e < n ? bin_of(k4[q4]) : -1;
+              bb[4 * u + q4] = (full || e < n) ? bin_of(k4[q4]) : -1;
               cnt2 += bb[4 * u + q4] > bstar ? 1 : (bb[4 * u + q4] == bstar ? 0x10000 : 0);
             }
           }
@@ -950,6 +965,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = t * kTileKeys + q * 32 + lane;
           float ks = 1.0f;
           if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          if constexpr (kOnePass) {
+            // one row's accumulator loads while the previous row is summed
+            uint32_t raw[TPW_MAX * HI];
+            const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * N;
+            tmem_ld_heads<HI>(ta, raw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < TPW_MAX; ++jj) {
+              if (jj >= p.tq) break;
+              const bool more = jj + 1 < TPW_MAX && jj + 1 < p.tq;
+              if (more) tmem_ld_heads<HI>(ta + (jj + 1) * HI, raw + (jj + 1) * HI);
+              if (jj < it.nrows && s < it.key_hi && s <= it.pos0 + jj && s < cap) {
+                const float4* w4 = reinterpret_cast<const float4*>(wbuf + jj * HI);
+                float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int h = 0; h < HI; h += 4) {
+                  const float4 wv = w4[h >> 2];
+                  const int o = (h >> 2) & 1 ? 4 : 0;
+                  fma2(a[o + 0], a[o + 1], wv.x, wv.y, fmaxf(__uint_as_float(raw[jj * HI + h + 0]), 0.0f),
+                       fmaxf(__uint_as_float(raw[jj * HI + h + 1]), 0.0f));
+                  fma2(a[o + 2], a[o + 3], wv.z, wv.w, fmaxf(__uint_as_float(raw[jj * HI + h + 2]), 0.0f),
+                       fmaxf(__uint_as_float(raw[jj * HI + h + 3]), 0.0f));
+                }
+                const uint32_t key =
+                    score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+                ckey[jj * cap + s] = key;
+                rmin[jj] = min(rmin[jj], key);
+                rmax[jj] = max(rmax[jj], key);
+              }
+              if (more) tmem_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          } else {
           for (int jb = 0; jb < p.tq; jb += TPW_MAX) {
             uint32_t raw[TPW_MAX * HI];
 #pragma unroll
@@ -985,18 +1035,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kmin = key;
                 kmax = key;
               }
-              if constexpr (kOnePass) {
-                rmin[jj] = min(rmin[jj], kmin);
-                rmax[jj] = max(rmax[jj], kmax);
-              } else {
-                kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-                kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-                if (lane == 0 && j < it.nrows) {
-                  atomicMin(&wcnt[j], kmin);
-                  atomicMax(&wcnt[4 + j], kmax);
-                }
+              kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+              kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+              if (lane == 0 && j < it.nrows) {
+                atomicMin(&wcnt[j], kmin);
+                atomicMax(&wcnt[4 + j], kmax);
               }
             }
+          }
           }
         }
         if constexpr (kOnePass) {
