@@ -102,16 +102,19 @@ int smla_version(void);
  *   w           [n_seqs*q_per_seq][h_idx] fp32 head weights.
  *   out_idx     [n_seqs*q_per_seq][topk] int32: the selected key positions of
  *               every query row, min(topk, pos+1) valid entries first in no
- *               particular order, then -1.
+ *               particular order (deterministic for given inputs), then -1.
  *   out_scores  [n_seqs*q_per_seq][topk] fp32 scores of out_idx, or NULL.
  * Supported: h_idx in {4, 8, 16, 32, 64}; 1 <= topk <= 2048. Integer-valued
  * inputs make the selection bit-identical to the exact fp32 definition.
  * Workspace: the returned size. When several query rows share the key stream
- * (long per-sequence batches), 256 bytes already suffice and the rest holds
- * per-row candidate buffers (up to 16384 / rows-per-work-item (key, index)
- * pairs of 8 bytes, plus a count per row) whose final exact selection then
- * runs in a separate light kernel instead of stalling the scoring pipeline;
- * with less room the selection stays in the scoring kernel. Decode-shaped
+ * (long per-sequence batches), 256 bytes already suffice. With max_seq_len at
+ * most 16384 (8192 at h_idx = 4) every row's scores fit in shared memory and
+ * the exact top-k is taken there; for longer sequences the rest of the
+ * workspace holds per-row candidate buffers (up to 16384 / rows-per-work-item
+ * (key, index) pairs of 8 bytes, plus a count per row) whose final exact
+ * selection then runs in a separate light kernel instead of stalling the
+ * scoring pipeline; with less room the selection stays in the scoring kernel.
+ * Decode-shaped
  * calls (few rows per sequence, whose keys are split across SMs) require a
  * score array per query row (4 bytes per key up to max_seq_len): the scoring
  * kernel writes every score and a per-row kernel then selects the exact top-k.

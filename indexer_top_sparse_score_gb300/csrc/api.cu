@@ -1,6 +1,7 @@
 // extern "C" entry points of libsmla.so: argument checks, workspace layout,
 // and the launch sequence of each call. No allocation, no synchronisation
 // (smla_read_status excepted).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -114,7 +115,7 @@ size_t smla_indexer_topk_workspace_size(int32_t n_seqs, int32_t max_seq_len, int
                                         int32_t h_idx, int32_t topk) {
   if (n_seqs <= 0 || max_seq_len <= 0 || q_per_seq <= 0 || topk <= 0) return kStatusBytes;
   return round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk)) +
-         indexer_group_cand_bytes(n_seqs * q_per_seq, q_per_seq, h_idx, topk);
+         indexer_group_cand_bytes(n_seqs * q_per_seq, q_per_seq, h_idx, topk, max_seq_len);
 }
 
 static int indexer_checks(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
@@ -209,7 +210,8 @@ size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_toke
   if (prefix_len < 0 || n_tokens <= 0 || topk <= 0) return kStatusBytes;
   return prefill_min_workspace(n_tokens, topk) +
          (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(prefix_len + n_tokens) : 0) +
-         indexer_group_cand_bytes(n_tokens, n_tokens, h_idx, topk);
+         indexer_group_cand_bytes(n_tokens, n_tokens, h_idx, topk,
+                                  static_cast<int32_t>(std::min<int64_t>(INT32_MAX, int64_t(prefix_len) + n_tokens)));
 }
 
 int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_table, int32_t prefix_len,

@@ -1617,8 +1617,10 @@ int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len) {
   return (max_seq_len <= cap && topk <= cap) ? tq : 0;
 }
 
-size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk) {
+size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk,
+                                int32_t max_seq_len) {
   if (indexer_split_mode(q_per_seq, h_idx) || n_rows <= 0) return 0;
+  if (indexer_dense_tokens(h_idx, topk, max_seq_len) > 0) return 0;  // dense mode keeps no candidate lists
   const int tq = indexer_tokens_per_cta(h_idx, topk, false, q_per_seq);
   if (tq <= 0) return 0;
   const size_t cap = kBufEntries / tq;
@@ -1679,7 +1681,7 @@ int launch_indexer(const IndexerLaunch& L) {
   } else {
     prm.n_groups = (L.q_per_seq + tq - 1) / tq;
     prm.n_items = L.n_seqs * prm.n_groups;
-    const size_t cand = dense ? 0 : indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk);
+    const size_t cand = indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk, L.max_seq_len);
     if (L.cand && cand > 0 && L.cand_bytes >= cand && (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
       prm.defer = 1;
       prm.cand_key = static_cast<uint32_t*>(L.cand);

@@ -89,7 +89,8 @@ int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len);
 size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
                                int32_t topk);
 // Group mode: bytes of the deferred per-row candidate buffers (0 if split mode).
-size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk);
+size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk,
+                                int32_t max_seq_len);
 
 int launch_indexer(const IndexerLaunch& L);   // returns smla_status
 int launch_mla(const MlaLaunch& L);           // returns smla_status

@@ -90,17 +90,21 @@ def test_decode_and_indexer_argument_checks(L):
 
 
 def test_workspace_sizes(L):
-    # prefill keeps the index list (status word + T x topk int32) and room for the
-    # candidate buffers of rows whose final selection is deferred: 4 query rows per
-    # indexer work item at 32 heads share 16384 entries, so 4096 (key, index) pairs
-    # per row, plus one count per row
-    cand = 16384 * 4096 * 8 + 16384 * 4
-    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4 + cand
+    # prefill keeps the index list (status word + T x topk int32); rows of at most
+    # 16384 keys are selected from full score rows in shared memory, so nothing more
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4
     # a BF16 cache adds an f16 copy of the sequence's rows (576 values x 2 bytes per key)
     assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 0) == \
-        256 + 16384 * 2048 * 4 + 16384 * 576 * 2 + cand
-    # the indexer alone: status word + the same candidate buffers
-    assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256 + cand
+        256 + 16384 * 2048 * 4 + 16384 * 576 * 2
+    # longer rows: room for the candidate buffers of rows whose final selection is
+    # deferred: 4 query rows per indexer work item at 32 heads share 16384 entries,
+    # so 4096 (key, index) pairs per row, plus one count per row
+    T, P = 8192, 20000
+    cand = T * 4096 * 8 + T * 4
+    assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 1) == 256 + T * 2048 * 4 + cand
+    # the indexer alone: status word (+ the same candidate buffers for long rows)
+    assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256
+    assert L.smla_indexer_topk_workspace_size(1, P + T, T, 32, 2048) == 256 + cand
     # decode: a score per (row, key) up to max_seq_len, the index list, then
     # room for the fp32 partial outputs (and lse) of rows split into up to 4 parts
     rows, k = 128, 2048
