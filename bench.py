@@ -39,6 +39,7 @@ METRIC = "query tokens/s per layer (indexer+top-k+sparse MLA)"
 UNIT = "tokens/s"
 WORKLOAD = "prefill16k"
 L2_FLUSH_BYTES = 256 << 20
+E2E_CHUNK = 2048  # query tokens per host-buffer chunk in the e2e measurement
 
 
 def peaks():
@@ -212,25 +213,21 @@ def run_reference(args, rank, world):
 
 
 def run_e2e(args, spec, dev, out, lse, stream, world):
-    """Same step through smla_sparse_mla_prefill with host inputs/outputs: every
-    step copies q, q_I and w from pinned host memory and reads out and lse back."""
+    """Same step from pinned HOST buffers through the package's host-buffer
+    prefill (smla_sparse_mla_prefill per chunk of E2E_CHUNK query tokens): every
+    step copies q, q_I and w in and reads out and lse back, the copies of one
+    chunk overlapping the kernels of the others."""
     T, H, k, P = spec.n_tokens, spec.n_heads, spec.topk, spec.prefix_len
     q_h = dev.q.cpu().pin_memory()
     qi_h = dev.q_idx.cpu().pin_memory()
     w_h = dev.w.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, qi_d, w_d = torch.empty_like(dev.q), torch.empty_like(dev.q_idx), torch.empty_like(dev.w)
-    ws_p = smla.workspace(smla.prefill_workspace_bytes(P, T, H, spec.h_idx, k, spec.kv_dtype))
+    hp = smla.HostPrefill(dev.cache, dev.page_table, P, T, H, spec.h_idx, spec.d_idx, spec.idx_dtype, k,
+                          spec.sm_scale, chunk=E2E_CHUNK)
 
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        qi_d.copy_(qi_h, non_blocking=True)
-        w_d.copy_(w_h, non_blocking=True)
-        smla.sparse_mla_prefill(dev.cache, dev.page_table, P, q_d, qi_d, w_d, k, spec.sm_scale, out=out,
-                                lse=lse, ws=ws_p)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        hp.run(q_h, qi_h, w_h, out_h, lse_h, stream=stream)
 
     for _ in range(3):
         e2e_step()
@@ -243,7 +240,9 @@ def run_e2e(args, spec, dev, out, lse, stream, world):
         e2e_step()
     e_e.record(stream)
     torch.cuda.synchronize()
-    assert smla.read_status(ws_p)[0] == 0
+    assert smla.read_status(hp.ws)[0] == 0
+    # the host copy of the result is the device result
+    assert torch.equal(out_h.view(torch.int16), hp.out.cpu().view(torch.int16))
     ms_e2e = reduce_max(e_s.elapsed_time(e_e) / n_e2e, world)
     h2d = q_h.numel() * q_h.element_size() + qi_h.numel() * qi_h.element_size() + w_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
@@ -443,7 +442,8 @@ def main():
         "e2e": {"value": world * T / (ms_e2e / 1e3) if ms_e2e == ms_e2e else None, "unit": UNIT,
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse"},
+                "path": f"pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse, pipelined in "
+                        f"chunks of {E2E_CHUNK} query tokens (HostPrefill)"},
         # per step: indexer_kernel, shadow_convert_kernel (BF16 cache only), mla_kernel
         "gpu_launches": (3 if spec.kv_dtype == "bf16" else 2) * args.steps,
         "decode": decode,

@@ -236,6 +236,65 @@ def sparse_mla_prefill(cache, page_table, prefix_len, q, q_idx, w, topk, sm_scal
     return out, lse, out_idx, ws
 
 
+class HostPrefill:
+    """Prefill from pinned HOST buffers: q, q_idx and w are copied in and out /
+    lse copied back chunk by chunk, on two copy streams, so the copies of one
+    chunk overlap the kernels of its neighbours. Each chunk of query tokens is
+    one smla_sparse_mla_prefill call with the earlier tokens as its prefix (the
+    cache already holds every token's rows), which gives the same rows the
+    single call would. Device buffers, workspace, streams and events are made
+    once here; run() may be called repeatedly (each call waits for the
+    previous call's use of a chunk's device buffers before reusing them).
+    """
+
+    def __init__(self, cache, page_table, prefix_len, n_tokens, n_heads, h_idx, d_idx, idx_dtype, topk,
+                 sm_scale, chunk=2048, device="cuda"):
+        self.cache, self.page_table, self.prefix_len = cache, page_table, prefix_len
+        self.T, self.topk, self.sm_scale = n_tokens, topk, sm_scale
+        self.chunks = [(a, min(n_tokens, a + chunk)) for a in range(0, n_tokens, chunk)]
+        idx_t = torch.bfloat16 if idx_dtype == "bf16" else torch.uint8
+        self.q = torch.empty((n_tokens, n_heads, D_QK), dtype=torch.bfloat16, device=device)
+        self.q_idx = torch.empty((n_tokens, h_idx, d_idx), dtype=idx_t, device=device)
+        self.w = torch.empty((n_tokens, h_idx), dtype=torch.float32, device=device)
+        self.out = torch.empty((n_tokens, n_heads, D_V), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((n_tokens, n_heads), dtype=torch.float32, device=device)
+        last = self.chunks[-1]
+        self.ws = workspace(prefill_workspace_bytes(prefix_len + last[0], last[1] - last[0], n_heads, h_idx, topk,
+                                                    cache.kv_dtype), device)
+        self.s_in, self.s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        n = len(self.chunks)
+        self.ev_in = [torch.cuda.Event() for _ in range(n)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(n)]
+        self.ev_out = [torch.cuda.Event() for _ in range(n)]
+
+    def run(self, q_h, q_idx_h, w_h, out_h, lse_h, stream=None):
+        comp = torch.cuda.current_stream() if stream is None else stream
+        start = torch.cuda.Event()
+        start.record(comp)
+        self.s_in.wait_event(start)
+        self.s_out.wait_event(start)
+        for c, (a, b) in enumerate(self.chunks):
+            with torch.cuda.stream(self.s_in):
+                self.s_in.wait_event(self.ev_comp[c])  # the previous run's kernels read these inputs
+                self.q[a:b].copy_(q_h[a:b], non_blocking=True)
+                self.q_idx[a:b].copy_(q_idx_h[a:b], non_blocking=True)
+                self.w[a:b].copy_(w_h[a:b], non_blocking=True)
+                self.ev_in[c].record(self.s_in)
+            comp.wait_event(self.ev_in[c])
+            comp.wait_event(self.ev_out[c])  # the previous run's copy-out of these outputs
+            sparse_mla_prefill(self.cache, self.page_table, self.prefix_len + a, self.q[a:b], self.q_idx[a:b],
+                               self.w[a:b], self.topk, self.sm_scale, out=self.out[a:b], lse=self.lse[a:b],
+                               ws=self.ws, stream=comp)
+            self.ev_comp[c].record(comp)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(self.ev_comp[c])
+                out_h[a:b].copy_(self.out[a:b], non_blocking=True)
+                lse_h[a:b].copy_(self.lse[a:b], non_blocking=True)
+                self.ev_out[c].record(self.s_out)
+        for c in range(len(self.chunks)):
+            comp.wait_event(self.ev_out[c])  # the call ends on `stream` once every result is on the host
+
+
 def decode_workspace_bytes(n_seqs, max_seq_len, q_per_seq, n_heads, h_idx, topk) -> int:
     return lib().smla_sparse_mla_decode_workspace_size(n_seqs, max_seq_len, q_per_seq, n_heads, h_idx, topk)
 

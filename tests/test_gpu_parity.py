@@ -256,3 +256,29 @@ def test_decode_indexer_heavy_ties(mode):
     compare_idx(_host(gidx), ridx)
     if mode == "constant":
         assert (np.sort(_host(gidx), axis=1) == np.arange(spec.topk)[None, :]).all()
+
+
+def test_host_prefill_chunks_match_single_call():
+    """The host-buffer prefill (chunks of query tokens, each one prefill call with
+    the earlier tokens as its prefix, the copies overlapped on two streams) returns
+    exactly what one device call returns, on two runs in a row (the second reuses
+    every device buffer), and its rows match the oracle."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=3000, prefix_len=500, shuffled=True)
+    dev = wl.make(spec, "cuda")
+    _, out, lse = run_prefill(dev, want_idx=False)
+    hp = smla.HostPrefill(dev.cache, dev.page_table, spec.prefix_len, spec.n_tokens, spec.n_heads, spec.h_idx,
+                          spec.d_idx, spec.idx_dtype, spec.topk, spec.sm_scale, chunk=1024)
+    q_h, qi_h, w_h = dev.q.cpu().pin_memory(), dev.q_idx.cpu().pin_memory(), dev.w.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    for _ in range(2):
+        out_h.fill_(float("nan"))
+        lse_h.fill_(float("nan"))
+        hp.run(q_h, qi_h, w_h, out_h, lse_h)
+        torch.cuda.synchronize()
+        assert smla.read_status(hp.ws)[0] == 0
+        assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
+        assert torch.equal(lse_h, lse.cpu())
+    rows = stratified_rows(spec.prefix_len, spec.n_tokens, spec.topk, extra=(1023, 1024, 2047, 2048), n_random=6)
+    _, _, rout, rlse, _ = sampled_oracle(dev, rows)
+    compare_out(out_h.float().numpy()[rows], rout, lse_h.numpy()[rows], rlse, spec.kv_dtype)
