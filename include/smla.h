@@ -70,7 +70,14 @@ typedef enum smla_dtype {
  *               NULL for 1 (footnote 3's 132-byte key = 128 FP8 + 4-byte scale).
  * page_size must be 64 and num_pages at most 2^25 (pool rows are indexed
  * with 32-bit integers; more is SMLA_ERR_UNSUPPORTED). An indexer row must be
- * 128 bytes: d_idx = 128 for e4m3 keys, d_idx = 64 for bf16 keys. */
+ * 128 bytes: d_idx = 128 for e4m3 keys, d_idx = 64 for bf16 keys.
+ * Host-resident latent cache ("Hybrid HiSparse": the KV of contexts too long
+ * for HBM kept in host memory): kv and kv_scale may point to page-locked host
+ * memory allocated or registered with CUDA (device-accessible through unified
+ * addressing). The attention then reads only the selected rows, over the
+ * host link, with the same results; k_idx, k_idx_scale, the page tables and
+ * every other buffer must be device memory (the indexer streams its keys with
+ * the tensor-memory accelerator). */
 typedef struct smla_paged_cache {
   const void* kv;
   const float* kv_scale;

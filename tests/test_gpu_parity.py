@@ -282,3 +282,28 @@ def test_host_prefill_chunks_match_single_call():
     rows = stratified_rows(spec.prefix_len, spec.n_tokens, spec.topk, extra=(1023, 1024, 2047, 2048), n_random=6)
     _, _, rout, rlse, _ = sampled_oracle(dev, rows)
     compare_out(out_h.float().numpy()[rows], rout, lse_h.numpy()[rows], rlse, spec.kv_dtype)
+
+
+def test_decode_host_resident_kv():
+    """Decode with the latent cache (rows and FP8 scales) in page-locked host memory:
+    the attention gathers the selected rows over the host link and returns exactly
+    what the device-resident cache gives; sampled rows also match the oracle."""
+    spec = wl.scaled(wl.SPECS["decode"], n_seqs=8, len_min=3000, len_max=20000, seed=77)
+    prob = wl.make(spec, "cpu")
+    dev = prob.to("cuda")
+    lens = dev.seq_lens
+    max_len = int(lens.max().item())
+    args = (dev.page_table, lens, max_len, spec.q_per_seq, dev.q, dev.q_idx, dev.w, spec.topk, spec.sm_scale)
+    ref_out, ref_lse, *_ = smla.sparse_mla_decode(dev.cache, *args)
+    host_cache = wl.Cache(prob.cache.kv.pin_memory(), prob.cache.kv_scale.pin_memory(), dev.cache.k_idx,
+                          dev.cache.k_idx_scale, spec.kv_dtype, spec.idx_dtype)
+    for _ in range(2):
+        out, lse, _, ws = smla.sparse_mla_decode(host_cache, *args)
+        assert smla.read_status(ws)[0] == 0
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse, ref_lse)
+    rows = np.arange(0, spec.n_seqs * spec.q_per_seq, 3)
+    ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(rows)
+    assert not bad.any()
+    compare_out(_host(out[torch.as_tensor(rows, device="cuda")].float()), rout,
+                _host(lse[torch.as_tensor(rows, device="cuda")]), rlse, spec.kv_dtype)
