@@ -16,6 +16,9 @@ synthetic tensors stand in for them.
 Value recipe (one seed per workload):
   * latent q and BF16 KV: N(0,1) drawn in fp32, rounded to bf16 (RNE);
   * FP8 KV: N(0,1) per token, scale = amax/448, e4m3 with RNE (torch cast);
+  * fp8_ds_mla KV (the 656-byte row size of the pages' footnote 1): N(0,1)
+    per token; the 512 latent values quantised to e4m3 in four tiles of 128,
+    each with scale = tile amax/448; the 64 rope values rounded to bf16;
   * indexer q_I / k_I: integers uniform in [-4, 4] (exact in e4m3 and bf16);
   * head weights w: integers uniform in [1, 4] stored as fp32;
   * decode context lengths uniform in [8192, 131072]; pages of every
@@ -35,6 +38,8 @@ PAGE = 64   # tokens per page
 
 BF16 = "bf16"
 FP8 = "fp8"
+FP8_DS_MLA = "fp8_ds_mla"  # 656-byte rows: 512 e4m3 latent | 4 fp32 tile scales | 64 bf16 rope
+DS_MLA_ROW_BYTES = 656
 
 
 @dataclasses.dataclass
@@ -92,7 +97,7 @@ def scaled(spec: Spec, **overrides) -> Spec:
 @dataclasses.dataclass
 class Cache:
     """Paged latent KV pool + paged indexer-key pool (one layer)."""
-    kv: torch.Tensor                  # [pages, 64, 576] bf16, or uint8 (e4m3 bits)
+    kv: torch.Tensor                  # [pages, 64, 576] bf16 or uint8 (e4m3 bits); fp8_ds_mla [pages, 64, 656] uint8
     kv_scale: Optional[torch.Tensor]  # [pages, 64] fp32 (FP8 only)
     k_idx: torch.Tensor               # [pages, 64, d_idx] bf16, or uint8 (e4m3 bits)
     k_idx_scale: Optional[torch.Tensor]
@@ -175,11 +180,31 @@ def _int_uniform(shape, lo, hi, g, device, dtype):
     raise ValueError(dtype)
 
 
+def _ds_mla_rows(n_rows: int, g, device, chunk_rows=1 << 16) -> torch.Tensor:
+    """656-byte rows: bytes 0..511 the e4m3 codes of the 512 latent values,
+    512..527 four fp32 scales (one per 128-value tile, amax/448), 528..655 the 64
+    rope values in bf16; all drawn N(0,1)."""
+    out = torch.empty((n_rows, DS_MLA_ROW_BYTES), dtype=torch.uint8, device=device)
+    for s in range(0, n_rows, chunk_rows):
+        e = min(n_rows, s + chunk_rows)
+        x = torch.randn((e - s, D_QK), generator=g, device=device, dtype=torch.float32)
+        lat = x[:, :D_V].reshape(e - s, 4, 128)
+        sc = (lat.abs().amax(dim=2).clamp_min(1e-12) / 448.0)
+        codes = (lat / sc[:, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[s:e, :D_V] = codes.reshape(e - s, D_V)
+        out[s:e, D_V:D_V + 16] = sc.contiguous().view(torch.uint8)
+        out[s:e, D_V + 16:] = x[:, D_V:].to(torch.bfloat16).contiguous().view(torch.uint8)
+    return out
+
+
 def make_cache(spec: Spec, n_tokens_total: int, g, device, pool_pages: Optional[int] = None) -> Cache:
     pages = pool_pages if pool_pages is not None else -(-n_tokens_total // PAGE)
     rows = pages * PAGE
     if spec.kv_dtype == BF16:
         kv = _normal_bf16((pages, PAGE, D_QK), g, device)
+        kv_scale = None
+    elif spec.kv_dtype == FP8_DS_MLA:
+        kv = _ds_mla_rows(rows, g, device).view(pages, PAGE, DS_MLA_ROW_BYTES)
         kv_scale = None
     else:
         codes, sc = _fp8_rows(rows, D_QK, g, device)

@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, FP8 = 0, 1
+BF16, FP8, FP8_DS_MLA = 0, 1, 2
 D_QK, D_V = 576, 512
 
 
@@ -118,7 +118,7 @@ class Oracle:
         self.c = _Problem(
             kv=_ptr(c.kv), kv_scale=_ptr(c.kv_scale), k_idx=_ptr(c.k_idx),
             k_idx_scale=_ptr(c.k_idx_scale),
-            kv_dtype=BF16 if c.kv_dtype == "bf16" else FP8,
+            kv_dtype={"bf16": BF16, "fp8": FP8, "fp8_ds_mla": FP8_DS_MLA}[c.kv_dtype],
             idx_dtype=BF16 if c.idx_dtype == "bf16" else FP8,
             d_idx=spec.d_idx, page_size=c.kv.shape[1], num_pages=c.kv.shape[0],
             q=_ptr(prob.q), q_idx=_ptr(prob.q_idx), w=_ptr(prob.w),

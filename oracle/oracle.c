@@ -27,7 +27,10 @@
  *        p_j   = exp(l_j - max l) / sum_j exp(l_j - max l)
  *        out_h = sum_j p_j * K[s_j, 0:512]
  *        lse_h = max l + ln sum_j exp(l_j - max l)
- *     in fp64, with K dequantised as float(e4m3) * per-token scale for FP8.
+ *     in fp64, with K dequantised as float(e4m3) * per-token scale for FP8,
+ *     and for the 656-byte tile-scaled FP8 row (footnote 1's fp8_ds_mla size)
+ *     as float(e4m3) * the scale of the value's 128-value tile for the 512
+ *     latent values and float(bf16) for the 64 rope values.
  *
  * Readings where the pages are silent: the diagonal is included, ties go to
  * the lower index, V is the first 512 values of the same row, lse uses the
@@ -43,6 +46,8 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_FP8 1
+#define ORACLE_FP8_DS_MLA 2  /* 656-byte row: 512 e4m3 | 4 fp32 tile scales | 64 bf16 rope */
+#define DS_MLA_ROW_BYTES 656
 
 #define D_QK 576
 #define D_V 512
@@ -125,8 +130,24 @@ static float idx_elem(const void *base, int dtype, int64_t i) {
     return e4m3_table[((const uint8_t *)base)[i]];
 }
 
-/* Row `prow` of the latent cache as fp64 values (FP8: e4m3 value * token scale). */
+/* Row `prow` of the latent cache as fp64 values (FP8: e4m3 value * token
+ * scale; tile-scaled FP8: byte d < 512 is the e4m3 code of latent value d,
+ * bytes 512 + 4t .. 515 + 4t the little-endian fp32 scale of values
+ * 128t .. 128t + 127, bytes 528 + 2r, 529 + 2r the bf16 rope value r). */
 static void kv_row(const oracle_problem *p, int64_t prow, double *dst) {
+    if (p->kv_dtype == ORACLE_FP8_DS_MLA) {
+        const uint8_t *row = (const uint8_t *)p->kv + prow * DS_MLA_ROW_BYTES;
+        for (int d = 0; d < D_V; ++d) {
+            float scale;
+            memcpy(&scale, row + D_V + 4 * (d / 128), sizeof scale);
+            dst[d] = (double)e4m3_table[row[d]] * (double)scale;
+        }
+        for (int r = 0; r < D_QK - D_V; ++r) {
+            const uint8_t *b = row + D_V + 16 + 2 * r;
+            dst[D_V + r] = (double)oracle_bf16_to_float((uint16_t)(b[0] | (b[1] << 8)));
+        }
+        return;
+    }
     for (int d = 0; d < D_QK; ++d) {
         int64_t i = prow * D_QK + d;
         if (p->kv_dtype == ORACLE_BF16) dst[d] = (double)oracle_bf16_to_float(((const uint16_t *)p->kv)[i]);

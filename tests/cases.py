@@ -37,6 +37,10 @@ def custom_prefill(q_idx, w, k_idx, *, n_heads=2, q=None, kv=None, kv_dtype="bf1
         kvp = torch.zeros(rows, wl.D_QK, dtype=torch.bfloat16)
         kvp[:N] = torch.as_tensor(kv).to(torch.bfloat16)
         kvs = None
+    elif kv_dtype == wl.FP8_DS_MLA:  # kv: packed 656-byte rows
+        kvp = torch.zeros(rows, wl.DS_MLA_ROW_BYTES, dtype=torch.uint8)
+        kvp[:N] = torch.as_tensor(kv, dtype=torch.uint8)
+        kvs = None
     else:
         kvp = torch.zeros(rows, wl.D_QK, dtype=torch.uint8)
         kvp[:N] = torch.as_tensor(kv, dtype=torch.uint8)
@@ -55,7 +59,7 @@ def custom_prefill(q_idx, w, k_idx, *, n_heads=2, q=None, kv=None, kv_dtype="bf1
         kis[:N] = torch.as_tensor(k_idx_scale, dtype=torch.float32)
         kis = kis.view(pages, wl.PAGE)
     pt = torch.arange(pages, dtype=torch.int32)
-    kvp = kvp.view(pages, wl.PAGE, wl.D_QK)
+    kvp = kvp.view(pages, wl.PAGE, kvp.shape[-1])
     kidx = kidx.view(pages, wl.PAGE, D_I)
     if kvs is not None:
         kvs = kvs.view(pages, wl.PAGE)

@@ -310,6 +310,31 @@ def test_attention_fp8_dequantises_with_per_token_scale():
     assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
 
 
+def test_attention_fp8_ds_mla_rows_dequantise_per_tile():
+    """656-byte rows (512 e4m3 latent values, four fp32 scales each for one
+    128-value tile, 64 bf16 rope values): K[d] = float(code[d]) * scale[d // 128]
+    for d < 512 and K[512 + r] = bf16 rope value r. Equals the BF16 path fed the
+    dequantised values (chosen exact in bf16); scales differ per row and per
+    tile, so a wrong tile index, scale offset or rope offset changes the result."""
+    N = 64
+    gen = torch.Generator().manual_seed(16)
+    lat = torch.randint(-8, 9, (N, wl.D_V), generator=gen).float() / 4
+    codes = fp8_codes(lat)
+    scales = torch.tensor([[2.0 ** ((r + 3 * t) % 5 - 2) for t in range(4)] for r in range(N)])
+    rope = (torch.randint(-64, 65, (N, wl.D_QK - wl.D_V), generator=gen).float() / 16).to(torch.bfloat16)
+    rows = torch.cat([codes, scales.contiguous().view(torch.uint8), rope.contiguous().view(torch.uint8)], dim=1)
+    assert rows.shape == (N, wl.DS_MLA_ROW_BYTES)
+    deq = torch.cat([codes.view(torch.float8_e4m3fn).float() * scales.repeat_interleave(128, dim=1),
+                     rope.float()], dim=1)  # exact in bf16 here
+    gq = torch.randn(1, 4, wl.D_QK, generator=gen)
+    pd = _attn_problem(N=N, q=gq, kv=rows, kv_dtype=wl.FP8_DS_MLA)
+    pb = _attn_problem(N=N, q=gq, kv=deq)
+    idx = np.arange(0, N, dtype=np.int32)
+    od, ld, _ = oracle.Oracle(pd).attend(0, idx)
+    ob, lb, _ = oracle.Oracle(pb).attend(0, idx)
+    assert np.array_equal(od, ob) and np.array_equal(ld, lb)
+
+
 def test_attention_rejects_future_and_missing_keys():
     o = oracle.Oracle(_attn_problem(N=70))
     _, _, bad = o.attend(0, np.array([1, 2, 500], np.int32))
