@@ -57,14 +57,23 @@ typedef enum smla_status {
 
 typedef enum smla_dtype {
   SMLA_BF16 = 0,      /* bfloat16 */
-  SMLA_FP8_E4M3 = 1   /* OCP FP8 E4M3 (e4m3fn), one byte per value */
+  SMLA_FP8_E4M3 = 1,  /* OCP FP8 E4M3 (e4m3fn), one byte per value */
+  SMLA_FP8_DS_MLA = 2 /* latent cache only: 656-byte tile-scaled FP8 rows (below) */
 } smla_dtype;
 
 /* Paged cache of one layer. Token s of a sequence lives in pool page
  * page_table[s / page_size] at slot s % page_size.
  *   kv          [num_pages][page_size][576]  kv_dtype. The latent row: values
  *               0..511 are the latent (also V), 512..575 the rope part.
- *   kv_scale    [num_pages][page_size] fp32, FP8 only: value = e4m3 * scale.
+ *               For SMLA_FP8_DS_MLA each row is 656 bytes (the row size that
+ *               footnote 1 of "Optimisations de GLM-5.3, partie 2" gives for
+ *               fp8_ds_mla; the split is this library's reading): bytes 0..511
+ *               the e4m3 codes of latent values 0..511, bytes 512..527 four
+ *               little-endian fp32 scales (scale t for values 128t..128t+127,
+ *               value = e4m3 * scale), bytes 528..655 the 64 rope values in
+ *               bf16. kv_scale is not used.
+ *   kv_scale    [num_pages][page_size] fp32, SMLA_FP8_E4M3 only: value = e4m3
+ *               * scale.
  *   k_idx       [num_pages][page_size][d_idx] idx_dtype: indexer keys.
  *   k_idx_scale [num_pages][page_size] fp32 positive per-key indexer scale, or
  *               NULL for 1 (footnote 3's 132-byte key = 128 FP8 + 4-byte scale).

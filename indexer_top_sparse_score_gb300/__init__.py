@@ -26,7 +26,7 @@ SOURCES = ["api.cu", "indexer.cu", "mla.cu", "noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 
-SMLA_BF16, SMLA_FP8_E4M3 = 0, 1
+SMLA_BF16, SMLA_FP8_E4M3, SMLA_FP8_DS_MLA = 0, 1, 2
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_WORKSPACE",
           4: "SMLA_ERR_CUDA", 5: "SMLA_ERR_DEVICE_BOUNDS", 6: "SMLA_ERR_TIMEOUT"}
 D_QK, D_V, PAGE = 576, 512, 64
@@ -139,7 +139,7 @@ def _check(rc: int, what: str):
 
 
 def _dtype_code(name: str) -> int:
-    return SMLA_BF16 if name == "bf16" else SMLA_FP8_E4M3
+    return {"bf16": SMLA_BF16, "fp8": SMLA_FP8_E4M3, "fp8_ds_mla": SMLA_FP8_DS_MLA}[name]
 
 
 def make_cache(cache) -> PagedCache:

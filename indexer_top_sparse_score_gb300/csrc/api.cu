@@ -41,7 +41,8 @@ int check_cache(const smla_paged_cache* c, bool need_kv, bool need_idx) {
   if (c->num_pages > (1 << 25)) return SMLA_ERR_UNSUPPORTED;  // pool rows must fit int32
   if (need_kv) {
     if (!c->kv || !aligned16(c->kv)) return SMLA_ERR_INVALID_ARG;
-    if (c->kv_dtype != SMLA_BF16 && c->kv_dtype != SMLA_FP8_E4M3) return SMLA_ERR_INVALID_ARG;
+    if (c->kv_dtype != SMLA_BF16 && c->kv_dtype != SMLA_FP8_E4M3 && c->kv_dtype != SMLA_FP8_DS_MLA)
+      return SMLA_ERR_INVALID_ARG;
     if (c->kv_dtype == SMLA_FP8_E4M3 && !c->kv_scale) return SMLA_ERR_INVALID_ARG;
   }
   if (need_idx) {

@@ -57,6 +57,10 @@ constexpr int kThreads = 512;
 constexpr int kProducers = 128;                    // warps 12-15
 constexpr uint32_t kColO = 0, kColS = 256, kColL = 320, kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+// latent cache formats: bf16 rows, e4m3 rows with one fp32 scale per token
+// (separate array), 656-byte rows of e4m3 with four fp32 tile scales + bf16 rope
+constexpr int kFmtBf16 = 0, kFmtTokenFp8 = 1, kFmtTileFp8 = 2;
+constexpr int kTileRowBytes = 656, kTileScaleOff = 512, kTileRopeOff = 528;
 
 struct MlaParams {
   const uint8_t* kv;
@@ -72,7 +76,7 @@ struct MlaParams {
   float scale_log2;  // sm_scale * log2(e)
   uint16_t* out;
   float* lse;
-  int32_t fp8;
+  int32_t fmt;  // latent cache format: kFmtBf16, kFmtTokenFp8 or kFmtTileFp8
   uint32_t* status;
   const uint16_t* shadow;  // f16 rows by logical position, or null
   int32_t shadow_rows;
@@ -241,7 +245,9 @@ __device__ __forceinline__ uint32_t sw_off(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
-template <int H>
+// TILE: 656-byte tile-scaled FP8 rows (a separate instance, so the bf16 and
+// per-token FP8 gathers compile as without it)
+template <int H, bool TILE>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const MlaParams p) {
   static_assert(H == 16 || H == 64, "heads");
@@ -447,10 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int key1 = fetch_key(1), key2 = fetch_key(2);
       int loc = locate(key0, fetch_page(key0));
       int pg1 = fetch_page(key1);
-      const uint32_t row_bytes = p.fp8 ? kDqk : 2 * kDqk;
+      const uint32_t row_bytes = TILE ? kTileRowBytes : p.fmt == kFmtTokenFp8 ? kDqk : 2 * kDqk;
       for (int b = 0; b < ri.nb && ok; ++b, ++g) {
         float ks = 1.0f;
-        if (p.fp8 && loc >= 0) ks = __ldg(p.kv_scale + loc);
+        if (!TILE && p.fmt == kFmtTokenFp8 && loc >= 0) ks = __ldg(p.kv_scale + loc);
         const int key3 = fetch_key(b + 3);
         const int loc1 = locate(key1, pg1);
         if (!p.shadow && loc1 >= 0) prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
@@ -460,7 +466,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           M.row[g & 1][32 * pw + lane] =
               loc >= 0 ? make_float4(ks * p.scale_log2, ks, 1.0f, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
         };
-        if (p.shadow) {
+        if constexpr (TILE) {
+          // 656-byte rows. Units 0-7: latent chunk u, lane l takes 16 bytes
+          // (q = l & 3) of row 32pw + (l >> 2) + 8i in pass i (as the per-token
+          // path) with the scale of the chunk's 128-value tile, and widens them
+          // times that scale; units 8 and 9: the bf16 rope of rows 32pw + 16h +
+          // (l >> 3) + 4i, lane piece l & 7 (as the bf16 path). Unit u+1 is in
+          // flight while unit u is stored.
+          const int rs8 = lane >> 2, q4 = lane & 3;
+          int rl8[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rl8[i] = __shfl_sync(0xFFFFFFFFu, loc, rs8 + 8 * i);
+          uint4 stt[2][4];
+          float scl[2][4];
+          auto loadt = [&](int u, int slot) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = u < 8 ? rl8[i] : __shfl_sync(0xFFFFFFFFu, loc, 16 * (u - 8) + psub + 4 * i);
+              const uint8_t* row = p.kv + static_cast<int64_t>(r < 0 ? 0 : r) * kTileRowBytes;
+              stt[slot][i] = r < 0 ? make_uint4(0, 0, 0, 0) : ldg_stream(row + (u < 8 ? u * 64 + q4 * 16 : kTileRopeOff + pj * 16));
+              if (u < 8) scl[slot][i] = r < 0 ? 0.0f : __ldg(reinterpret_cast<const float*>(row + kTileScaleOff) + (u >> 1));
+            }
+          };
+          auto widen = [&](uint16_t v, float sc) -> uint32_t {
+            const uint32_t hv = e4m3x2_to_f16x2(v);  // exact
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+            const float a = f.x * sc, b = f.y * sc;
+            over |= fabsf(a) > 65504.0f || fabsf(b) > 65504.0f;
+            return pack_f16(a, b);
+          };
+          loadt(0, 0);
+#pragma unroll
+          for (int u = 0; u < 10; ++u) {
+            const int c = u < 8 ? u : 8;
+            const int grp = c < 8 ? c >> 1 : 4;
+            if (u + 1 < 10) loadt(u + 1, (u + 1) & 1);
+            if (((u < 8 && (u & 1) == 0) || u == 8) &&
+                !mbar_wait(&M.empty[grp < 4 ? grp : 3], ph_e, abort_v, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* cp = stage + c * kChunkBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 w = stt[u & 1][i];
+              if (u < 8) {
+                const float sc = scl[u & 1][i];
+                const int rw = 32 * pw + rs8 + 8 * i;
+                *reinterpret_cast<uint4*>(cp + sw_off(rw, 2 * q4)) =
+                    make_uint4(widen(static_cast<uint16_t>(w.x & 0xFFFFu), sc), widen(static_cast<uint16_t>(w.x >> 16), sc),
+                               widen(static_cast<uint16_t>(w.y & 0xFFFFu), sc), widen(static_cast<uint16_t>(w.y >> 16), sc));
+                *reinterpret_cast<uint4*>(cp + sw_off(rw, 2 * q4 + 1)) =
+                    make_uint4(widen(static_cast<uint16_t>(w.z & 0xFFFFu), sc), widen(static_cast<uint16_t>(w.z >> 16), sc),
+                               widen(static_cast<uint16_t>(w.w & 0xFFFFu), sc), widen(static_cast<uint16_t>(w.w >> 16), sc));
+              } else {
+                over |= bf16x2_over_f16(w.x) | bf16x2_over_f16(w.y) | bf16x2_over_f16(w.z) | bf16x2_over_f16(w.w);
+                *reinterpret_cast<uint4*>(cp + sw_off(32 * pw + 16 * (u - 8) + psub + 4 * i, pj)) =
+                    make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+              }
+            }
+            if ((u < 8 && (u & 1) == 1) || u == 9) {
+              if (u == 9) meta();
+              fence_proxy_async_smem();
+              mbar_arrive(&M.full[grp]);
+            }
+          }
+        } else if (p.shadow) {
           int rl[8];  // pool rows of this lane's copy passes
 #pragma unroll
           for (int i = 0; i < 8; ++i) rl[i] = __shfl_sync(0xFFFFFFFFu, loc, psub + 4 * i);
@@ -488,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           meta();
           fence_proxy_async_smem();
           mbar_arrive(&M.full[kGroups - 1]);
-        } else if (p.fp8) {
+        } else if (p.fmt == kFmtTokenFp8) {
           // e4m3 rows: one chunk (64 values = 64 bytes per row) per unit; lane l
           // takes 16 bytes (q = l & 3) of row 32pw + (l >> 2) + 8i in pass i and
           // widens them into f16 pieces 2q and 2q+1; units u+1 and u+2 are in
@@ -855,17 +926,17 @@ __global__ void __launch_bounds__(256) part_merge_kernel(const float* __restrict
   }
 }
 
-template <int H>
+template <int H, bool TILE>
 int launch_t(const MlaLaunch& L, const MlaParams& prm) {
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(mla_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mla_kernel<H, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     attr_done = true;
   }
   const int grid = std::max(1, std::min(num_sms(), (prm.n_rows * prm.n_parts + 1) / 2));
-  mla_kernel<H><<<grid, kThreads, kSmemBytes, L.stream>>>(prm);
+  mla_kernel<H, TILE><<<grid, kThreads, kSmemBytes, L.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   if (prm.n_parts > 1) {
     part_merge_kernel<<<dim3(prm.n_rows, (H + kMergeHeads - 1) / kMergeHeads), 256, 0, L.stream>>>(
@@ -960,7 +1031,7 @@ int launch_mla(const MlaLaunch& L) {
   prm.scale_log2 = L.sm_scale * 1.4426950408889634f;
   prm.out = static_cast<uint16_t*>(L.out);
   prm.lse = L.lse;
-  prm.fp8 = L.cache->kv_dtype == SMLA_FP8_E4M3;
+  prm.fmt = L.cache->kv_dtype == SMLA_FP8_E4M3 ? kFmtTokenFp8 : L.cache->kv_dtype == SMLA_FP8_DS_MLA ? kFmtTileFp8 : kFmtBf16;
   prm.status = L.status;
   prm.shadow = static_cast<const uint16_t*>(L.shadow);
   prm.shadow_rows = L.shadow_rows;
@@ -977,8 +1048,8 @@ int launch_mla(const MlaLaunch& L) {
     prm.part_lse = prm.part_o + static_cast<size_t>(prm.n_rows) * kMaxParts * L.n_heads * kDv;
   }
   switch (L.n_heads) {
-    case 16: return launch_t<16>(L, prm);
-    case 64: return launch_t<64>(L, prm);
+    case 16: return prm.fmt == kFmtTileFp8 ? launch_t<16, true>(L, prm) : launch_t<16, false>(L, prm);
+    case 64: return prm.fmt == kFmtTileFp8 ? launch_t<64, true>(L, prm) : launch_t<64, false>(L, prm);
     default: return SMLA_ERR_UNSUPPORTED;
   }
 }

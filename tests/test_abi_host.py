@@ -65,6 +65,10 @@ def test_prefill_argument_checks(L):
     assert _prefill(L, _cache(d_idx=64)) == UNSUPPORTED             # e4m3 x 64 = 64-byte rows
     assert _prefill(L, _cache(kv_scale=None)) == INVALID            # FP8 needs scales
     assert _prefill(L, _cache(kv_dtype=7)) == INVALID
+    # the 656-byte tile-scaled FP8 rows carry their scales: no scale array needed,
+    # and the format is for the latent cache only (not the indexer keys)
+    assert _prefill(L, _cache(kv_dtype=smla.SMLA_FP8_DS_MLA, kv_scale=None), H=32) == UNSUPPORTED  # cache ok
+    assert _prefill(L, _cache(kv_dtype=smla.SMLA_FP8_DS_MLA, idx_dtype=smla.SMLA_FP8_DS_MLA)) == INVALID
     assert _prefill(L, _cache(), H=32) == UNSUPPORTED
     assert _prefill(L, _cache(), h_idx=12) == UNSUPPORTED
     assert _prefill(L, _cache(), topk=4096) == UNSUPPORTED

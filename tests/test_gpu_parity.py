@@ -307,3 +307,36 @@ def test_decode_host_resident_kv():
     assert not bad.any()
     compare_out(_host(out[torch.as_tensor(rows, device="cuda")].float()), rout,
                 _host(lse[torch.as_tensor(rows, device="cuda")]), rlse, spec.kv_dtype)
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_fp8_ds_mla_rows(kind):
+    """The 656-byte tile-scaled FP8 latent rows (512 e4m3 values with one fp32
+    scale per 128, 64 bf16 rope values): a ragged prefill after a prefix and a
+    decode batch in shuffled pools; index sets exact, outputs within the FP8
+    tolerance of the oracle, which dequantises the same bytes."""
+    if kind == "prefill":
+        spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=1200, prefix_len=2500, shuffled=True,
+                         kv_dtype=wl.FP8_DS_MLA)
+        dev = wl.make(spec, "cuda")
+        idx, out, lse = run_prefill(dev)
+        rows = stratified_rows(spec.prefix_len, spec.n_tokens, spec.topk, n_random=10)
+        ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
+        r = torch.as_tensor(rows, device="cuda")
+        compare_idx(_host(idx[r]), ridx)
+        compare_out(_host(out[r].float()), rout, _host(lse[r]), rlse, spec.kv_dtype)
+    else:
+        spec = wl.scaled(wl.SPECS["decode"], n_seqs=10, len_min=1500, len_max=30000, seed=55,
+                         kv_dtype=wl.FP8_DS_MLA)
+        prob = wl.make(spec, "cpu")
+        dev = prob.to("cuda")
+        rows = spec.n_seqs * spec.q_per_seq
+        max_len = int(dev.seq_lens.max())
+        idx = torch.empty((rows, spec.topk), dtype=torch.int32, device="cuda")
+        out, lse, _, ws = smla.sparse_mla_decode(dev.cache, dev.page_table, dev.seq_lens, max_len, spec.q_per_seq,
+                                                 dev.q, dev.q_idx, dev.w, spec.topk, spec.sm_scale, out_idx=idx)
+        assert smla.read_status(ws)[0] == 0
+        ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(np.arange(rows))
+        assert not bad.any()
+        compare_idx(_host(idx), ridx)
+        compare_out(_host(out.float()), rout, _host(lse), rlse, spec.kv_dtype)
