@@ -39,7 +39,20 @@ METRIC = "query tokens/s per layer (indexer+top-k+sparse MLA)"
 UNIT = "tokens/s"
 WORKLOAD = "prefill16k"
 L2_FLUSH_BYTES = 256 << 20
-E2E_CHUNK = 2048  # query tokens per host-buffer chunk in the e2e measurement
+E2E_CHUNK = 2048  # query tokens per host-buffer chunk in the middle of the e2e schedule
+
+
+def e2e_chunks(T: int):
+    """Chunk sizes of the e2e measurement: E2E_CHUNK tokens, tapered at both
+    ends (256, 768, 1024, then 2048s, then 1024, 768, 256) when T allows, so the
+    copy-in before the first kernel and the copy-out after the last are short
+    (16K tokens: 9.77 ms per step against 9.97 with even 2048-token chunks, on
+    one GB300)."""
+    ends = [256, 768, 1024]
+    mid = T - 2 * sum(ends)
+    if mid <= 0 or mid % E2E_CHUNK:
+        return E2E_CHUNK
+    return ends + [E2E_CHUNK] * (mid // E2E_CHUNK) + ends[::-1]
 
 
 def peaks():
@@ -224,7 +237,7 @@ def run_e2e(args, spec, dev, out, lse, stream, world):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     hp = smla.HostPrefill(dev.cache, dev.page_table, P, T, H, spec.h_idx, spec.d_idx, spec.idx_dtype, k,
-                          spec.sm_scale, chunk=E2E_CHUNK)
+                          spec.sm_scale, chunk=e2e_chunks(T))
 
     def e2e_step():
         hp.run(q_h, qi_h, w_h, out_h, lse_h, stream=stream)
@@ -466,8 +479,8 @@ def main():
         "e2e": {"value": world * T / (ms_e2e / 1e3) if ms_e2e == ms_e2e else None, "unit": UNIT,
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                "path": f"pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse, pipelined in "
-                        f"chunks of {E2E_CHUNK} query tokens (HostPrefill)"},
+                "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse, pipelined in "
+                        f"chunks of query tokens {e2e_chunks(T)} (HostPrefill)"},
         # per step: indexer_kernel, shadow_convert_kernel (BF16 cache only), mla_kernel
         "gpu_launches": (3 if spec.kv_dtype == "bf16" else 2) * args.steps,
         "decode": decode,

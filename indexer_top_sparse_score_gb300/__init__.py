@@ -242,25 +242,37 @@ class HostPrefill:
     chunk overlap the kernels of its neighbours. Each chunk of query tokens is
     one smla_sparse_mla_prefill call with the earlier tokens as its prefix (the
     cache already holds every token's rows), which gives the same rows the
-    single call would. Device buffers, workspace, streams and events are made
-    once here; run() may be called repeatedly (each call waits for the
-    previous call's use of a chunk's device buffers before reusing them).
+    single call would. `chunk` is a chunk size, or a list of chunk sizes that
+    sum to n_tokens (small first and last chunks shorten the copy-in before
+    the first kernel and the copy-out after the last). Device buffers,
+    workspace, streams and events are made once here; run() may be called
+    repeatedly (each call waits for the previous call's use of a chunk's
+    device buffers before reusing them).
     """
 
     def __init__(self, cache, page_table, prefix_len, n_tokens, n_heads, h_idx, d_idx, idx_dtype, topk,
                  sm_scale, chunk=2048, device="cuda"):
         self.cache, self.page_table, self.prefix_len = cache, page_table, prefix_len
         self.T, self.topk, self.sm_scale = n_tokens, topk, sm_scale
-        self.chunks = [(a, min(n_tokens, a + chunk)) for a in range(0, n_tokens, chunk)]
+        if isinstance(chunk, int):
+            self.chunks = [(a, min(n_tokens, a + chunk)) for a in range(0, n_tokens, chunk)]
+        else:
+            sizes = [int(c) for c in chunk]
+            if any(c <= 0 for c in sizes) or sum(sizes) != n_tokens:
+                raise ValueError("chunk sizes must be positive and sum to n_tokens")
+            bounds = [0]
+            for c in sizes:
+                bounds.append(bounds[-1] + c)
+            self.chunks = list(zip(bounds[:-1], bounds[1:]))
         idx_t = torch.bfloat16 if idx_dtype == "bf16" else torch.uint8
         self.q = torch.empty((n_tokens, n_heads, D_QK), dtype=torch.bfloat16, device=device)
         self.q_idx = torch.empty((n_tokens, h_idx, d_idx), dtype=idx_t, device=device)
         self.w = torch.empty((n_tokens, h_idx), dtype=torch.float32, device=device)
         self.out = torch.empty((n_tokens, n_heads, D_V), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((n_tokens, n_heads), dtype=torch.float32, device=device)
-        last = self.chunks[-1]
-        self.ws = workspace(prefill_workspace_bytes(prefix_len + last[0], last[1] - last[0], n_heads, h_idx, topk,
-                                                    cache.kv_dtype), device)
+        need = max(prefill_workspace_bytes(prefix_len + a, b - a, n_heads, h_idx, topk, cache.kv_dtype)
+                   for a, b in self.chunks)
+        self.ws = workspace(need, device)
         self.s_in, self.s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
         n = len(self.chunks)
         self.ev_in = [torch.cuda.Event() for _ in range(n)]

@@ -258,7 +258,8 @@ def test_decode_indexer_heavy_ties(mode):
         assert (np.sort(_host(gidx), axis=1) == np.arange(spec.topk)[None, :]).all()
 
 
-def test_host_prefill_chunks_match_single_call():
+@pytest.mark.parametrize("chunk", [1024, [200, 800, 1000, 1000]], ids=["even", "tapered"])
+def test_host_prefill_chunks_match_single_call(chunk):
     """The host-buffer prefill (chunks of query tokens, each one prefill call with
     the earlier tokens as its prefix, the copies overlapped on two streams) returns
     exactly what one device call returns, on two runs in a row (the second reuses
@@ -267,7 +268,7 @@ def test_host_prefill_chunks_match_single_call():
     dev = wl.make(spec, "cuda")
     _, out, lse = run_prefill(dev, want_idx=False)
     hp = smla.HostPrefill(dev.cache, dev.page_table, spec.prefix_len, spec.n_tokens, spec.n_heads, spec.h_idx,
-                          spec.d_idx, spec.idx_dtype, spec.topk, spec.sm_scale, chunk=1024)
+                          spec.d_idx, spec.idx_dtype, spec.topk, spec.sm_scale, chunk=chunk)
     q_h, qi_h, w_h = dev.q.cpu().pin_memory(), dev.q_idx.cpu().pin_memory(), dev.w.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
