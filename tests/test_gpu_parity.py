@@ -341,3 +341,29 @@ def test_fp8_ds_mla_rows(kind):
         assert not bad.any()
         compare_idx(_host(idx), ridx)
         compare_out(_host(out.float()), rout, _host(lse), rlse, spec.kv_dtype)
+
+
+@pytest.mark.parametrize("prefix", [500, 17000], ids=["dense", "streaming"])
+@pytest.mark.parametrize("h_idx", [8, 16, 64])
+def test_indexer_head_counts(h_idx, prefix):
+    """Indexer heads other than the workloads' 4 and 32 (FP8 keys of 128 values):
+    rows of at most 16,384 keys take the dense group mode (at 64 heads always its
+    radix fallback: no staging room beside a 128-row query tile), longer rows the
+    streaming candidate buffers; index sets exact against the oracle."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=300, prefix_len=prefix, shuffled=True, h_idx=h_idx,
+                     topk=512)
+    prob = wl.make(spec, "cpu")
+    dev = prob.to("cuda")
+    L = spec.prefix_len + spec.n_tokens
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    gidx, gsc, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
+                                      spec.topk, want_scores=True)
+    assert smla.read_status(ws)[0] == 0
+    rows = np.arange(0, spec.n_tokens, 7)
+    ridx, rsc, *_ = oracle.Oracle(prob).rows(rows, attend=False)
+    compare_idx(_host(gidx)[rows], ridx)
+    g_i, g_s = _host(gidx)[rows], _host(gsc)[rows]
+    for r in range(len(rows)):
+        ok = g_i[r] >= 0
+        full = oracle.Oracle(prob).scores(int(rows[r]))
+        assert np.array_equal(g_s[r][ok], full[g_i[r][ok]])
