@@ -470,10 +470,13 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"{spec.name}: T={T} new tokens, prefix {P}, {H} heads, latent 576 BF16 KV, "
                                f"indexer {spec.h_idx}x{spec.d_idx} FP8, top-{k}",
-                   "indexer_dtype": "fp8(e4m3) operands, fp32 accumulate", "parallelism": f"replicas x{world}",
+                   "indexer_dtype": "fp8(e4m3) operands, fp32 accumulate",
+                   "mla_dtype": "bf16 q and cache widened exactly to f16 MMA operands, f16 P, fp32 accumulate, "
+                                "bf16 output",
+                   "parallelism": f"replicas x{world}",
                    "l2": "256 MB buffer written between timed steps", "wall_s_timed_region": wall},
         "roofline": roof, "kernels": kernels,
         "e2e": {"value": world * T / (ms_e2e / 1e3) if ms_e2e == ms_e2e else None, "unit": UNIT,
