@@ -236,6 +236,22 @@ def sparse_mla_prefill(cache, page_table, prefix_len, q, q_idx, w, topk, sm_scal
     return out, lse, out_idx, ws
 
 
+def chunk_bounds(n_tokens: int, chunk) -> list:
+    """[(start, end)] of the query-token chunks of HostPrefill: `chunk` is a size
+    (the last chunk takes the rest) or a list of sizes that sum to n_tokens."""
+    if isinstance(chunk, int):
+        if chunk <= 0:
+            raise ValueError("chunk size must be positive")
+        return [(a, min(n_tokens, a + chunk)) for a in range(0, n_tokens, chunk)]
+    sizes = [int(c) for c in chunk]
+    if any(c <= 0 for c in sizes) or sum(sizes) != n_tokens:
+        raise ValueError("chunk sizes must be positive and sum to n_tokens")
+    bounds = [0]
+    for c in sizes:
+        bounds.append(bounds[-1] + c)
+    return list(zip(bounds[:-1], bounds[1:]))
+
+
 class HostPrefill:
     """Prefill from pinned HOST buffers: q, q_idx and w are copied in and out /
     lse copied back chunk by chunk, on two copy streams, so the copies of one
@@ -254,16 +270,7 @@ class HostPrefill:
                  sm_scale, chunk=2048, device="cuda"):
         self.cache, self.page_table, self.prefix_len = cache, page_table, prefix_len
         self.T, self.topk, self.sm_scale = n_tokens, topk, sm_scale
-        if isinstance(chunk, int):
-            self.chunks = [(a, min(n_tokens, a + chunk)) for a in range(0, n_tokens, chunk)]
-        else:
-            sizes = [int(c) for c in chunk]
-            if any(c <= 0 for c in sizes) or sum(sizes) != n_tokens:
-                raise ValueError("chunk sizes must be positive and sum to n_tokens")
-            bounds = [0]
-            for c in sizes:
-                bounds.append(bounds[-1] + c)
-            self.chunks = list(zip(bounds[:-1], bounds[1:]))
+        self.chunks = chunk_bounds(n_tokens, chunk)
         idx_t = torch.bfloat16 if idx_dtype == "bf16" else torch.uint8
         self.q = torch.empty((n_tokens, n_heads, D_QK), dtype=torch.bfloat16, device=device)
         self.q_idx = torch.empty((n_tokens, h_idx, d_idx), dtype=idx_t, device=device)
