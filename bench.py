@@ -1,11 +1,18 @@
 """Throughput of the indexer -> top-k -> sparse MLA layer step on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-the fused indexer + exact top-k kernel, then the sparse-MLA kernel, for the
-16,384-token prefill workload (64 heads, 32x128 FP8 indexer, top-2048, BF16
-latent cache). Metric: query tokens per second per layer.
+One step = one pass of the whole hot path over one batch of synthetic input.
+The headline workload is the long prefill: 131,072 query tokens of one
+sequence (64 heads, 32x128 FP8 indexer, top-2048, FP8 latent cache with a
+per-token scale), processed as 8,192-token query chunks against the growing
+cache, each chunk one call of the product entry smla_sparse_mla_prefill
+(indexer + exact top-k, then sparse MLA). Metric: query tokens per second per
+layer.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smla|reference]
+
+Next to the headline the line carries a per-kernel split of the same step
+(indexer and attention timed in a separate pass), the 16,384-token prefill, the
+million-token prefix extension and the decode batch as extra keys.
 
 N > 1 is launched with torchrun: every rank runs its own replica of the
 workload on its GPU (query tokens are independent given the cache), so the
@@ -37,22 +44,10 @@ from indexer_top_sparse_score_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "query tokens/s per layer (indexer+top-k+sparse MLA)"
 UNIT = "tokens/s"
-WORKLOAD = "prefill16k"
+WORKLOAD = "prefill128k"
 L2_FLUSH_BYTES = 256 << 20
-E2E_CHUNK = 2048  # query tokens per host-buffer chunk in the middle of the e2e schedule
-
-
-def e2e_chunks(T: int):
-    """Chunk sizes of the e2e measurement: E2E_CHUNK tokens, tapered at both
-    ends (256, 768, 1024, then 2048s, then 1024, 768, 256) when T allows, so the
-    copy-in before the first kernel and the copy-out after the last are short
-    (16K tokens: 9.77 ms per step against 9.97 with even 2048-token chunks, on
-    one GB300)."""
-    ends = [256, 768, 1024]
-    mid = T - 2 * sum(ends)
-    if mid <= 0 or mid % E2E_CHUNK:
-        return E2E_CHUNK
-    return ends + [E2E_CHUNK] * (mid // E2E_CHUNK) + ends[::-1]
+# oracle rows timed for the CPU baseline (about 10-30 s of host work per workload)
+CPU_ROWS = {"prefill128k": 1600, "prefill16k": 2560, "prefix1m": 64}
 
 
 def peaks():
@@ -78,7 +73,7 @@ def kernel_sources_digest():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel, summary="dram_traffic_prefill16k.md"):
+def measured_traffic(kernel, summary):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
     when there is none or the kernel sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", summary)
@@ -156,7 +151,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, max_mhz_default=2070.0):
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
@@ -165,6 +160,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[5:9]):
@@ -173,7 +169,130 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else max_mhz_default,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def chunk_list(spec):
+    """(prefix, n_tokens) of every prefill call of one step of `spec`."""
+    step = spec.chunk if spec.chunk > 0 else spec.n_tokens
+    return [(spec.prefix_len + a, min(spec.n_tokens, a + step) - a) for a in range(0, spec.n_tokens, step)]
+
+
+class PrefillStep:
+    """One step of a prefill workload on resident device inputs: every chunk is
+    one smla_sparse_mla_prefill call (the product entry) on one workspace."""
+
+    def __init__(self, spec, dev):
+        self.spec, self.dev = spec, dev
+        T, H = spec.n_tokens, spec.n_heads
+        self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        self.chunks = chunk_list(spec)
+        need = max(smla.prefill_workspace_bytes(P, n, H, spec.h_idx, spec.topk, spec.kv_dtype)
+                   for P, n in self.chunks)
+        self.ws = smla.workspace(need)
+
+    def run(self, stream=None):
+        s, d = self.spec, self.dev
+        for P, n in self.chunks:
+            a = P - s.prefix_len
+            smla.sparse_mla_prefill(d.cache, d.page_table, P, d.q[a:a + n], d.q_idx[a:a + n], d.w[a:a + n],
+                                    s.topk, s.sm_scale, out=self.out[a:a + n], lse=self.lse[a:a + n],
+                                    ws=self.ws, stream=stream)
+
+    def launches(self):
+        """Kernels one step launches: per chunk the indexer, the deferred
+        selection (rows too long for the in-kernel selection), the f16 shadow
+        (BF16 caches) and the attention."""
+        n = 0
+        for P, T in self.chunks:
+            n += 2 + (self.spec.kv_dtype == "bf16")
+            if P + T > 16384:
+                n += 1
+        return n
+
+
+def time_steps(run, n, stream, flush):
+    """CUDA-event time (ms) of each of n calls of run(), L2 flushed before each."""
+    ev = []
+    for _ in range(n):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def stage_split(spec, dev, stream, flush, n_steps):
+    """Per-kernel split of a prefill step: every chunk as smla_indexer_topk
+    (indexer + exact top-k, the same kernels the prefill entry launches) then
+    smla_sparse_mla_fwd on its index list (with the f16 shadow for BF16
+    caches), events between them. Returns mean ms of the indexer and the
+    attention per step."""
+    H, k = spec.n_heads, spec.topk
+    chunks = chunk_list(spec)
+    nmax = max(n for _, n in chunks)
+    idx = torch.empty((nmax, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((nmax, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((nmax, H), dtype=torch.float32, device="cuda")
+    L = smla.lib()
+    ws_i = smla.workspace(max(L.smla_indexer_topk_workspace_size(1, P + n, n, spec.h_idx, k) for P, n in chunks))
+    ws_m = smla.workspace(max(L.smla_sparse_mla_fwd_workspace_size(P + n, n, H, k, smla._dtype_code(spec.kv_dtype))
+                              for P, n in chunks))
+    lens = [torch.tensor([P + n], dtype=torch.int32, device="cuda") for P, n in chunks]
+
+    def one(evs):
+        for c, (P, n) in enumerate(chunks):
+            a = P - spec.prefix_len
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            smla.indexer_topk(dev.cache, dev.page_table, lens[c], P + n, n, dev.q_idx[a:a + n], dev.w[a:a + n], k,
+                              out_idx=idx[:n], ws=ws_i, stream=stream)
+            e[1].record(stream)
+            smla.sparse_mla_fwd(dev.cache, dev.page_table, dev.q[a:a + n], idx[:n], spec.sm_scale, prefix_len=P,
+                                out=out[:n], lse=lse[:n], ws=ws_m, stream=stream)
+            e[2].record(stream)
+            evs.append(e)
+
+    one([])
+    torch.cuda.synchronize()
+    assert smla.read_status(ws_i)[0] == 0 and smla.read_status(ws_m)[0] == 0
+    t_idx, t_mla = [], []
+    for _ in range(n_steps):
+        flush.zero_()
+        evs = []
+        one(evs)
+        torch.cuda.synchronize()
+        t_idx.append(sum(e[0].elapsed_time(e[1]) for e in evs))
+        t_mla.append(sum(e[1].elapsed_time(e[2]) for e in evs))
+        per_chunk = [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in evs]
+    return float(np.mean(t_idx)), float(np.mean(t_mla)), per_chunk
+
+
+def stage_report(spec, ms_idx, ms_mla, pk):
+    """Achieved rates of the two stages against their rooflines."""
+    cnt = {"pairs": 0, "idx_flops": 0, "mla_flops": 0, "mla_bytes": 0, "mla_gather_bytes": 0, "idx_bytes": 0}
+    for P, n in chunk_list(spec):
+        c = counting.prefill_counts(P, n, spec.n_heads, spec.h_idx, spec.d_idx, spec.topk, spec.kv_dtype,
+                                    1 if spec.idx_dtype == "fp8" else 2)
+        for key in cnt:
+            cnt[key] += c[key]
+    fp8_burst, fp8_sust = 2 * pk["bf16"], 2 * pk["bf16_sust"]
+    idx_tf = cnt["idx_flops"] / (ms_idx / 1e3) / 1e12
+    mla_tf = cnt["mla_flops"] / (ms_mla / 1e3) / 1e12
+    return cnt, {
+        "indexer_topk": {"ms": ms_idx, "share": ms_idx / (ms_idx + ms_mla), "tflops_fp8": idx_tf,
+                         "frac_of_fp8_peak_sustained": idx_tf / fp8_sust, "frac_of_fp8_peak_burst": idx_tf / fp8_burst,
+                         "flops": cnt["idx_flops"], "pairs": cnt["pairs"]},
+        "sparse_mla": {"ms": ms_mla, "share": ms_mla / (ms_idx + ms_mla), "tflops_bf16": mla_tf,
+                       "frac_of_bf16_peak_sustained": mla_tf / pk["bf16_sust"],
+                       "frac_of_bf16_peak_burst": mla_tf / pk["bf16"], "flops": cnt["mla_flops"],
+                       "gbs_hbm_algorithmic": cnt["mla_bytes"] / (ms_mla / 1e3) / 1e9,
+                       "gbs_l2_gathers": cnt["mla_gather_bytes"] / (ms_mla / 1e3) / 1e9},
+    }
 
 
 def host_sample_rows(T: int, n: int, seed: int = 2024):
@@ -181,18 +300,20 @@ def host_sample_rows(T: int, n: int, seed: int = 2024):
     return np.sort(rng.choice(T, size=n, replace=False))
 
 
-def cpu_oracle_sample(spec, dev, n_rows):
+def cpu_oracle_sample(spec, dev, n_rows, cache_h=None):
     """Time the CPU oracle (all host cores) on n_rows random rows of the workload."""
     import oracle
     rows = host_sample_rows(spec.n_tokens, n_rows)
-    cache_h = dev.cache.to("cpu")
+    if cache_h is None:
+        cache_h = dev.cache.to("cpu")
     oracle.build()
     t0 = time.perf_counter()
     _, _, _, _, used, _ = oracle.prefill_rows(dev, rows, cache_host=cache_h)
     dt = time.perf_counter() - t0
     return dict(value=n_rows / dt, unit=UNIT, cores=int(used), kind="oracle",
                 sample=f"{n_rows} random query rows of {spec.name} (full indexer over their causal keys, "
-                       f"full-sort top-{spec.topk}, fp64 attention), {dt:.1f} s wall")
+                       f"full-sort top-{spec.topk}, fp64 attention), {dt:.1f} s wall; tokens/s of the sample, "
+                       "extrapolated to the workload")
 
 
 def run_reference(args, rank, world):
@@ -202,13 +323,14 @@ def run_reference(args, rank, world):
     spec = wl.SPECS[WORKLOAD]
     dev_name = "cuda" if torch.cuda.is_available() else "cpu"
     dev = wl.make(spec, dev_name)
-    rows_per_step = 256
+    cache_h = dev.cache.to("cpu")
+    rows_per_step = 32
     for _ in range(args.warmup):
-        cpu_oracle_sample(spec, dev, 4)
+        cpu_oracle_sample(spec, dev, 2, cache_h)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = cpu_oracle_sample(spec, dev, rows_per_step)
+        r = cpu_oracle_sample(spec, dev, rows_per_step, cache_h)
         vals.append(r["value"])
     wall = time.perf_counter() - t0
     value = float(np.mean(vals))
@@ -217,7 +339,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec.name, "n_tokens": spec.n_tokens, "prefix_len": spec.prefix_len,
-                   "n_heads": spec.n_heads, "topk": spec.topk, "step_sample_rows": rows_per_step},
+                   "chunk": spec.chunk, "n_heads": spec.n_heads, "topk": spec.topk,
+                   "step_sample_rows": rows_per_step},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                          "sample": f"{rows_per_step} random query rows per step of {spec.name}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -225,48 +348,77 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, spec, dev, out, lse, stream, world):
-    """Same step from pinned HOST buffers through the package's host-buffer
-    prefill (smla_sparse_mla_prefill per chunk of E2E_CHUNK query tokens): every
-    step copies q, q_I and w in and reads out and lse back, the copies of one
-    chunk overlapping the kernels of the others."""
+def run_e2e(args, spec, dev, ref_out, stream, world):
+    """The step from pinned HOST buffers through the package's host-buffer
+    prefill: every step copies q, q_I and w in and reads out and lse back, chunk
+    by chunk (the workload's own 8,192-token chunks, each one
+    smla_sparse_mla_prefill call), the copies of one chunk overlapping the
+    kernels of the others."""
     T, H, k, P = spec.n_tokens, spec.n_heads, spec.topk, spec.prefix_len
     q_h = dev.q.cpu().pin_memory()
     qi_h = dev.q_idx.cpu().pin_memory()
     w_h = dev.w.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    out_h = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    chunk = spec.chunk if spec.chunk > 0 else T
     hp = smla.HostPrefill(dev.cache, dev.page_table, P, T, H, spec.h_idx, spec.d_idx, spec.idx_dtype, k,
-                          spec.sm_scale, chunk=e2e_chunks(T))
+                          spec.sm_scale, chunk=chunk)
 
     def e2e_step():
         hp.run(q_h, qi_h, w_h, out_h, lse_h, stream=stream)
 
-    for _ in range(3):
+    for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
     barrier(world)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, min(args.steps, 10))
-    e_s.record(stream)
+    n_e2e = max(3, min(args.steps, 6))
+    times = []
     for _ in range(n_e2e):
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
         e2e_step()
-    e_e.record(stream)
+        e_e.record(stream)
+        times.append((e_s, e_e))
     torch.cuda.synchronize()
     assert smla.read_status(hp.ws)[0] == 0
-    # the host copy of the result is the device result
-    assert torch.equal(out_h.view(torch.int16), hp.out.cpu().view(torch.int16))
-    ms_e2e = reduce_max(e_s.elapsed_time(e_e) / n_e2e, world)
+    # the host copy of the result is the device-resident step's result
+    assert torch.equal(out_h.view(torch.int16), ref_out.cpu().view(torch.int16))
+    ms_e2e = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in times])), world)
     h2d = q_h.numel() * q_h.element_size() + qi_h.numel() * qi_h.element_size() + w_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
-    return ms_e2e, h2d, d2h
+    return ms_e2e, h2d, d2h, chunk
+
+
+def measure_extra_prefill(name, args, stream, flush):
+    """An extra prefill workload: the step through the product entry, then the
+    per-kernel split."""
+    spec = wl.SPECS[name]
+    dev = wl.make(spec, "cuda")
+    ps = PrefillStep(spec, dev)
+    for _ in range(3):
+        ps.run(stream)
+    torch.cuda.synchronize()
+    assert smla.read_status(ps.ws)[0] == 0
+    n = max(3, min(args.steps, 10))
+    ms = float(np.mean(time_steps(lambda: ps.run(stream), n, stream, flush)))
+    ms_idx, ms_mla, _ = stage_split(spec, dev, stream, flush, 2)
+    _, kern = stage_report(spec, ms_idx, ms_mla, peaks())
+    res = {"workload": f"{spec.name}: T={spec.n_tokens} new tokens after a prefix of {spec.prefix_len}"
+                       + (f" in {spec.chunk}-token chunks" if spec.chunk else "")
+                       + f", {spec.n_heads} heads, {spec.kv_dtype} latent cache, indexer {spec.h_idx}x{spec.d_idx} "
+                       f"{spec.idx_dtype}, top-{spec.topk}" + (", shuffled pages" if spec.shuffled else ""),
+           "ms_per_step": ms, "tokens_per_s": spec.n_tokens / (ms / 1e3), "kernels": kern,
+           "gpu_launches_per_step": ps.launches()}
+    del ps, dev
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_decode(args, stream, flush):
     """The decode workload (64 requests x 2 MTP tokens, 8K-128K keys each, FP8
     cache in a shuffled pool): one step = smla_sparse_mla_decode (split-key
-    indexer, candidate merge, sparse MLA). Reported next to the headline; its
-    roofline is HBM bandwidth over the algorithmic bytes of the step."""
+    indexer, candidate merge, sparse MLA). Its roofline is HBM bandwidth over
+    the algorithmic bytes of the step."""
     spec = wl.SPECS["decode"]
     dev = wl.make(spec, "cuda")
     lens = dev.seq_lens
@@ -290,16 +442,7 @@ def measure_decode(args, stream, flush):
     n = max(5, min(args.steps, 20))
 
     def timed(run):
-        ev = []
-        for _ in range(n):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            run()
-            e1.record(stream)
-            ev.append((e0, e1))
-        torch.cuda.synchronize()
-        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+        return float(np.median(time_steps(run, n, stream, flush)))
 
     # a decode step is a few short kernels: launched one by one from Python the
     # host work between launches shows up as device idle time, so the step is
@@ -351,17 +494,18 @@ def measure_decode(args, stream, flush):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=["prefill128k", "prefill16k", "prefix1m"],
+                    help="benchmarked prefill workload (default: the 131,072-token prefill in 8,192-token chunks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=2560)
-    ap.add_argument("--workload", default=WORKLOAD, choices=["prefill16k"],
-                    help="benchmarked workload (the 16,384-token prefill)")
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle rows of the CPU baseline (0: the default)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: use this many query tokens instead of the workload's")
     ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the host-buffer pass")
-    ap.add_argument("--no-decode", action="store_true", help="profiling only: skip the decode measurement")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="profiling only: skip the extra workloads (16K prefill, 1M prefix, decode)")
     ap.add_argument("--decode-only", action="store_true",
                     help="profiling only: run and print the decode measurement alone")
     args = ap.parse_args()
@@ -374,10 +518,11 @@ def main():
     if rank == 0:
         smla.build()
     barrier(world)
-    L = smla.lib()
+    smla.lib()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     if args.decode_only:
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-        d = measure_decode(args, torch.cuda.current_stream(), flush)
+        d = measure_decode(args, stream, flush)
         if rank == 0:
             print(json.dumps({"decode": d}))
         return
@@ -385,115 +530,99 @@ def main():
     if args.tokens:
         spec = wl.scaled(spec, n_tokens=args.tokens)
     dev = wl.make(spec, "cuda")
-    T, H, k = spec.n_tokens, spec.n_heads, spec.topk
-    P = spec.prefix_len
-    stream = torch.cuda.current_stream()
-    seq_lens = torch.tensor([P + T], dtype=torch.int32, device="cuda")
-    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
-    ws_i = smla.workspace(L.smla_indexer_topk_workspace_size(1, P + T, T, spec.h_idx, k))
-    ws_m = smla.workspace(L.smla_sparse_mla_fwd_workspace_size(P + T, T, H, k, smla._dtype_code(spec.kv_dtype)))
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-
-    def step():
-        smla.indexer_topk(dev.cache, dev.page_table, seq_lens, P + T, T, dev.q_idx, dev.w, k, out_idx=idx,
-                          ws=ws_i)
-        e_mid = torch.cuda.Event(enable_timing=True)
-        e_mid.record(stream)
-        smla.sparse_mla_fwd(dev.cache, dev.page_table, dev.q, idx, spec.sm_scale, prefix_len=P, out=out,
-                            lse=lse, ws=ws_m)
-        return e_mid
-
+    T, H, k, P = spec.n_tokens, spec.n_heads, spec.topk, spec.prefix_len
+    ps = PrefillStep(spec, dev)
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        ps.run(stream)
     torch.cuda.synchronize()
-    assert smla.read_status(ws_i)[0] == 0 and smla.read_status(ws_m)[0] == 0
+    assert smla.read_status(ps.ws)[0] == 0
     barrier(world)
     torch.cuda.synchronize()
-    t_idx, t_mla, t_step = [], [], []
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            flush.zero_()  # write > L2 between steps
-            e0 = torch.cuda.Event(enable_timing=True)
-            e2 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            e1 = step()
-            e2.record(stream)
-            t_step.append((e0, e1, e2))
-        torch.cuda.synchronize()
+        t_step = time_steps(lambda: ps.run(stream), args.steps, stream, flush)
         wall = time.perf_counter() - wall0
     barrier(world)
-    for e0, e1, e2 in t_step:
-        t_idx.append(e0.elapsed_time(e1))
-        t_mla.append(e1.elapsed_time(e2))
-    ms_step = float(np.mean([a + b for a, b in zip(t_idx, t_mla)]))
+    assert smla.read_status(ps.ws)[0] == 0
+    ms_step = float(np.mean(t_step))
     ms_step_max = reduce_max(ms_step, world)
-    ms_idx, ms_mla = float(np.mean(t_idx)), float(np.mean(t_mla))
     value = world * T / (ms_step_max / 1e3)
+
+    # ------------------------------------------------------------------ per-kernel split (separate pass)
+    ms_idx, ms_mla, per_chunk = stage_split(spec, dev, stream, flush, 2)
+    pk = peaks()
+    cnt, kernels = stage_report(spec, ms_idx, ms_mla, pk)
+    kernels["split_pass"] = ("the same chunks as smla_indexer_topk + smla_sparse_mla_fwd calls with events between "
+                             "them, mean of 2 steps; the headline times the smla_sparse_mla_prefill calls")
+    kernels["last_chunk_ms"] = {"indexer_topk": per_chunk[-1][0], "sparse_mla": per_chunk[-1][1]}
 
     # ------------------------------------------------------------------ e2e through host buffers
     if args.no_e2e:
-        ms_e2e, h2d, d2h = float("nan"), 0, 0
+        ms_e2e, h2d, d2h, e2e_chunk = float("nan"), 0, 0, 0
     else:
-        ms_e2e, h2d, d2h = run_e2e(args, spec, dev, out, lse, stream, world)
+        ms_e2e, h2d, d2h, e2e_chunk = run_e2e(args, spec, dev, ps.out, stream, world)
 
-    decode = None if args.no_decode else measure_decode(args, stream, flush)
-
-    # ------------------------------------------------------------------ roofline
-    pk = peaks()
-    cnt = counting.prefill_counts(P, T, H, spec.h_idx, spec.d_idx, k, spec.kv_dtype,
-                                  1 if spec.idx_dtype == "fp8" else 2)
-    mla_tflops = cnt["mla_flops"] / (ms_mla / 1e3) / 1e12
-    idx_tflops = cnt["idx_flops"] / (ms_idx / 1e3) / 1e12
-    fp8_peak = 2 * pk["bf16"]
+    # ------------------------------------------------------------------ roofline of the dominant kernel
     dominant_is_mla = ms_mla >= ms_idx
-    roof = {"kernel": "sparse_mla (mla_kernel)" if dominant_is_mla else "indexer_topk (indexer_kernel)",
-            "bound": "tensor", "unit": "TFLOP/s",
-            "achieved": mla_tflops if dominant_is_mla else idx_tflops,
-            "peak": pk["bf16"] if dominant_is_mla else fp8_peak,
-            "peak_src": (f"{pk['src']} bf16 burst" if dominant_is_mla else
-                         f"{pk['src']} bf16 burst x2 (nominal fp8/bf16 ratio)"),
-            "traffic": measured_traffic("mla_kernel" if dominant_is_mla else "indexer_kernel")}
-    if T != wl.SPECS[args.workload].n_tokens:
-        roof["traffic"] = None  # the capture is of the full-size workload
+    n_launch = len(ps.chunks)
+    if dominant_is_mla:
+        roof = {"kernel": "mla_kernel (sparse MLA)", "bound": "tensor", "unit": "TFLOP/s",
+                "achieved": kernels["sparse_mla"]["tflops_bf16"], "peak": pk["bf16_sust"],
+                "peak_src": f"{pk['src']} bf16 sustained (the kernel runs inside a long step)",
+                "traffic": measured_traffic("mla_kernel", f"dram_traffic_{spec.name}.md")}
+    else:
+        roof = {"kernel": "indexer_kernel (indexer + exact top-k)", "bound": "tensor", "unit": "TFLOP/s",
+                "achieved": kernels["indexer_topk"]["tflops_fp8"], "peak": 2 * pk["bf16_sust"],
+                "peak_src": f"{pk['src']} bf16 sustained x2 (the nominal fp8/bf16 ratio; the kernel runs inside "
+                            "a long step)",
+                "traffic": measured_traffic("indexer_kernel", f"dram_traffic_{spec.name}.md")}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    kernels = {
-        "indexer_topk": {"ms": ms_idx, "share": ms_idx / (ms_idx + ms_mla), "tflops_fp8": idx_tflops,
-                         "frac_of_fp8_peak": idx_tflops / fp8_peak},
-        "sparse_mla": {"ms": ms_mla, "share": ms_mla / (ms_idx + ms_mla), "tflops_bf16": mla_tflops,
-                       "frac_of_bf16_peak": mla_tflops / pk["bf16"],
-                       "gbs_algorithmic": cnt["mla_bytes"] / (ms_mla / 1e3) / 1e9},
-    }
+    roof["per_launch"] = (f"achieved = the kernel's algorithmic FLOPs over the step's {n_launch} launches / their "
+                          "summed event time")
+    if args.tokens:
+        roof["traffic"] = None
+
+    launches_per_step = ps.launches()
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        cpu_base = cpu_oracle_sample(spec, dev, args.cpu_rows or CPU_ROWS.get(spec.name, 256))
+    extras = {}
+    if not args.no_extras:
+        del dev, ps
+        torch.cuda.empty_cache()
+        for name in ("prefill16k", "prefix1m"):
+            if name != spec.name:
+                extras[name] = measure_extra_prefill(name, args, stream, flush)
+        extras["decode"] = measure_decode(args, stream, flush)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"{spec.name}: T={T} new tokens, prefix {P}, {H} heads, latent 576 BF16 KV, "
-                               f"indexer {spec.h_idx}x{spec.d_idx} FP8, top-{k}",
-                   "indexer_dtype": "fp8(e4m3) operands, fp32 accumulate",
-                   "mla_dtype": "bf16 q and cache widened exactly to f16 MMA operands, f16 P, fp32 accumulate, "
+        "vs_baseline": None, "dtype": "fp8" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": f"{spec.name}: T={T} new tokens after a prefix of {P}"
+                               + (f", in {spec.chunk}-token chunks against the growing cache" if spec.chunk else "")
+                               + f", {H} heads, latent 576 {spec.kv_dtype} KV"
+                               + (" with a per-token fp32 scale" if spec.kv_dtype == "fp8" else "")
+                               + f", indexer {spec.h_idx}x{spec.d_idx} {spec.idx_dtype}, top-{k}",
+                   "entry": "smla_sparse_mla_prefill per chunk",
+                   "indexer_dtype": "e4m3 operands, fp32 accumulate, fp32 head-weighted sum",
+                   "mla_dtype": "cache rows widened exactly to f16 MMA operands, f16 q and P, fp32 accumulate, "
                                 "bf16 output",
                    "parallelism": f"replicas x{world}",
-                   "l2": "256 MB buffer written between timed steps", "wall_s_timed_region": wall},
+                   "l2": "inputs larger than L2, and a 256 MB buffer written between timed steps",
+                   "wall_s_timed_region": wall},
         "roofline": roof, "kernels": kernels,
         "e2e": {"value": world * T / (ms_e2e / 1e3) if ms_e2e == ms_e2e else None, "unit": UNIT,
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "path": "pinned host q/q_I/w -> H2D -> smla_sparse_mla_prefill -> D2H out/lse, pipelined in "
-                        f"chunks of query tokens {e2e_chunks(T)} (HostPrefill)"},
-        # per step: indexer_kernel, shadow_convert_kernel (BF16 cache only), mla_kernel
-        "gpu_launches": (3 if spec.kv_dtype == "bf16" else 2) * args.steps,
-        "decode": decode,
+                        f"chunks of {e2e_chunk} query tokens (HostPrefill)"},
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    line.update(extras)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_oracle_sample(spec, dev, args.cpu_rows)
-        elif not args.no_cpu_baseline:
-            line["cpu_baseline"] = None
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_base
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

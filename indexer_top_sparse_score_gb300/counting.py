@@ -24,7 +24,10 @@ def mla_intensity(heads: int, rows: int = 2048, row_bytes: int = 660) -> float:
 
 
 def kv_row_bytes(kv_dtype: str) -> int:
-    """Bytes of one latent KV row as the library stores it (FP8 adds its fp32 scale)."""
+    """Bytes of one latent KV row as the library stores it (FP8 adds its fp32 scale;
+    the tile-scaled FP8 row of the GLM page's footnote 1 is 656 bytes)."""
+    if kv_dtype == "fp8_ds_mla":
+        return 656
     return D_QK * 2 if kv_dtype == "bf16" else D_QK + 4
 
 
@@ -41,12 +44,17 @@ def prefill_counts(prefix_len: int, n_tokens: int, n_heads: int, h_idx: int, d_i
     sel = sum(n_selected(P + t, topk) for t in range(T)) if T < 4096 else \
         _sum_selected(P, T, topk)
     rb = kv_row_bytes(kv_dtype)
+    per_query = T * n_heads * (2 * D_QK + 2 * D_V + 4) + T * topk * 4  # q, out, lse, index list
     return dict(
         idx_flops=2 * h_idx * d_idx * pairs,
         mla_flops=MLA_FLOP_PER_ROW_HEAD * n_heads * sel,
         pairs=pairs, selected_rows=sel,
-        # sparse-MLA kernel: gathered rows + q + out + lse + index list
-        mla_bytes=sel * rb + T * n_heads * (2 * D_QK + 2 * D_V + 4) + T * topk * 4,
+        # sparse-MLA kernel, HBM: every cache row at most once (P + T rows), q, out,
+        # lse and the index list
+        mla_bytes=(P + T) * rb + per_query,
+        # the same with every selected-row gather counted (L2-level traffic: the
+        # rows a query selects are mostly shared with its neighbours)
+        mla_gather_bytes=sel * rb + per_query,
         # indexer kernel: every key row once, q_I, w, and the index list it writes
         idx_bytes=(P + T) * d_idx * idx_bytes + T * h_idx * (d_idx * idx_bytes + 4) + T * topk * 4,
     )

@@ -179,7 +179,7 @@ class Oracle:
         return out, lse
 
 
-def prefill_rows(prob, rows, cache_host=None, n_threads: int = 0):
+def prefill_rows(prob, rows, cache_host=None, n_threads: int = 0, sm_scale: Optional[float] = None):
     """Full step for chosen rows of a prefill Problem whose tensors may live on a GPU.
 
     Each chosen row becomes a one-token sequence of length pos+1 that shares the
@@ -197,7 +197,7 @@ def prefill_rows(prob, rows, cache_host=None, n_threads: int = 0):
     sub = wl.Problem(wl.scaled(spec, kind="decode", n_seqs=n, q_per_seq=1), cache, pts,
                      prob.q[r].cpu().contiguous(), prob.q_idx[r].cpu().contiguous(),
                      prob.w[r].cpu().contiguous(), torch.as_tensor(pos + 1, dtype=torch.int32), 0, 0)
-    return Oracle(sub).rows(np.arange(n), n_threads=n_threads)
+    return Oracle(sub, sm_scale=sm_scale).rows(np.arange(n), n_threads=n_threads)
 
 
 def select_topk(scores: np.ndarray, k: int):

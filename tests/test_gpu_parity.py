@@ -80,7 +80,7 @@ def test_prefill16k_full_size_sampled():
     spec = wl.SPECS["prefill16k"]
     dev = wl.make(spec, "cuda")
     idx, out, lse = run_prefill(dev)
-    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=(4095, 8191, 12287), n_random=16)
+    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=(4095, 4096, 8191, 8192, 12287), n_random=480)
     ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
     r = torch.as_tensor(rows, device="cuda")
     compare_idx(_host(idx[r]), ridx)
@@ -99,8 +99,9 @@ def test_prefill128k_chunked_sampled():
     spec = wl.SPECS["prefill128k"]
     dev = wl.make(spec, "cuda")
     idx, out, lse = run_prefill(dev, chunk=spec.chunk)
-    edges = [c * spec.chunk + d for c in (1, 7, 15) for d in (-1, 0, 1)]
-    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=edges, n_random=6)
+    # every 8,192-token chunk edge, rows around t = k, and random rows (~530 in all)
+    edges = [c * spec.chunk + d for c in range(1, 16) for d in (-1, 0, 1)]
+    rows = stratified_rows(0, spec.n_tokens, spec.topk, extra=edges, n_random=480)
     ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
     r = torch.as_tensor(rows, device="cuda")
     compare_idx(_host(idx[r]), ridx)
@@ -112,7 +113,13 @@ def test_prefix1m_sampled():
     spec = wl.SPECS["prefix1m"]
     dev = wl.make(spec, "cuda")
     idx, out, lse = run_prefill(dev)
-    rows = np.array([0, 1, 4095, 8190, 8191, 1234, 5678], dtype=np.int64)
+    # first and last rows, rows at page boundaries of the new tokens (position
+    # P + t with (P + t) % 64 in {0, 63}) and random rows: 64 in all
+    rng = np.random.default_rng(5)
+    fixed = {0, 1, 2, 63, 64, 127, 128, 4095, 4096, 8127, 8128, 8190, 8191}
+    rnd = set(rng.choice(spec.n_tokens, 64, replace=False).tolist()) - fixed
+    rows = np.array(sorted(fixed | set(sorted(rnd)[:64 - len(fixed)])), dtype=np.int64)
+    assert len(rows) == 64
     ridx, _, rout, rlse, _ = sampled_oracle(dev, rows)
     r = torch.as_tensor(rows, device="cuda")
     compare_idx(_host(idx[r]), ridx)

@@ -24,12 +24,63 @@ def test_chunk_bounds_explicit_sizes():
         smla.chunk_bounds(3000, 0)
 
 
-def test_bench_e2e_schedule_tapers_and_covers():
+def test_bench_chunk_schedule_covers_workloads():
+    """The long prefill is timed as 16 calls of 8,192 query tokens against the
+    growing cache; the other prefills as one call after their prefix."""
     sys.argv = ["bench.py"]
     import bench
-    c = bench.e2e_chunks(16384)
-    assert sum(c) == 16384 and c[:3] == [256, 768, 1024] and c[-3:] == [1024, 768, 256]
-    assert set(c[3:-3]) == {bench.E2E_CHUNK}
-    b = smla.chunk_bounds(16384, c)
-    assert b[0][0] == 0 and b[-1][1] == 16384 and all(x[1] == y[0] for x, y in zip(b, b[1:]))
-    assert bench.e2e_chunks(4096) == bench.E2E_CHUNK   # too short to taper: even chunks
+    from indexer_top_sparse_score_gb300 import workloads as wl
+    c = bench.chunk_list(wl.SPECS["prefill128k"])
+    assert c == [(8192 * i, 8192) for i in range(16)]
+    assert bench.chunk_list(wl.SPECS["prefix1m"]) == [(1 << 20, 8192)]
+    assert bench.chunk_list(wl.SPECS["prefill16k"]) == [(0, 16384)]
+    assert bench.chunk_list(wl.scaled(wl.SPECS["prefill128k"], n_tokens=20000)) == [(0, 8192), (8192, 8192),
+                                                                                       (16384, 3616)]
+
+
+def test_bench_stage_counts_match_the_workload_sizing():
+    """The per-kernel FLOP counts of a bench step reproduce the sizing of the
+    workloads: ~70.4 TFLOP of indexer and ~37.1 TFLOP of attention for the
+    131,072-token prefill, ~70.6 and ~2.34 TFLOP for the 1M-token prefix."""
+    sys.argv = ["bench.py"]
+    import bench
+    from indexer_top_sparse_score_gb300 import workloads as wl
+    pk = dict(hbm=1.0, bf16=1.0, bf16_sust=1.0, src="test")
+    cnt, _ = bench.stage_report(wl.SPECS["prefill128k"], 1.0, 1.0, pk)
+    assert round(cnt["idx_flops"] / 1e12, 1) == 70.4 and round(cnt["mla_flops"] / 1e12, 1) == 37.1
+    cnt, _ = bench.stage_report(wl.SPECS["prefix1m"], 1.0, 1.0, pk)
+    assert round(cnt["idx_flops"] / 1e12, 1) == 70.6 and round(cnt["mla_flops"] / 1e12, 2) == 2.34
+    cnt, _ = bench.stage_report(wl.SPECS["prefill16k"], 1.0, 1.0, pk)
+    assert round(cnt["idx_flops"] / 1e12, 2) == 1.10 and round(cnt["mla_flops"] / 1e12, 2) == 4.38
+
+
+def test_output_checker_catches_one_wrong_head_and_one_wrong_lse():
+    """The GPU parity checker (per-(row, head) bound on top of the aggregate bar):
+    outputs rounded like the kernel's pass; one (row, head) among 128 x 64 that is
+    5% off fails although the aggregate rel-L2 and the max-abs bars pass; one
+    wrong lse fails."""
+    import numpy as np
+    import torch
+    from tests.gpu_common import compare_out
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((128, 64, 512)) * 0.04
+    lse = 8.0 + rng.standard_normal((128, 64))
+    got = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()  # bf16 output rounding
+    for kv in ("bf16", "fp8"):
+        compare_out(got, ref, lse.astype(np.float32), lse, kv)
+        bad = got.copy()
+        bad[77, 5] *= 1.05
+        with pytest.raises(AssertionError, match="row, head"):
+            compare_out(bad, ref, lse.astype(np.float32), lse, kv)
+        bl = lse.copy()
+        bl[3, 60] += 0.1
+        with pytest.raises(AssertionError, match="lse"):
+            compare_out(got, ref, bl.astype(np.float32), lse, kv)
+    # a row with no usable key: out = 0 and lse = -inf on both sides
+    ref2, lse2, got2 = ref.copy(), lse.copy(), got.copy()
+    ref2[9], got2[9], lse2[9] = 0.0, 0.0, -np.inf
+    compare_out(got2, ref2, lse2.astype(np.float32), lse2, "bf16")
+    lse3 = lse2.copy()
+    lse3[9, 0] = 1.0
+    with pytest.raises(AssertionError):
+        compare_out(got2, ref2, lse3.astype(np.float32), lse2, "bf16")

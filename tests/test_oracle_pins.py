@@ -357,3 +357,88 @@ def test_generated_workload_shapes_and_value_sets():
     assert all(100 <= L <= 300 for L in lens)
     used = [int(x) for b, L in enumerate(lens) for x in d.page_table[b, :-(-L // 64)].tolist()]
     assert sorted(used) == list(range(d.cache.num_pages))
+
+
+# --------------------------------------------------------------- decode rows ----
+def _decode_problem(lens, pts, topk, H=3, H_I=2, D_I=16, seed=41, winner=False):
+    """Two requests over one shared pool of 6 pages (bf16 latent rows, bf16
+    indexer keys), q_per_seq = 2. Page table row b maps request b's logical
+    pages to pool pages. With `winner`, the last token of every request gets a
+    key that out-scores every other key for every query."""
+    gen = torch.Generator().manual_seed(seed)
+    pages, B, qps = 6, len(lens), 2
+    rows = pages * wl.PAGE
+    kv = torch.randn(rows, wl.D_QK, generator=gen).to(torch.bfloat16)
+    k_idx = torch.randint(-1, 2, (rows, D_I), generator=gen).float()
+    q_idx = torch.randint(-4, 5, (B * qps, H_I, D_I), generator=gen).float()
+    if winner:
+        q_idx = torch.ones(B * qps, H_I, D_I)
+        for b, L in enumerate(lens):
+            pr = pts[b][(L - 1) // wl.PAGE] * wl.PAGE + (L - 1) % wl.PAGE
+            k_idx[pr] = 4.0
+    w = torch.randint(1, 5, (B * qps, H_I), generator=gen).float()
+    q = torch.randn(B * qps, H, wl.D_QK, generator=gen).to(torch.bfloat16)
+    pt = torch.full((B, max(len(p) for p in pts)), -1, dtype=torch.int32)
+    for b, p in enumerate(pts):
+        pt[b, :len(p)] = torch.tensor(p, dtype=torch.int32)
+    cache = wl.Cache(kv.view(pages, wl.PAGE, wl.D_QK).contiguous(), None,
+                     k_idx.to(torch.bfloat16).view(pages, wl.PAGE, D_I).contiguous(), None, "bf16", "bf16")
+    spec = wl.Spec("custom-decode", "decode", n_heads=H, h_idx=H_I, d_idx=D_I, idx_dtype="bf16",
+                   kv_dtype="bf16", topk=topk, seed=0, n_seqs=B, q_per_seq=qps)
+    return wl.Problem(spec, cache, pt, q.contiguous(), q_idx.to(torch.bfloat16).contiguous(), w.contiguous(),
+                      torch.tensor(lens, dtype=torch.int32), 0, 0)
+
+
+def test_decode_rows_sit_at_the_end_of_each_request():
+    """Decode with two query tokens per request (the MTP shape): query j of a
+    request of L keys sits at position L - 2 + j and sees keys 0..that position,
+    so the first token does not see the second. With L <= k every visible key is
+    selected and each row equals dense causal attention over the request's own
+    rows (gathered through its page table), computed with torch in fp64."""
+    lens, pts = [37, 100], [[2], [3, 1]]
+    prob = _decode_problem(lens, pts, topk=128)
+    scale = 0.05
+    o = oracle.Oracle(prob, sm_scale=scale)
+    idx, _, out, lse, _, bad = o.rows(range(4))
+    assert not bad.any()
+    kv = prob.cache.kv.view(-1, wl.D_QK).double()
+    for b, L in enumerate(lens):
+        logical = torch.tensor([pts[b][s // wl.PAGE] * wl.PAGE + s % wl.PAGE for s in range(L)])
+        K = kv[logical]
+        for j in range(2):
+            r = 2 * b + j
+            pos = L - 2 + j
+            assert o.position(r) == pos
+            assert idx[r, :pos + 1].tolist() == list(range(pos + 1)) and (idx[r, pos + 1:] == -1).all()
+            logits = scale * (prob.q[r].double() @ K[:pos + 1].T)
+            ref = torch.softmax(logits, dim=-1) @ K[:pos + 1, :wl.D_V]
+            assert np.allclose(out[r], ref.numpy(), rtol=1e-12, atol=1e-12)
+            assert np.allclose(lse[r], torch.logsumexp(logits, dim=-1).numpy(), rtol=1e-12)
+
+
+def test_decode_first_mtp_token_cannot_select_the_second():
+    """A key that beats every other is placed at the last token of each request:
+    the request's last query row selects it, the row before cannot see it."""
+    lens, pts = [120, 200], [[0, 2], [3, 1, 5, 4]]
+    prob = _decode_problem(lens, pts, topk=8, winner=True)
+    idx, *_ = oracle.Oracle(prob).rows(range(4), attend=False)
+    for b, L in enumerate(lens):
+        assert (L - 1) in idx[2 * b + 1].tolist()
+        assert (L - 1) not in idx[2 * b].tolist()
+        assert idx[2 * b].max() <= L - 2
+
+
+def test_decode_rows_equal_prefill_rows_at_the_same_positions():
+    """Each decode row equals the prefill row at the same absolute position of
+    the same sequence (same cache, same page table), with longer requests than k."""
+    lens, pts = [150, 230], [[1, 3, 0], [2, 0, 3, 1]]
+    prob = _decode_problem(lens, pts, topk=16, seed=43)
+    idx, sc, out, lse, _, _ = oracle.Oracle(prob).rows(range(4))
+    for b, L in enumerate(lens):
+        sub = wl.Problem(wl.scaled(prob.spec, kind="prefill", n_tokens=2, prefix_len=L - 2), prob.cache,
+                         prob.page_table[b].clone(), prob.q[2 * b:2 * b + 2].contiguous(),
+                         prob.q_idx[2 * b:2 * b + 2].contiguous(), prob.w[2 * b:2 * b + 2].contiguous(),
+                         None, L - 2, 2)
+        pi, ps, po, pl, _, _ = oracle.Oracle(sub).rows(range(2))
+        assert np.array_equal(pi, idx[2 * b:2 * b + 2]) and np.array_equal(ps, sc[2 * b:2 * b + 2])
+        assert np.array_equal(po, out[2 * b:2 * b + 2]) and np.array_equal(pl, lse[2 * b:2 * b + 2])
