@@ -190,15 +190,19 @@ class PrefillStep:
         self.chunks = chunk_list(spec)
         need = max(smla.prefill_workspace_bytes(P, n, H, spec.h_idx, spec.topk, spec.kv_dtype)
                    for P, n in self.chunks)
-        self.ws = smla.workspace(need)
+        # chunk c's workspace starts 256 bytes after chunk c-1's: its own status word
+        self.ws = smla.workspace(need + smla.STATUS_BYTES * len(self.chunks))
 
     def run(self, stream=None):
         s, d = self.spec, self.dev
-        for P, n in self.chunks:
+        for c, (P, n) in enumerate(self.chunks):
             a = P - s.prefix_len
             smla.sparse_mla_prefill(d.cache, d.page_table, P, d.q[a:a + n], d.q_idx[a:a + n], d.w[a:a + n],
                                     s.topk, s.sm_scale, out=self.out[a:a + n], lse=self.lse[a:a + n],
-                                    ws=self.ws, stream=stream)
+                                    ws=self.ws[smla.STATUS_BYTES * c:], stream=stream)
+
+    def status(self):
+        return smla.read_status_chunks(self.ws, len(self.chunks))[0]
 
     def launches(self):
         """Kernels one step launches: per chunk the indexer, the deferred
@@ -380,7 +384,7 @@ def run_e2e(args, spec, dev, ref_out, stream, world):
         e_e.record(stream)
         times.append((e_s, e_e))
     torch.cuda.synchronize()
-    assert smla.read_status(hp.ws)[0] == 0
+    assert hp.read_status()[0] == 0
     # the host copy of the result is the device-resident step's result
     assert torch.equal(out_h.view(torch.int16), ref_out.cpu().view(torch.int16))
     ms_e2e = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in times])), world)
@@ -398,7 +402,7 @@ def measure_extra_prefill(name, args, stream, flush):
     for _ in range(3):
         ps.run(stream)
     torch.cuda.synchronize()
-    assert smla.read_status(ps.ws)[0] == 0
+    assert ps.status() == 0
     n = max(3, min(args.steps, 10))
     ms = float(np.mean(time_steps(lambda: ps.run(stream), n, stream, flush)))
     ms_idx, ms_mla, _ = stage_split(spec, dev, stream, flush, 2)
@@ -536,7 +540,7 @@ def main():
         flush.zero_()
         ps.run(stream)
     torch.cuda.synchronize()
-    assert smla.read_status(ps.ws)[0] == 0
+    assert ps.status() == 0
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -544,7 +548,7 @@ def main():
         t_step = time_steps(lambda: ps.run(stream), args.steps, stream, flush)
         wall = time.perf_counter() - wall0
     barrier(world)
-    assert smla.read_status(ps.ws)[0] == 0
+    assert ps.status() == 0
     ms_step = float(np.mean(t_step))
     ms_step_max = reduce_max(ms_step, world)
     value = world * T / (ms_step_max / 1e3)

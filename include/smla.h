@@ -231,19 +231,33 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
  * the library until the process exits. Limit: n_tokens * topk * 4 + 256
  * bytes must fit in 16 MiB (e.g. 2047 tokens at topk = 2048); larger calls
  * return SMLA_ERR_WORKSPACE and enqueue nothing. The f16 copy of a BF16 cache
- * (see smla_sparse_mla_prefill) is made only if it fits in the rest. The selected indices are
- * not returned. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. Every call on a device shares the one
- * array and leaves its contents behind (each call clears the status word
- * and rewrites the index list): calls whose work overlaps on the GPU, on
- * different streams or threads, race and give wrong results. Arguments
- * otherwise as smla_sparse_mla_prefill.
+ * (see smla_sparse_mla_prefill) is made only if it fits in the rest, and the
+ * deferred candidate buffers of rows longer than 16,384 keys never do: such
+ * rows take their exact top-k inside the scoring kernel (same index sets). The
+ * selected indices are not returned. Device-side errors (an out-of-range page,
+ * a bounded wait that gave up) go to the array's status word: read them with
+ * smla_noalloc_read_status after the call. The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. The address is kept per
+ * device for the process: it belongs to the runtime's primary context of the
+ * device, so calls from another context (made current through the driver API)
+ * and calls after cudaDeviceReset are not supported. Every call on a device
+ * shares the one array and leaves its contents behind (each call clears the
+ * status word and rewrites the index list): calls whose work overlaps on the
+ * GPU, on different streams or threads, race and give wrong results.
+ * Arguments otherwise as smla_sparse_mla_prefill.
  * ------------------------------------------------------------------------- */
 int smla_sparse_mla_prefill_noalloc(const smla_paged_cache* cache, const int32_t* page_table,
                                     int32_t prefix_len, int32_t n_tokens, const void* q, int32_t n_heads,
                                     const void* q_idx, const float* w, int32_t h_idx, int32_t topk,
                                     float sm_scale, void* out, float* lse, void* stream);
+
+/* smla_noalloc_read_status — smla_read_status for the status word of
+ * smla_sparse_mla_prefill_noalloc (the first word of the library's scratch
+ * array on the current device): waits for `stream`, then returns the status of
+ * the calls since the last one began, with the raw bits in *bits if non-NULL.
+ * Allocates nothing. (No counterpart in the pages either.) */
+int smla_noalloc_read_status(void* stream, uint32_t* bits);
 
 /* ---------------------------------------------------------------------------
  * smla_read_status — waits for `stream`, then reads the device status word of

@@ -30,6 +30,7 @@ SMLA_BF16, SMLA_FP8_E4M3, SMLA_FP8_DS_MLA = 0, 1, 2
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_WORKSPACE",
           4: "SMLA_ERR_CUDA", 5: "SMLA_ERR_DEVICE_BOUNDS", 6: "SMLA_ERR_TIMEOUT"}
 D_QK, D_V, PAGE = 576, 512, 64
+STATUS_BYTES = 256  # the status word heads every workspace
 
 _lock = threading.Lock()
 _lib = None
@@ -106,6 +107,7 @@ _SIGS = {
                                                _i32, _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "smla_sparse_mla_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
                                                         _f32, _vp, _vp, _vp]),
+    "smla_noalloc_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "smla_read_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -264,6 +266,12 @@ class HostPrefill:
     workspace, streams and events are made once here; run() may be called
     repeatedly (each call waits for the previous call's use of a chunk's
     device buffers before reusing them).
+
+    Chunk c is given the workspace from byte 256 * c on, so its status word
+    (the first 256 bytes of what it is given) is its own: the scratch of chunk c
+    covers only the status words of later chunks, which clear theirs when they
+    start, so after run() every chunk's word is intact and read_status() reports
+    the device errors of all of them.
     """
 
     def __init__(self, cache, page_table, prefix_len, n_tokens, n_heads, h_idx, d_idx, idx_dtype, topk,
@@ -279,7 +287,7 @@ class HostPrefill:
         self.lse = torch.empty((n_tokens, n_heads), dtype=torch.float32, device=device)
         need = max(prefill_workspace_bytes(prefix_len + a, b - a, n_heads, h_idx, topk, cache.kv_dtype)
                    for a, b in self.chunks)
-        self.ws = workspace(need, device)
+        self.ws = workspace(need + STATUS_BYTES * len(self.chunks), device)
         self.s_in, self.s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
         n = len(self.chunks)
         self.ev_in = [torch.cuda.Event() for _ in range(n)]
@@ -303,7 +311,7 @@ class HostPrefill:
             comp.wait_event(self.ev_out[c])  # the previous run's copy-out of these outputs
             sparse_mla_prefill(self.cache, self.page_table, self.prefix_len + a, self.q[a:b], self.q_idx[a:b],
                                self.w[a:b], self.topk, self.sm_scale, out=self.out[a:b], lse=self.lse[a:b],
-                               ws=self.ws, stream=comp)
+                               ws=self.ws[STATUS_BYTES * c:], stream=comp)
             self.ev_comp[c].record(comp)
             with torch.cuda.stream(self.s_out):
                 self.s_out.wait_event(self.ev_comp[c])
@@ -312,6 +320,27 @@ class HostPrefill:
                 self.ev_out[c].record(self.s_out)
         for c in range(len(self.chunks)):
             comp.wait_event(self.ev_out[c])  # the call ends on `stream` once every result is on the host
+
+    def read_status(self, stream=None):
+        """(status code, raw bits) over every chunk of the last run() (waits on
+        the stream)."""
+        return read_status_chunks(self.ws, len(self.chunks), stream)
+
+
+# precedence of the device status codes (as smla_read_status orders them)
+_STATUS_RANK = {0: 0, 2: 1, 5: 2, 6: 3}
+
+
+def read_status_chunks(ws: torch.Tensor, n_chunks: int, stream=None):
+    """Status of n_chunks calls whose workspaces start at ws + 256 * c: the most
+    severe code and the union of the raw bits."""
+    code, bits = 0, 0
+    for c in range(n_chunks):
+        rc, b = read_status(ws[STATUS_BYTES * c:], stream)
+        bits |= b
+        if _STATUS_RANK.get(rc, 4) > _STATUS_RANK.get(code, 4):
+            code = rc
+    return code, bits
 
 
 def decode_workspace_bytes(n_seqs, max_seq_len, q_per_seq, n_heads, h_idx, topk) -> int:

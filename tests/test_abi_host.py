@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_symbols_exported(L):
     names = declared_functions()
-    assert len(names) == 12
+    assert len(names) == 13
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(smla._SIGS), "binding signatures and header disagree"

@@ -374,3 +374,25 @@ def test_indexer_head_counts(h_idx, prefix):
         ok = g_i[r] >= 0
         full = oracle.Oracle(prob).scores(int(rows[r]))
         assert np.array_equal(g_s[r][ok], full[g_i[r][ok]])
+
+
+def test_host_prefill_reports_errors_of_every_chunk():
+    """Each chunk of the host-buffer prefill keeps its own status word: a query
+    value outside the f16 range in a row of the FIRST chunk is still reported
+    after run() (later chunks start with clean words of their own), and a run
+    on clean inputs reports nothing."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=3000, prefix_len=500, shuffled=True)
+    dev = wl.make(spec, "cuda")
+    hp = smla.HostPrefill(dev.cache, dev.page_table, spec.prefix_len, spec.n_tokens, spec.n_heads, spec.h_idx,
+                          spec.d_idx, spec.idx_dtype, spec.topk, spec.sm_scale, chunk=1024)
+    q_bad = dev.q.cpu()
+    q_bad[5, 3, 10] = 70000.0  # beyond f16's 65504
+    q_bad = q_bad.pin_memory()
+    qi_h, w_h = dev.q_idx.cpu().pin_memory(), dev.w.cpu().pin_memory()
+    out_h = torch.empty((spec.n_tokens, spec.n_heads, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((spec.n_tokens, spec.n_heads), dtype=torch.float32).pin_memory()
+    hp.run(q_bad, qi_h, w_h, out_h, lse_h)
+    rc, bits = hp.read_status()
+    assert rc == 2 and bits & 4, (rc, bits)  # SMLA_ERR_UNSUPPORTED, the overflow bit
+    hp.run(dev.q.cpu().pin_memory(), qi_h, w_h, out_h, lse_h)
+    assert hp.read_status() == (0, 0)
