@@ -161,10 +161,12 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
  * value beyond it is reported by smla_read_status as SMLA_ERR_UNSUPPORTED.
  * Supported: n_heads in {16, 64} (16 and 64 query heads of the configurations),
  * topk <= 2048.
- * Workspace: 256 bytes suffice. For a BF16 cache of one sequence (seq_lens
- * NULL) a larger workspace, as returned for max_keys = prefix_len + q_per_seq,
- * lets the call first widen the sequence's rows to f16 once (576 * 2 bytes per
- * key) so the attention gathers them without per-row conversion.
+ * Workspace: 256 bytes suffice. For a BF16 or SMLA_FP8_E4M3 cache of one
+ * sequence (seq_lens NULL) a larger workspace, as returned for max_keys =
+ * prefix_len + q_per_seq, lets the call first widen the sequence's rows to f16
+ * once (576 * 2 bytes per key, plus 4 bytes per key for the FP8 scales kept in
+ * the same order) so the attention gathers them without per-row conversion.
+ * Both widenings are exact, so the result does not depend on the workspace.
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_fwd_workspace_size(int32_t max_keys, int32_t rows, int32_t n_heads, int32_t topk,
                                           int32_t kv_dtype);
@@ -184,11 +186,12 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
  *              in the workspace only.
  * Workspace: at least 256 + n_tokens * topk * 4 bytes (rounded to 256). The
  * returned size lays out, in order: the status word, the index list, for
- * kv_dtype = SMLA_BF16 an f16 copy of the sequence's prefix_len + n_tokens
- * cache rows (written once per call and gathered by the attention without
- * per-row conversion), and the indexer's deferred candidate buffers (see
- * smla_indexer_topk). Each optional part is used only when the workspace
- * reaches its end.
+ * kv_dtype = SMLA_BF16 or SMLA_FP8_E4M3 an f16 copy of the sequence's
+ * prefix_len + n_tokens cache rows (widened exactly, written once per call and
+ * gathered by the attention without per-row conversion; for FP8 followed by
+ * the rows' scales in the same order), and the indexer's deferred candidate
+ * buffers (see smla_indexer_topk). Each optional part is used only when the
+ * workspace reaches its end.
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t n_heads,
                                               int32_t h_idx, int32_t topk, int32_t kv_dtype);
@@ -230,7 +233,7 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
  * is a fixed 16 MiB array inside the library, held by every GPU that loads
  * the library until the process exits. Limit: n_tokens * topk * 4 + 256
  * bytes must fit in 16 MiB (e.g. 2047 tokens at topk = 2048); larger calls
- * return SMLA_ERR_WORKSPACE and enqueue nothing. The f16 copy of a BF16 cache
+ * return SMLA_ERR_WORKSPACE and enqueue nothing. The f16 copy of the cache rows
  * (see smla_sparse_mla_prefill) is made only if it fits in the rest, and the
  * deferred candidate buffers of rows longer than 16,384 keys never do: such
  * rows take their exact top-k inside the scoring kernel (same index sets). The

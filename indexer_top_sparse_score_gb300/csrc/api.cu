@@ -159,7 +159,7 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
 
 // ----------------------------------------------------------------- sparse MLA (given indices)
 size_t smla_sparse_mla_fwd_workspace_size(int32_t max_keys, int32_t, int32_t, int32_t, int32_t kv_dtype) {
-  return kStatusBytes + (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(max_keys) : 0);
+  return kStatusBytes + mla_shadow_bytes(max_keys, kv_dtype);
 }
 
 static int mla_checks(const smla_paged_cache* cache, const int32_t* page_tables, int32_t max_pages,
@@ -194,10 +194,10 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
   if ((rc = reset_status(workspace, st))) return rc;
   MlaLaunch L{cache, page_tables, max_pages, n_seqs, q_per_seq, seq_lens, prefix_len, q, n_heads, idx, topk,
               sm_scale, out, lse, static_cast<uint32_t*>(workspace), st};
-  // one BF16 sequence and room in the workspace: widen its rows once, gather f16
+  // one sequence and room in the workspace: widen its rows once, gather f16
   const int32_t n_keys = prefix_len + q_per_seq;
-  if (!seq_lens && cache->kv_dtype == SMLA_BF16 &&
-      workspace_bytes >= kStatusBytes + mla_shadow_bytes(n_keys)) {
+  const size_t shadow_bytes = mla_shadow_bytes(n_keys, cache->kv_dtype);
+  if (!seq_lens && shadow_bytes > 0 && workspace_bytes >= kStatusBytes + shadow_bytes) {
     L.shadow = static_cast<uint8_t*>(workspace) + kStatusBytes;
     L.shadow_rows = n_keys;
     if ((rc = launch_shadow_convert(L))) return rc;
@@ -210,7 +210,7 @@ size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_toke
                                               int32_t topk, int32_t kv_dtype) {
   if (prefix_len < 0 || n_tokens <= 0 || topk <= 0) return kStatusBytes;
   return prefill_min_workspace(n_tokens, topk) +
-         (kv_dtype == SMLA_BF16 ? mla_shadow_bytes(prefix_len + n_tokens) : 0) +
+         mla_shadow_bytes(prefix_len + n_tokens, kv_dtype) +
          indexer_group_cand_bytes(n_tokens, n_tokens, h_idx, topk,
                                   static_cast<int32_t>(std::min<int64_t>(INT32_MAX, int64_t(prefix_len) + n_tokens)));
 }
@@ -240,9 +240,9 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   int32_t* idx = out_idx ? out_idx : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   IndexerLaunch IL{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, static_cast<int32_t>(total), q_idx,
                    w, h_idx, topk, idx, nullptr, workspace, workspace_bytes, st};
-  // layout: status | index list | f16 shadow (BF16 caches) | deferred candidate buffers
-  const size_t cand_off =
-      ws_min + (cache->kv_dtype == SMLA_BF16 ? mla_shadow_bytes(static_cast<int32_t>(total)) : 0);
+  // layout: status | index list | f16 shadow (BF16 and FP8 caches) | deferred candidate buffers
+  const size_t shadow_bytes = mla_shadow_bytes(static_cast<int32_t>(total), cache->kv_dtype);
+  const size_t cand_off = ws_min + shadow_bytes;
   if (workspace_bytes > cand_off) {
     IL.cand = static_cast<uint8_t*>(workspace) + cand_off;
     IL.cand_bytes = workspace_bytes - cand_off;
@@ -250,8 +250,8 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   if ((rc = launch_indexer(IL))) return rc;
   MlaLaunch ML{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, q, n_heads, idx, topk, sm_scale, out,
                lse, static_cast<uint32_t*>(workspace), st};
-  // BF16 cache and room in the workspace: widen the sequence's rows once, gather f16
-  if (cache->kv_dtype == SMLA_BF16 && workspace_bytes >= ws_min + mla_shadow_bytes(static_cast<int32_t>(total))) {
+  // room in the workspace: widen the sequence's rows once, gather f16
+  if (shadow_bytes > 0 && workspace_bytes >= ws_min + shadow_bytes) {
     ML.shadow = static_cast<uint8_t*>(workspace) + ws_min;
     ML.shadow_rows = static_cast<int32_t>(total);
     if ((rc = launch_shadow_convert(ML))) return rc;

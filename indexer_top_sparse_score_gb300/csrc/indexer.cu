@@ -52,6 +52,11 @@ constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
+// Streaming prefill with 32 indexer heads: four tokens per item, one epilogue
+// warpgroup per token (16 epilogue warps), see the epilogue.
+constexpr int kTokWarpgroups = 4;
+constexpr int kTokThreads = 128 + 128 * kTokWarpgroups;
+constexpr int kHistWords = 3 * 256 * kTokWarpgroups;  // selection histograms, one set per warpgroup
 constexpr int kMaxAcc = 4;                            // TMEM accumulator buffers at most
 constexpr int kIssuers = 2;                           // MMA issuer warps
 static_assert(kStages % kIssuers == 0 && kSplitStages % kIssuers == 0 && kMaxAcc % kIssuers == 0,
@@ -81,6 +86,7 @@ struct IdxParams {
   uint32_t* cand_idx;
   int32_t* cand_cnt;
   int32_t defer;       // group mode: hand rows with more than topk candidates to finish_kernel
+  int32_t rot_span;    // group mode: tiles over which the CTAs' start tiles are spread (0: the whole range)
   uint32_t* scores;    // split mode: score keys [rows][score_stride], written for keys 0..pos
   int64_t score_stride;
   uint32_t* status;
@@ -179,7 +185,8 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, co
   if (it.key_hi <= it.key_lo) return 0;
   it.t0 = it.key_lo / kTileKeys;
   it.t1 = (it.key_hi + kTileKeys - 1) / kTileKeys;
-  it.rot = static_cast<int>((blockIdx.x * 97u + static_cast<unsigned>(k) * 31u) % static_cast<unsigned>(it.t1 - it.t0));
+  const int span = (!p.split && p.rot_span > 0) ? min(p.rot_span, it.t1 - it.t0) : it.t1 - it.t0;
+  it.rot = static_cast<int>((blockIdx.x * 97u + static_cast<unsigned>(k) * 31u) % static_cast<unsigned>(span));
   return 1;
 }
 
@@ -223,11 +230,13 @@ __device__ __forceinline__ void smem_inc(uint32_t* p) {
 
 // SPLIT: decode shape (compile-time, so the decode kernel carries none of the
 // candidate-selection code). DENSE: prefill rows short enough that every
-// score of a work item fits in shared memory (see the epilogue).
-template <int HI, bool SPLIT, bool DENSE>
-__global__ void __launch_bounds__(kThreads, 1)
+// score of a work item fits in shared memory (see the epilogue). TOK: the
+// streaming prefill with one epilogue warpgroup per token (32 heads).
+template <int HI, bool SPLIT, bool DENSE, bool TOK>
+__global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IdxParams p) {
+  static_assert(!TOK || (HI == 32 && !SPLIT && !DENSE), "the token-per-warpgroup mode is a 32-head prefill mode");
   constexpr int TPW_MAX = 64 / HI;  // tokens per epilogue warpgroup held in registers
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* a_tiles = smem;
@@ -235,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* ckey = reinterpret_cast<uint32_t*>(b_tile + kMaxN * kIdxRowBytes);
   uint32_t* cidx = ckey + kBufEntries;
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]; dense mode [2][4][256]
-  uint32_t* scratch = hist + 2048;                              // [2][16]
-  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 32);      // [2 tile parities][128 tokens]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]; dense [2][4][256]; TOK [4][3][256]
+  uint32_t* scratch = hist + kHistWords;                        // [2][16]; TOK [4][16]
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 64);      // [2 tile parities][128 tokens]
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 256);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]
   uint32_t* wcnt = wsum + 16;                                   // [2 wg][2 parities][16 tokens][4 warps]
@@ -257,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qb_x = ring_x + 2 * (kSplitStages - kStages);  // [full, empty] of query buffer 1
   auto q_full = [&](int qb) { return qb == 0 ? b_full : qb_x; };
   auto q_empty = [&](int qb) { return qb == 0 ? b_empty : qb_x + 1; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qb_x + 2);
+  uint64_t* wg_bar = qb_x + 2;  // TOK: one barrier per epilogue warpgroup (its four warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + kTokWarpgroups);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,8 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], (SPLIT || DENSE) ? 4 : kEpiThreads / 32);  // one warpgroup per buffer
+      // one warpgroup per buffer; TOK: every epilogue warp reads every buffer
+      mbar_init(&acc_empty[i], TOK ? 4 * kTokWarpgroups : (SPLIT || DENSE) ? 4 : kEpiThreads / 32);
     }
+    for (int i = 0; i < kTokWarpgroups; ++i) mbar_init(&wg_bar[i], 4);
+    for (int i = 0; i < 8 * kTokWarpgroups; ++i) wcnt[i] = 0;  // TOK: per-token counters
     mbar_init(b_full, 1);
     mbar_init(b_empty, kIssuers);
     mbar_init(q_full(1), 1);
@@ -456,6 +469,466 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_warp(q_empty(qb));
     }
   } else if (warp >= 4) {
+    if constexpr (TOK) {
+      // ---------------------------------------------------------- epilogue, one warpgroup per token
+      // Warpgroup g (warps 4g+4 .. 4g+7) owns row g of every item (four rows at
+      // 32 heads, N = 128) and reads that row's 32 accumulator columns of every
+      // tile; its four warps cover the four TMEM lane quadrants (32 keys each).
+      // A key whose score reaches the row's threshold is appended to the row's
+      // candidate buffer at a position reserved with one shared-memory atomic
+      // per warp and tile: there is no barrier per tile. A warp whose
+      // reservation runs past the buffer's end keeps its entries in registers
+      // and requests a cut; the four warps of that warpgroup alone then meet on
+      // their own mbarrier (entered from wherever each warp is: while waiting
+      // for its next accumulator, or at the end of the item), cut the buffer to
+      // a superset of the row's top-k, raise the row's threshold and append the
+      // held entries. The other warpgroups keep scoring meanwhile, up to the
+      // depth of the accumulator ring. A warp waiting for an accumulator keeps
+      // watching for a cut request of its warpgroup, so no warp can hold the
+      // ring while its peers wait for it in a cut. At the end of an item a row
+      // with more than topk candidates goes to the workspace for finish_kernel
+      // (or, without room there, is selected here); the final index list of
+      // every row is in ascending index order.
+      const int ew = warp - 4;
+      const int g = ew >> 2;
+      const int q = warp & 3;
+      const int w4 = ew & 3;
+      const int tid_wg = w4 * 32 + lane;
+      const int cap = p.cap;
+      const int topk = p.topk;
+      uint32_t* kb = ckey + g * cap;
+      uint32_t* ib = cidx + g * cap;
+      // per-token state: [0] entries in the buffer, [1] threshold key, [2] cut
+      // requested, [3] items whose tiles this warpgroup's warps have finished
+      uint32_t* stw = wcnt + 8 * g;
+      volatile uint32_t* vst = stw;
+      uint32_t* hist_wg = hist + 768 * g;
+      uint32_t* red_wg = scratch + 16 * g;
+      const uint32_t lanemask_lt = (1u << lane) - 1u;
+      uint32_t bar_phase = 0;  // phases of wg_bar[g] this warp has completed
+      bool ok = true;
+      bool hold = false;       // this lane keeps an entry that did not fit
+      uint32_t hkey = 0, hidx = 0;
+
+      // The four warps of the warpgroup meet (bounded; false once the kernel gives up).
+      auto meet = [&]() -> bool {
+        __syncwarp();
+        bool r = true;
+        if (lane == 0) {
+          mbar_arrive(&wg_bar[g]);
+          r = mbar_wait_spin(&wg_bar[g], bar_phase & 1u, abort_v, p.status);
+        }
+        ++bar_phase;
+        r = __shfl_sync(0xFFFFFFFFu, r, 0);
+        __syncwarp();
+        if (!r) ok = false;
+        return r;
+      };
+      auto sync = [&]() { meet(); };
+      // Keep the entries of [0, n) that pass `take`, in place, in a fixed order
+      // (rounds of 2048 entries, 16 per thread). Returns the count, or -1.
+      auto compact = [&](int n, auto take) -> int {
+        int base = 0;
+        for (int r0 = 0, rnd = 0; r0 < n; r0 += 2048, ++rnd) {
+          uint32_t kk[16], ii[16];
+          bool tk16[16];
+          int c = 0;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int e0 = r0 + 4 * tid_wg + 512 * v;
+            uint4 kv = make_uint4(0, 0, 0, 0), iv = make_uint4(0, 0, 0, 0);
+            if (e0 < n) {
+              kv = *reinterpret_cast<const uint4*>(kb + e0);
+              iv = *reinterpret_cast<const uint4*>(ib + e0);
+            }
+            kk[4 * v + 0] = kv.x; kk[4 * v + 1] = kv.y; kk[4 * v + 2] = kv.z; kk[4 * v + 3] = kv.w;
+            ii[4 * v + 0] = iv.x; ii[4 * v + 1] = iv.y; ii[4 * v + 2] = iv.z; ii[4 * v + 3] = iv.w;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              tk16[4 * v + u] = e0 + u < n && take(kk[4 * v + u], ii[4 * v + u]);
+              c += tk16[4 * v + u];
+            }
+          }
+          int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t2;
+          }
+          uint32_t* ws = red_wg + 8 + 4 * (rnd & 1);
+          if (lane == 31) ws[w4] = static_cast<uint32_t>(incl);
+          if (!meet()) return -1;
+          int off = base, total = 0;
+#pragma unroll
+          for (int w2 = 0; w2 < 4; ++w2) {
+            const int v = static_cast<int>(ws[w2]);
+            if (w2 < w4) off += v;
+            total += v;
+          }
+          off += incl - c;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            if (!tk16[u]) continue;
+            if (off < cap) {
+              kb[off] = kk[u];
+              ib[off] = ii[u];
+            }
+            ++off;
+          }
+          base += total;
+        }
+        return base;
+      };
+      // Cut the buffer of this warpgroup's row to a superset of its top-k and
+      // raise the threshold; then append the held entries. All four warps call
+      // it (each from wherever it noticed the request).
+      auto cut = [&]() -> bool {
+        if (!meet()) return false;  // every warp's reservations and writes are done
+        const int n = min(static_cast<int>(vst[0]), cap);
+        // 1. the range of the buffer's keys (clears the histogram meanwhile)
+        uint32_t lo = 0xFFFFFFFFu, hi = 0;
+        for (int e0 = 4 * tid_wg; e0 < n; e0 += 512) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+          const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e0 + u < n) {
+              lo = min(lo, v4[u]);
+              hi = max(hi, v4[u]);
+            }
+        }
+        lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+        hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+        if (lane == 0) {
+          red_wg[w4] = lo;
+          red_wg[4 + w4] = hi;
+        }
+        hist_wg[tid_wg] = 0;
+        hist_wg[tid_wg + 128] = 0;
+        if (!meet()) return false;
+        lo = min(min(red_wg[0], red_wg[1]), min(red_wg[2], red_wg[3]));
+        hi = max(max(red_wg[4], red_wg[5]), max(red_wg[6], red_wg[7]));
+        const uint32_t range = hi - lo;
+        const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
+        // 2. histogram of the keys over 256 bins of [lo, hi]
+        for (int e0 = 4 * tid_wg; e0 < n; e0 += 512) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+          const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e0 + u < n && v4[u] >= lo && v4[u] <= hi) smem_inc(&hist_wg[(v4[u] - lo) >> shift]);
+        }
+        if (!meet()) return false;
+        // 3. every warp: the bin holding the topk-th best key and the entries
+        //    from that bin up (lane l owns bins 255-8l down to 248-8l)
+        uint32_t c8[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c8[i] = hist_wg[255 - 8 * lane - i];
+          sum += c8[i];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        const uint32_t excl = incl - sum;
+        uint32_t mine = 0, kept = 0;
+        if (excl < static_cast<uint32_t>(topk) && incl >= static_cast<uint32_t>(topk)) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + c8[i] >= static_cast<uint32_t>(topk)) {
+              mine = 0x80000000u | (255u - 8u * lane - i);
+              kept = run + c8[i];
+              break;
+            }
+            run += c8[i];
+          }
+        }
+        const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine != 0)) - 1;
+        uint32_t tk = 0, ti = 0xFFFFFFFFu;
+        bool exact = false;
+        if (src >= 0) {  // more than topk entries (always: a cut is requested when the buffer overflows)
+          const uint32_t bin = __shfl_sync(0xFFFFFFFFu, mine, src) & 0xFFu;
+          kept = __shfl_sync(0xFFFFFFFFu, kept, src);
+          tk = lo + (bin << shift);
+          // a bin too full (heavy ties) would free too little room: exact selection
+          exact = static_cast<int>(kept) > cap - 512;
+        }
+        if (!meet()) return false;  // the histogram is read; wg_select reuses it
+        if (exact && n > topk) {
+          wg_select(kb, ib, n, topk, tid_wg, hist_wg, red_wg, sync, tk, ti);
+          if (!ok) return false;
+        }
+        const uint32_t ctk = tk, cti = ti;
+        const int m = exact ? compact(n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, ctk, cti); })
+                            : compact(n, [&](uint32_t k2, uint32_t) { return k2 >= ctk; });
+        if (m < 0 || !meet()) return false;
+        // later keys from the cut value up are admitted: keys arrive in no
+        // particular order, so one equal to it may still win on its index
+        if (tid_wg == 0) {
+          stw[0] = static_cast<uint32_t>(m);
+          stw[1] = tk;
+          stw[2] = 0;
+        }
+        if (!meet()) return false;
+        // 4. the held entries (at most one per lane) that still qualify
+        const bool re = hold && hkey >= tk;
+        hold = false;
+        const uint32_t mm = __ballot_sync(0xFFFFFFFFu, re);
+        if (mm) {
+          uint32_t old = 0;
+          if (lane == 0) old = atomicAdd(&stw[0], static_cast<uint32_t>(__popc(mm)));
+          old = __shfl_sync(0xFFFFFFFFu, old, 0);
+          const uint32_t pos = old + __popc(mm & lanemask_lt);
+          if (re) {
+            if (pos < static_cast<uint32_t>(cap)) {
+              kb[pos] = hkey;
+              ib[pos] = hidx;
+            } else {
+              set_status(p.status, kStatusTimeout);  // cannot happen: a cut frees >= 128 slots
+            }
+          }
+        }
+        return meet();
+      };
+      // Ascending index order of the first m entries (bitonic network over the
+      // next power of two, padded with the largest index).
+      auto sort_by_index = [&](int m) -> bool {
+        int P = 1;
+        while (P < m) P <<= 1;
+        for (int e = m + tid_wg; e < P; e += 128) {
+          ib[e] = 0xFFFFFFFFu;
+          kb[e] = 0;
+        }
+        if (!meet()) return false;
+        for (int size = 2; size <= P; size <<= 1)
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid_wg; i < P / 2; i += 128) {
+              const int a = 2 * i - (i & (stride - 1));
+              const int b = a + stride;
+              const bool up = (a & size) == 0;
+              const uint32_t ia = ib[a], ibb = ib[b];
+              if ((ia > ibb) == up) {
+                const uint32_t ka = kb[a];
+                ib[a] = ibb;
+                ib[b] = ia;
+                kb[a] = kb[b];
+                kb[b] = ka;
+              }
+            }
+            if (!meet()) return false;
+          }
+        return true;
+      };
+
+      uint32_t ac = 0, items_done = 0;
+      for (int k = 0; ok; ++k) {
+        Item it;
+        const int r = next_item(p, k, it, pref);
+        if (r < 0) break;
+        if (r == 0) continue;
+        const bool active = g < it.nrows;
+        const int row = it.row0 + g;
+        if (it.trivial) {
+          // every key of the row is selected: 0..pos, then -1
+          if (active) {
+            const int n = it.pos0 + g + 1;
+            int32_t* o = p.out_idx + static_cast<size_t>(row) * topk;
+            for (int e = tid_wg; e < topk; e += 128) o[e] = e < n ? e : -1;
+            if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;
+          }
+          continue;
+        }
+        // the row's head weights, read back as float4 broadcasts per tile; the
+        // row's state starts empty (reset here, not at the end of the previous
+        // item: every warp reads the final count there before the last meeting)
+        float* wrow = wbuf + g * HI;
+        if (tid_wg < HI) wrow[tid_wg] = active ? __ldg(p.w + static_cast<size_t>(row) * HI + tid_wg) : 0.0f;
+        if (tid_wg == 0) {
+          stw[0] = 0;
+          stw[1] = 0;
+        }
+        if (!meet()) break;
+        const float4* wv4 = reinterpret_cast<const float4*>(wrow);
+        const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
+        const uint32_t ac0 = ac;
+        const int nt = it.t1 - it.t0;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * HI);
+        for (int tt = 0; tt < nt && ok; ++tt) {
+          const uint32_t gt = ac0 + tt;
+          const int buf = gt & 3;
+          // wait for the tile's accumulator, serving cut requests meanwhile
+          {
+            // lane 0 polls; bit 1: a cut is requested (served first: a warp
+            // that holds an entry has requested one and must not take another
+            // tile before it is appended), bit 0: the accumulator is ready,
+            // bit 2: give up (the kernel aborts or the wait ran out)
+            const uint32_t par = (gt >> 2) & 1u;
+            const long long t0 = clock64();
+            for (uint32_t itw = 0;; ++itw) {
+              uint32_t st2 = 0;
+              if (lane == 0) {
+                st2 = vst[2] ? 2u : (mbar_test_wait(&acc_full[buf], par) ? 1u : 0u);
+                // the limit holds for the whole wait, cuts served included
+                if (st2 != 1u && (itw & 15u) == 15u) {
+                  if (*abort_v) {
+                    st2 = 4u;
+                  } else if (clock64() - t0 > kWaitLimitCycles) {
+                    set_status(p.status, kStatusTimeout);
+                    *abort_v = 1;
+                    st2 = 4u;
+                  }
+                }
+              }
+              st2 = __shfl_sync(0xFFFFFFFFu, st2, 0);
+              if (st2 & 4u) {
+                ok = false;
+                break;
+              }
+              if (st2 & 2u) {
+                if (!cut()) break;
+                continue;
+              }
+              if (st2 & 1u) break;
+            }
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const int t = tile_at(it, tt);
+          const int s = t * kTileKeys + q * 32 + lane;
+          uint32_t key = 0;
+          if (active) {
+            uint32_t raw[32];
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN), raw);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            float ks = 1.0f;
+            if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+            float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int h = 0; h < HI; h += 8) {
+              const float4 wa = wv4[h / 4], wb = wv4[h / 4 + 1];
+              fma2(a[0], a[1], wa.x, wa.y, fmaxf(__uint_as_float(raw[h + 0]), 0.0f),
+                   fmaxf(__uint_as_float(raw[h + 1]), 0.0f));
+              fma2(a[2], a[3], wa.z, wa.w, fmaxf(__uint_as_float(raw[h + 2]), 0.0f),
+                   fmaxf(__uint_as_float(raw[h + 3]), 0.0f));
+              fma2(a[4], a[5], wb.x, wb.y, fmaxf(__uint_as_float(raw[h + 4]), 0.0f),
+                   fmaxf(__uint_as_float(raw[h + 5]), 0.0f));
+              fma2(a[6], a[7], wb.z, wb.w, fmaxf(__uint_as_float(raw[h + 6]), 0.0f),
+                   fmaxf(__uint_as_float(raw[h + 7]), 0.0f));
+            }
+            key = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          }
+          const bool valid = active && s < it.key_hi && s <= it.pos0 + g;
+          const bool adm = valid && key >= vst[1];
+          const uint32_t m = __ballot_sync(0xFFFFFFFFu, adm);
+          if (m) {
+            uint32_t old = 0;
+            if (lane == 0) old = atomicAdd(&stw[0], static_cast<uint32_t>(__popc(m)));
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            const uint32_t pos = old + __popc(m & lanemask_lt);
+            if (adm) {
+              if (pos < static_cast<uint32_t>(cap)) {
+                kb[pos] = key;
+                ib[pos] = static_cast<uint32_t>(s);
+              } else {
+                hold = true;
+                hkey = key;
+                hidx = static_cast<uint32_t>(s);
+              }
+            }
+            if (lane == 0 && old + __popc(m) > static_cast<uint32_t>(cap)) vst[2] = 1u;
+          }
+        }
+        ac = ac0 + nt;
+        if (!ok) break;
+        // this warp is done with the item's tiles: wait for the other three,
+        // serving cut requests meanwhile (a request can only come from a tile)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd(&stw[3], 1u);
+        }
+        ++items_done;
+        {
+          // lane 0 polls; bit 1: a cut is requested (served first), bit 0: all
+          // four warps are done, bit 2: give up. The count is read before the
+          // request: a warp's request precedes its count (fenced), so a full
+          // count read first cannot miss a request read after it.
+          const long long t0 = clock64();
+          for (uint32_t itw = 0;; ++itw) {
+            uint32_t st2 = 0;
+            if (lane == 0) {
+              const uint32_t done = vst[3];
+              __threadfence_block();
+              if (vst[2]) st2 = 2u;
+              else if (static_cast<int>(done - 4u * items_done) >= 0) st2 = 1u;
+              // the limit holds for the whole wait, cuts served included
+              if (st2 != 1u && (itw & 15u) == 15u) {
+                if (*abort_v) {
+                  st2 = 4u;
+                } else if (clock64() - t0 > kWaitLimitCycles) {
+                  set_status(p.status, kStatusTimeout);
+                  *abort_v = 1;
+                  st2 = 4u;
+                }
+              }
+            }
+            st2 = __shfl_sync(0xFFFFFFFFu, st2, 0);
+            if (st2 & 4u) {
+              ok = false;
+              break;
+            }
+            if (st2 & 2u) {
+              if (!cut()) break;
+              continue;
+            }
+            if (st2 & 1u) break;
+          }
+        }
+        if (!ok || !meet()) break;  // every append and cut of the item is done
+        // the row's result: to the workspace for finish_kernel, or selected here
+        if (active) {
+          const int n = min(static_cast<int>(vst[0]), cap);
+          int32_t* o = p.out_idx + static_cast<size_t>(row) * topk;
+          float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * topk : nullptr;
+          if (n > topk && p.defer) {
+            uint4* dk = reinterpret_cast<uint4*>(p.cand_key + static_cast<size_t>(row) * cap);
+            uint4* di = reinterpret_cast<uint4*>(p.cand_idx + static_cast<size_t>(row) * cap);
+            for (int e = 4 * tid_wg; e < n; e += 512) {
+              dk[e >> 2] = *reinterpret_cast<const uint4*>(kb + e);
+              di[e >> 2] = *reinterpret_cast<const uint4*>(ib + e);
+            }
+            if (tid_wg == 0) p.cand_cnt[row] = n;
+          } else {
+            int m = n;
+            if (n > topk) {
+              uint32_t tk = 0, ti = 0xFFFFFFFFu;
+              wg_select(kb, ib, n, topk, tid_wg, hist_wg, red_wg, sync, tk, ti);
+              if (!ok) break;
+              m = compact(n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, tk, ti); });
+              if (m < 0 || !meet()) break;
+            }
+            if (!sort_by_index(m)) break;
+            for (int e = tid_wg; e < topk; e += 128) {
+              o[e] = e < m ? static_cast<int32_t>(ib[e]) : -1;
+              if (os) os[e] = e < m ? key_score(kb[e]) : 0.0f;
+            }
+            if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;
+          }
+        }
+        if (!meet()) break;  // the buffer is free for the next item
+      }
+    } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 4;
     const int wg = ew >> 2;
@@ -850,12 +1323,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       wg_sync();  // histograms, counts and staging are reused by the next row
     };
 
+    // A warp whose bounded wait gives up does not leave the item loop on its
+    // own: the epilogue warps meet at named barriers, which have no time
+    // limit. It carries on to its group's next barrier, where a vote tells
+    // every warp of the group to leave together (the item's first barrier
+    // for all epilogue warps, the per-tile barrier of a warpgroup in the
+    // streaming mode).
+    bool item_ok = true;
     for (int k = 0;; ++k) {
       Item it;
       const int r = next_item(p, k, it, pref);
       if (r < 0) break;
       if (r == 0) continue;
-      named_bar_sync(3, kEpiThreads);
+      if (named_bar_or(3, kEpiThreads, !item_ok)) break;
       for (int i = threadIdx.x - 128; i < N; i += kEpiThreads) {
         const int gi = it.row0 * HI + i;
         wbuf[i] = gi < p.n_rows * HI ? __ldg(p.w + gi) : 0.0f;
@@ -892,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t g = ac0 + tt;
           const int t = tile_at(it, tt);
           const int buf = g & ((1u << p.acc_shift) - 1);
-          if (!mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status)) {
+          if (__any_sync(0xFFFFFFFFu, !mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status))) {
             ok = false;
             break;
           }
@@ -934,7 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ac = ac0 + nt;
-        if (!ok) break;
+        item_ok = ok;  // a failure is voted on at the next item's first barrier
       } else if constexpr (DENSE) {
         // prefill, rows of at most `cap` keys: every score goes to the token's
         // array in shared memory at its key's position, so a tile needs no
@@ -957,7 +1437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t g = ac0 + tt;
           const int t = tile_at(it, tt);
           const int buf = g & ((1u << p.acc_shift) - 1);
-          if (!mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status)) {
+          if (__any_sync(0xFFFFFFFFu, !mbar_wait_backoff(&acc_full[buf], (g >> p.acc_shift) & 1, abort_v, p.status))) {
             ok = false;
             break;
           }
@@ -1058,16 +1538,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ac = ac0 + nt;
-        if (!ok) break;
-        named_bar_sync(3, kEpiThreads);  // every score of the item is in shared memory
+        // every score of the item is in shared memory (or some warp gave up a wait)
+        if (named_bar_or(3, kEpiThreads, !ok)) {
+          item_ok = false;
+          break;
+        }
         for (int j = wg; j < it.nrows; j += 2) dense_token(j, it);
       } else {
         // prefill: both warpgroups take every tile, each for its own query rows
         for (int tt = 0; tt < it.t1 - it.t0; ++tt, ++ac) {
           const int t = tile_at(it, tt);
           const int buf = ac & ((1 << p.acc_shift) - 1);
-          if (!mbar_wait_backoff(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status)) {
+          if (__any_sync(0xFFFFFFFFu, !mbar_wait_backoff(&acc_full[buf], (ac >> p.acc_shift) & 1, abort_v, p.status))) {
             ok = false;
+            named_bar_or(bar_wg, 128, true);  // the warpgroup's vote of this tile
             break;
           }
           tc_fence_after();
@@ -1123,7 +1607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < TPW_MAX; ++jj) wc[jj * 4 + (ew & 3)] = static_cast<uint32_t>(__popc(m[jj]));
           }
-          wg_sync();
+          if (named_bar_or(bar_wg, 128, false)) {  // a warp of the warpgroup gave up its wait
+            ok = false;
+            break;
+          }
 #pragma unroll
           for (int jj = 0; jj < TPW_MAX; ++jj) {
             const int j = j0 + jj;
@@ -1145,10 +1632,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid_wg == 0) cnt[(par ^ 1) * 128 + j] = cb + tot;
           }
         }
-        if (!ok) break;
-        wg_sync();
-        for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, cnt[(ac & 1u) * 128 + j], topk, true, it);
+        item_ok = ok;  // a failure is voted on at the next item's first barrier
+        if (ok) {
+          wg_sync();
+          for (int j = j0; j < j1 && j < it.nrows; ++j) select_token(j, cnt[(ac & 1u) * 128 + j], topk, true, it);
+        }
       }
+    }
     }
   }
 
@@ -1520,6 +2010,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
   int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
   float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
   const uint32_t lanemask_lt = (1u << lane) - 1u;
+  // the selected entries to the front, in place (a round's reads all precede its writes)
   int base = 0;
   for (int e0 = 0; e0 < n; e0 += kFinishThreads) {
     const int e = e0 + tid;
@@ -1543,18 +2034,45 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
     __syncthreads();
     if (take) {
       const int pos = off + __popc(m & lanemask_lt);
-      o[pos] = static_cast<int32_t>(ii);
-      if (os) os[pos] = key_score(kk);
+      keys[pos] = kk;
+      idxs[pos] = ii;
     }
     base += tot;
   }
-  for (int e = base + tid; e < p.topk; e += kFinishThreads) {
-    o[e] = -1;
-    if (os) os[e] = 0.0f;
+  // ascending index order (bitonic network over the next power of two, padded
+  // with the largest index), so a row's list does not depend on the order in
+  // which its candidates were gathered
+  int P = 1;
+  while (P < base) P <<= 1;
+  for (int e = base + tid; e < P; e += kFinishThreads) {
+    idxs[e] = 0xFFFFFFFFu;
+    keys[e] = 0;
+  }
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P / 2; i += kFinishThreads) {
+        const int a = 2 * i - (i & (stride - 1));
+        const int b = a + stride;
+        const bool up = (a & size) == 0;
+        const uint32_t ia = idxs[a], ib2 = idxs[b];
+        if ((ia > ib2) == up) {
+          const uint32_t ka = keys[a];
+          idxs[a] = ib2;
+          idxs[b] = ia;
+          keys[a] = keys[b];
+          keys[b] = ka;
+        }
+      }
+      __syncthreads();
+    }
+  for (int e = tid; e < p.topk; e += kFinishThreads) {
+    o[e] = e < base ? static_cast<int32_t>(idxs[e]) : -1;
+    if (os) os[e] = e < base ? key_score(keys[e]) : 0.0f;
   }
 }
 
-template <int HI, bool SPLIT, bool DENSE>
+template <int HI, bool SPLIT, bool DENSE, bool TOK = false>
 int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
   CUtensorMap map_k, map_q;
   const CUtensorMapDataType dt = prm.is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -1568,10 +2086,11 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
-                      2048 * 4 + 32 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 + (2 * kSplitStages + 2 * kMaxAcc + 4) * 8 + 16;
+                      kHistWords * 4 + 64 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 +
+                      (2 * kSplitStages + 2 * kMaxAcc + 4 + kTokWarpgroups) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT, DENSE, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     attr_done = true;
@@ -1582,7 +2101,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                          : prm.n_seqs <= kMaxPrefixSeqs ? static_cast<int>(std::min<int64_t>(split_tiles, 1 << 30))
                                                         : prm.n_items;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
-  indexer_kernel<HI, SPLIT, DENSE><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  indexer_kernel<HI, SPLIT, DENSE, TOK><<<grid, TOK ? kTokThreads : kThreads, smem, L.stream>>>(map_k, map_q, prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
@@ -1681,6 +2200,10 @@ int launch_indexer(const IndexerLaunch& L) {
   } else {
     prm.n_groups = (L.q_per_seq + tq - 1) / tq;
     prm.n_items = L.n_seqs * prm.n_groups;
+    // streaming prefill with 32 heads: the CTAs read the key tiles in nearly the
+    // same order (start tiles spread over 8 tiles), so a key range larger than
+    // L2 is read from HBM about once per wave of items instead of once per CTA
+    if (!dense && L.h_idx == 32) prm.rot_span = 8;
     const size_t cand = indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk, L.max_seq_len);
     if (L.cand && cand > 0 && L.cand_bytes >= cand && (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
       prm.defer = 1;
@@ -1704,8 +2227,9 @@ int launch_indexer(const IndexerLaunch& L) {
            : split ? launch_indexer_t<16, true, false>(L, prm) : launch_indexer_t<16, false, false>(L, prm);
       break;
     case 32:
+      // the streaming prefill runs one epilogue warpgroup per token
       rc = dense ? launch_indexer_t<32, false, true>(L, prm)
-           : split ? launch_indexer_t<32, true, false>(L, prm) : launch_indexer_t<32, false, false>(L, prm);
+           : split ? launch_indexer_t<32, true, false>(L, prm) : launch_indexer_t<32, false, false, true>(L, prm);
       break;
     case 64:
       rc = dense ? launch_indexer_t<64, false, true>(L, prm)

@@ -56,8 +56,9 @@ struct MlaLaunch {
   float* lse;
   uint32_t* status;
   cudaStream_t stream;
-  // f16 copy of the sequence's cache rows in logical token order (BF16 caches
-  // of a single sequence), or null to gather and widen the pool rows in-kernel
+  // f16 copy of the sequence's cache rows in logical token order (BF16 or
+  // per-token FP8 caches of a single sequence), or null to gather and widen the
+  // pool rows in-kernel
   void* shadow = nullptr;
   int32_t shadow_rows = 0;
   // room for the partial outputs of split rows (few rows: each row's
@@ -74,9 +75,10 @@ size_t mla_partial_bytes(int32_t n_rows, int32_t n_heads);
 
 // Workspace of a prefill without the optional f16 shadow (status + index list).
 size_t prefill_min_workspace(int32_t n_tokens, int32_t topk);
-// Bytes of the f16 shadow of n_keys cache rows (0 when unused).
-size_t mla_shadow_bytes(int32_t n_keys);
-// Fills the shadow from the BF16 pool through the page table (one sequence).
+// Bytes of the f16 shadow of n_keys cache rows (BF16 and per-token FP8
+// caches; the FP8 shadow also holds the scales), 0 for other formats.
+size_t mla_shadow_bytes(int32_t n_keys, int32_t kv_dtype);
+// Fills the shadow from the pool through the page table (one sequence).
 int launch_shadow_convert(const MlaLaunch& L);
 
 // Whether the indexer runs token groups over the full key range (prefill) or

@@ -79,6 +79,7 @@ struct MlaParams {
   int32_t fmt;  // latent cache format: kFmtBf16, kFmtTokenFp8 or kFmtTileFp8
   uint32_t* status;
   const uint16_t* shadow;  // f16 rows by logical position, or null
+  const float* shadow_scale;  // per-token FP8 scales by logical position (FP8 cache with a shadow)
   int32_t shadow_rows;
   // split rows: each row's blocks are cut into n_parts items of part_blocks
   // blocks; each item writes a normalised fp32 partial output and its lse
@@ -96,6 +97,7 @@ struct SmemMeta {
   float red[4][64];   // cross-warp reduction
   float linv[64];
   uint64_t q_full, q_empty, full[kGroups], empty[4], s_full, p_full, o_empty;
+  uint64_t gather_meet;  // the four gather warps meet here once per query row
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -132,17 +134,6 @@ __device__ __forceinline__ RowInfo row_info(const MlaParams& p, int item) {
   r.b0 = part * p.part_blocks;
   r.nb = max(0, min(nb_row - r.b0, p.part_blocks));
   return r;
-}
-
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = 0
@@ -270,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&M.s_full, 1);
     mbar_init(&M.p_full, 8);
     mbar_init(&M.o_empty, 8);
+    mbar_init(&M.gather_meet, kProducers / 32);
     M.abort_flag = 0;
     fence_mbar_init();
   }
@@ -364,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 384;
     const int psub = lane >> 3, pj = lane & 7;  // pass row offset, 16-byte piece
     const uint32_t st0 = smem_u32(stage);
-    uint32_t g = 0, tok = 0;
+    uint32_t g = 0, tok = 0, meet_phase = 0;
     bool ok = true;
     bool over = false;
     for (int k = 0; ok; ++k) {
@@ -443,7 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           *qp = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(2, kProducers);
+        // the four gather warps meet (a bounded wait on an mbarrier rather than a
+        // named barrier: a warp that gave up an earlier wait has left the loop,
+        // and the others must be able to give up too instead of waiting for it)
+        __syncwarp();
+        bool met = true;
+        if (lane == 0) {
+          mbar_arrive(&M.gather_meet);
+          met = mbar_wait_spin(&M.gather_meet, meet_phase & 1u, abort_v, p.status);
+        }
+        ++meet_phase;
+        if (!__shfl_sync(0xFFFFFFFFu, met, 0)) {
+          ok = false;
+          break;
+        }
         if (tid == 0) mbar_arrive(&M.q_full);
       }
       // keys three blocks ahead and page ids two ahead (each consumed a block
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t row_bytes = TILE ? kTileRowBytes : p.fmt == kFmtTokenFp8 ? kDqk : 2 * kDqk;
       for (int b = 0; b < ri.nb && ok; ++b, ++g) {
         float ks = 1.0f;
-        if (!TILE && p.fmt == kFmtTokenFp8 && loc >= 0) ks = __ldg(p.kv_scale + loc);
+        if (!TILE && p.fmt == kFmtTokenFp8 && loc >= 0) ks = __ldg((p.shadow ? p.shadow_scale : p.kv_scale) + loc);
         const int key3 = fetch_key(b + 3);
         const int loc1 = locate(key1, pg1);
         if (!p.shadow && loc1 >= 0) prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
@@ -689,21 +694,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      // A warp whose bounded wait gives up does not leave on its own: the eight
+      // softmax warps meet at named barriers, so it carries on (touching no
+      // accumulator) to the block's first barrier, which it makes take the
+      // branch whose next barrier is a vote on `failed`; all eight leave there
+      // together. The same vote ends a query row's epilogue.
       bool ok = true;
       for (int b = 0; b < ri.nb; ++b) {
         const uint32_t gb = g + b, ph = gb & 1;
-        if (!mbar_wait(&M.s_full, ph, abort_v, p.status) || !mbar_wait(&M.full[kGroups - 1], ph, abort_v, p.status)) {
-          ok = false;
-          break;
-        }
+        const bool failed = __any_sync(0xFFFFFFFFu, !mbar_wait(&M.s_full, ph, abort_v, p.status) ||
+                                                        !mbar_wait(&M.full[kGroups - 1], ph, abort_v, p.status));
         tc_fence_after();
         const float4 mt = M.row[ph][rrow];
-        const bool valid = mt.z != 0.0f;
+        const bool valid = !failed && mt.z != 0.0f;
         // (tcgen05.ld and its wait are warp-collective: every lane executes them,
         // `valid` only gates the arithmetic)
         uint32_t raw[HW];
-        tmem_ld_cols<HW>(tmem + lane_base + kColS + h0, raw);
-        tmem_wait_ld();
+        if (!failed) {
+          tmem_ld_cols<HW>(tmem + lane_base + kColS + h0, raw);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < HW; ++i) raw[i] = 0;
+        }
         // this thread's heads' reference maxima (16-byte broadcast loads)
         float mh[HW];
         auto load_m = [&]() {
@@ -718,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         load_m();
         // does any logit exceed its head's reference max by more than 2^8?
-        bool flag = b == 0;
+        bool flag = b == 0 || failed;
         if (!flag && valid) {
           float tmax = -INFINITY;
 #pragma unroll
@@ -734,7 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx = warp_reduce_scatter<HW>(x, lane, MaxOp());
             if ((lane & (32 / HW - 1)) == 0) M.red[qd][h0 + lane / (32 / HW)] = mx;
           }
-          named_bar_sync(1, 256);
+          if (named_bar_or(1, 256, failed)) {  // some warp gave up a wait: all leave
+            ok = false;
+            break;
+          }
           bool resc = false;
           if (tid < H) {
             const float bm = fmaxf(fmaxf(M.red[0][tid], M.red[1][tid]), fmaxf(M.red[2][tid], M.red[3][tid]));
@@ -800,23 +816,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      {
-        // the last PV of this query row has finished
-        const uint32_t gl = g + ri.nb - 1;
-        if (!mbar_wait(&M.empty[3], gl & 1, abort_v, p.status)) break;
-      }
+      // the last PV of this query row has finished (a warp that gives up the
+      // wait carries on to the vote below, as in the block loop)
+      const bool failed = __any_sync(0xFFFFFFFFu, !mbar_wait(&M.empty[3], (g + ri.nb - 1) & 1, abort_v, p.status));
       tc_fence_after();
       {
         uint32_t raw[HW];
-        tmem_ld_cols<HW>(tmem + lane_base + kColL + h0, raw);
-        tmem_wait_ld();
+        if (!failed) {
+          tmem_ld_cols<HW>(tmem + lane_base + kColL + h0, raw);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < HW; ++i) raw[i] = 0;
+        }
         float x[HW];
 #pragma unroll
         for (int i = 0; i < HW; ++i) x[i] = __uint_as_float(raw[i]);
         const float sm = warp_reduce_scatter<HW>(x, lane, AddOp());
         if ((lane & (32 / HW - 1)) == 0) M.red[qd][h0 + lane / (32 / HW)] = sm;
       }
-      named_bar_sync(1, 256);
+      if (named_bar_or(1, 256, failed)) break;
       if (tid < H) {
         const float lt = (M.red[0][tid] + M.red[1][tid]) + (M.red[2][tid] + M.red[3][tid]);
         M.linv[tid] = lt > 0.0f ? 1.0f / lt : 0.0f;
@@ -946,12 +965,16 @@ int launch_t(const MlaLaunch& L, const MlaParams& prm) {
   return SMLA_OK;
 }
 
-// Widen the BF16 rows of one sequence (logical positions 0..n_rows-1, through
-// its page table) to f16, stored contiguously by position.
-__global__ void __launch_bounds__(256) shadow_convert_kernel(const uint16_t* __restrict__ kv,
+// Widen the rows of one sequence (logical positions 0..n_rows-1, through its
+// page table) to f16, stored contiguously by position: bf16 rows (exact in the
+// f16 range), or e4m3 rows (always exact; their per-token scales are copied to
+// shadow_scale in the same order and applied by the attention as before).
+__global__ void __launch_bounds__(256) shadow_convert_kernel(const uint8_t* __restrict__ kv,
+                                                             const float* __restrict__ kv_scale, int32_t fp8,
                                                              const int32_t* __restrict__ pt, int32_t max_pages,
                                                              int32_t num_pages, int32_t n_rows,
-                                                             uint16_t* __restrict__ shadow, uint32_t* status) {
+                                                             uint16_t* __restrict__ shadow,
+                                                             float* __restrict__ shadow_scale, uint32_t* status) {
   const int64_t pieces = static_cast<int64_t>(n_rows) * 72;  // 8 values each
   bool over = false, bad = false;
   for (int64_t pc = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; pc < pieces;
@@ -961,17 +984,28 @@ __global__ void __launch_bounds__(256) shadow_convert_kernel(const uint16_t* __r
     const int pg = lp < max_pages ? __ldg(pt + lp) : -1;
     uint4 o = make_uint4(0, 0, 0, 0);
     if (pg >= 0 && pg < num_pages) {
-      const uint4 v = ldg_stream(kv + (static_cast<int64_t>(pg) * kPage + (r & 63)) * kDqk + c * 8);
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t w[4];
+      const int64_t prow = static_cast<int64_t>(pg) * kPage + (r & 63);
+      if (fp8) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(kv + prow * kDqk + c * 8));
+        o = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(v.x & 0xFFFFu)),
+                       e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16)),
+                       e4m3x2_to_f16x2(static_cast<uint16_t>(v.y & 0xFFFFu)),
+                       e4m3x2_to_f16x2(static_cast<uint16_t>(v.y >> 16)));
+        if (c == 0) shadow_scale[r] = __ldg(kv_scale + prow);
+      } else {
+        const uint4 v = ldg_stream(reinterpret_cast<const uint16_t*>(kv) + prow * kDqk + c * 8);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        over |= ((in[t] & 0x7FFFu) > 0x477Fu) || ((in[t] & 0x7FFF0000u) > 0x477F0000u);
-        w[t] = bf16x2_to_f16x2(in[t]);
+        for (int t = 0; t < 4; ++t) {
+          over |= ((in[t] & 0x7FFFu) > 0x477Fu) || ((in[t] & 0x7FFF0000u) > 0x477F0000u);
+          w[t] = bf16x2_to_f16x2(in[t]);
+        }
+        o = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      o = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       bad = true;
+      if (fp8 && c == 0) shadow_scale[r] = 0.0f;
     }
     *reinterpret_cast<uint4*>(shadow + static_cast<int64_t>(r) * kDqk + c * 8) = o;
   }
@@ -999,17 +1033,29 @@ size_t mla_partial_bytes(int32_t n_rows, int32_t n_heads) {
   return items * n_heads * kDv * 4 + (items * n_heads * 4 + 255) / 256 * 256;
 }
 
-size_t mla_shadow_bytes(int32_t n_keys) {
-  return n_keys > 0 ? (static_cast<size_t>(n_keys) * kDqk * 2 + 255) / 256 * 256 : 0;
+size_t mla_shadow_bytes(int32_t n_keys, int32_t kv_dtype) {
+  if (n_keys <= 0 || (kv_dtype != SMLA_BF16 && kv_dtype != SMLA_FP8_E4M3)) return 0;
+  const size_t rows = (static_cast<size_t>(n_keys) * kDqk * 2 + 255) / 256 * 256;
+  return kv_dtype == SMLA_BF16 ? rows : rows + (static_cast<size_t>(n_keys) * 4 + 255) / 256 * 256;
 }
+
+namespace {
+// the per-token scales of an FP8 shadow follow its rows
+float* shadow_scales(void* shadow, int32_t n_keys) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(shadow) +
+                                  (static_cast<size_t>(n_keys) * kDqk * 2 + 255) / 256 * 256);
+}
+}  // namespace
 
 int launch_shadow_convert(const MlaLaunch& L) {
   const int64_t pieces = static_cast<int64_t>(L.shadow_rows) * 72;
   const int64_t want = (pieces + 255) / 256;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8LL * num_sms())));
-  shadow_convert_kernel<<<grid, 256, 0, L.stream>>>(static_cast<const uint16_t*>(L.cache->kv), L.page_tables,
-                                                   L.max_pages, L.cache->num_pages, L.shadow_rows,
-                                                   static_cast<uint16_t*>(L.shadow), L.status);
+  const bool fp8 = L.cache->kv_dtype == SMLA_FP8_E4M3;
+  shadow_convert_kernel<<<grid, 256, 0, L.stream>>>(
+      static_cast<const uint8_t*>(L.cache->kv), L.cache->kv_scale, fp8 ? 1 : 0, L.page_tables, L.max_pages,
+      L.cache->num_pages, L.shadow_rows, static_cast<uint16_t*>(L.shadow),
+      fp8 ? shadow_scales(L.shadow, L.shadow_rows) : nullptr, L.status);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
@@ -1035,6 +1081,7 @@ int launch_mla(const MlaLaunch& L) {
   prm.status = L.status;
   prm.shadow = static_cast<const uint16_t*>(L.shadow);
   prm.shadow_rows = L.shadow_rows;
+  if (L.shadow && prm.fmt == kFmtTokenFp8) prm.shadow_scale = shadow_scales(L.shadow, L.shadow_rows);
   prm.n_parts = 1;
   prm.part_blocks = (L.topk + kBlk - 1) / kBlk;
   if (prm.n_rows == 0) return SMLA_OK;

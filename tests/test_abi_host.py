@@ -95,17 +95,26 @@ def test_decode_and_indexer_argument_checks(L):
 
 def test_workspace_sizes(L):
     # prefill keeps the index list (status word + T x topk int32); rows of at most
-    # 16384 keys are selected from full score rows in shared memory, so nothing more
-    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == 256 + 16384 * 2048 * 4
-    # a BF16 cache adds an f16 copy of the sequence's rows (576 values x 2 bytes per key)
+    # 16384 keys are selected from full score rows in shared memory, so nothing
+    # more for the indexer. A BF16 cache adds an f16 copy of the sequence's rows
+    # (576 values x 2 bytes per key), a per-token FP8 cache the same copy and its
+    # scales in the same order (4 bytes per key, rounded to 256), the 656-byte
+    # tile-scaled FP8 rows nothing
+    def r256(b):
+        return (b + 255) // 256 * 256
     assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 0) == \
         256 + 16384 * 2048 * 4 + 16384 * 576 * 2
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == \
+        256 + 16384 * 2048 * 4 + 16384 * 576 * 2 + r256(16384 * 4)
+    assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 2) == 256 + 16384 * 2048 * 4
     # longer rows: room for the candidate buffers of rows whose final selection is
     # deferred: 4 query rows per indexer work item at 32 heads share 16384 entries,
     # so 4096 (key, index) pairs per row, plus one count per row
     T, P = 8192, 20000
     cand = T * 4096 * 8 + T * 4
-    assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 1) == 256 + T * 2048 * 4 + cand
+    assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 2) == 256 + T * 2048 * 4 + cand
+    assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 1) == \
+        256 + T * 2048 * 4 + r256((P + T) * 1152) + r256((P + T) * 4) + cand
     # the indexer alone: status word (+ the same candidate buffers for long rows)
     assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256
     assert L.smla_indexer_topk_workspace_size(1, P + T, T, 32, 2048) == 256 + cand
@@ -115,5 +124,6 @@ def test_workspace_sizes(L):
     dec = L.smla_sparse_mla_decode_workspace_size(64, 131072, 2, 64, 32, 2048)
     assert dec == 256 + rows * 131072 * 4 + rows * k * 4 + rows * 4 * 64 * 512 * 4 + rows * 4 * 64 * 4
     assert L.smla_sparse_mla_fwd_workspace_size(0, 100, 64, 2048, 0) == 256
-    assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 1) == 256
+    assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 2) == 256
+    assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 1) == 256 + 1000 * 1152 + r256(4000)
     assert L.smla_sparse_mla_fwd_workspace_size(1000, 100, 64, 2048, 0) == 256 + 1000 * 1152
