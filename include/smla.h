@@ -125,11 +125,17 @@ int smla_version(void);
  * Workspace: the returned size. When several query rows share the key stream
  * (long per-sequence batches), 256 bytes already suffice. With max_seq_len at
  * most 16384 (8192 at h_idx = 4) every row's scores fit in shared memory and
- * the exact top-k is taken there; for longer sequences the rest of the
- * workspace holds per-row candidate buffers (up to 16384 / rows-per-work-item
- * (key, index) pairs of 8 bytes, plus a count per row) whose final exact
- * selection then runs in a separate light kernel instead of stalling the
- * scoring pipeline; with less room the selection stays in the scoring kernel.
+ * the exact top-k is taken there. Longer sequences at h_idx = 32 of at most
+ * 262144 keys: the rest of the workspace holds a score array (4 bytes per key
+ * up to max_seq_len rounded up to 32, per query row) that the scoring kernel
+ * fills and a per-row kernel selects from; rows are processed in blocks (the
+ * same rows of every sequence) of which the returned size holds one of up to
+ * 4 GiB, or at least 608 rows per sequence. Other long sequences, or a
+ * workspace too small for such a block: per-row candidate buffers (up to
+ * 16384 / rows-per-work-item (key, index) pairs of 8 bytes, plus a count per
+ * row) whose final exact selection then runs in a separate light kernel
+ * instead of stalling the scoring pipeline; with less room still the
+ * selection stays in the scoring kernel. All modes select the same index sets.
  * Decode-shaped
  * calls (few rows per sequence, whose keys are split across SMs) require a
  * score array per query row (4 bytes per key up to max_seq_len): the scoring
@@ -189,9 +195,9 @@ int smla_sparse_mla_fwd(const smla_paged_cache* cache, const int32_t* page_table
  * kv_dtype = SMLA_BF16 or SMLA_FP8_E4M3 an f16 copy of the sequence's
  * prefix_len + n_tokens cache rows (widened exactly, written once per call and
  * gathered by the attention without per-row conversion; for FP8 followed by
- * the rows' scales in the same order), and the indexer's deferred candidate
- * buffers (see smla_indexer_topk). Each optional part is used only when the
- * workspace reaches its end.
+ * the rows' scales in the same order), and the indexer's score array or
+ * deferred candidate buffers (see smla_indexer_topk). Each optional part is
+ * used only when the workspace reaches its end.
  * ------------------------------------------------------------------------- */
 size_t smla_sparse_mla_prefill_workspace_size(int32_t prefix_len, int32_t n_tokens, int32_t n_heads,
                                               int32_t h_idx, int32_t topk, int32_t kv_dtype);
@@ -235,8 +241,9 @@ int smla_sparse_mla_decode(const smla_paged_cache* cache, const int32_t* page_ta
  * bytes must fit in 16 MiB (e.g. 2047 tokens at topk = 2048); larger calls
  * return SMLA_ERR_WORKSPACE and enqueue nothing. The f16 copy of the cache rows
  * (see smla_sparse_mla_prefill) is made only if it fits in the rest, and the
- * deferred candidate buffers of rows longer than 16,384 keys never do: such
- * rows take their exact top-k inside the scoring kernel (same index sets). The
+ * indexer's score array and deferred candidate buffers for rows longer than
+ * 16,384 keys only for small calls: otherwise such rows take their exact
+ * top-k inside the scoring kernel (same index sets). The
  * selected indices are not returned. Device-side errors (an out-of-range page,
  * a bounded wait that gave up) go to the array's status word: read them with
  * smla_noalloc_read_status after the call. The first call on a device looks up

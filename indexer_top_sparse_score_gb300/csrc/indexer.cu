@@ -52,11 +52,10 @@ constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
-// Streaming prefill with 32 indexer heads: four tokens per item, one epilogue
-// warpgroup per token (16 epilogue warps), see the epilogue.
-constexpr int kTokWarpgroups = 4;
-constexpr int kTokThreads = 128 + 128 * kTokWarpgroups;
-constexpr int kHistWords = 3 * 256 * kTokWarpgroups;  // selection histograms, one set per warpgroup
+// Streaming prefill with 32 indexer heads (see the epilogue): the eight
+// epilogue warps meet on one mbarrier of the kTokBars slots.
+constexpr int kTokBars = 4;
+constexpr int kHistWords = 3 * 256 * 4;  // selection histograms
 constexpr int kMaxAcc = 4;                            // TMEM accumulator buffers at most
 constexpr int kIssuers = 2;                           // MMA issuer warps
 static_assert(kStages % kIssuers == 0 && kSplitStages % kIssuers == 0 && kMaxAcc % kIssuers == 0,
@@ -75,7 +74,8 @@ struct IdxParams {
   int32_t tq, cap;
   int32_t is_bf16;
   int32_t split;
-  int32_t n_groups;   // group mode: groups per sequence
+  int32_t n_groups;   // group mode: groups per sequence (of the launch's row block)
+  int32_t row_base, block_rows;  // group mode: rows [row_base, row_base + block_rows) of every sequence
   int32_t n_kblocks;  // split mode: key blocks per sequence
   int32_t n_items;    // group mode: n_seqs * n_groups; split: n_seqs * n_kblocks
   int32_t tmem_cols;
@@ -87,13 +87,14 @@ struct IdxParams {
   int32_t* cand_cnt;
   int32_t defer;       // group mode: hand rows with more than topk candidates to finish_kernel
   int32_t rot_span;    // group mode: tiles over which the CTAs' start tiles are spread (0: the whole range)
-  uint32_t* scores;    // split mode: score keys [rows][score_stride], written for keys 0..pos
+  uint32_t* scores;    // split and score-array modes: score keys [rows][score_stride], keys 0..pos
   int64_t score_stride;
   uint32_t* status;
 };
 
 struct Item {
   int seq, row0, nrows, pos0;
+  int srow;  // the item's first row in the launch's score array
   int key_lo, key_hi;
   int t0, t1;
   int rot;  // tiles are streamed from t0 + rot, wrapping: CTAs start at different tiles
@@ -135,10 +136,11 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, co
     if ((k & 1) && g == pair) return 0;
     const int seq = g / p.n_groups;
     const int gi = g - seq * p.n_groups;
-    const int rin = gi * p.tq;
+    const int rin = p.row_base + gi * p.tq;
     it.seq = seq;
     it.row0 = seq * p.q_per_seq + rin;
-    it.nrows = min(p.tq, p.q_per_seq - rin);
+    it.nrows = min(p.tq, p.row_base + p.block_rows - rin);
+    it.srow = seq * p.block_rows + gi * p.tq;
     const int L = p.seq_lens ? p.seq_lens[seq] : p.prefix_len + p.q_per_seq;
     it.pos0 = L - p.q_per_seq + rin;
     it.key_lo = 0;
@@ -178,6 +180,7 @@ __device__ __forceinline__ int next_item(const IdxParams& p, int k, Item& it, co
     }
     it.seq = seq;
     it.row0 = seq * p.q_per_seq;
+    it.srow = it.row0;
     it.nrows = p.q_per_seq;
     it.pos0 = p.seq_lens[seq] - p.q_per_seq;
     it.trivial = false;
@@ -231,12 +234,16 @@ __device__ __forceinline__ void smem_inc(uint32_t* p) {
 // SPLIT: decode shape (compile-time, so the decode kernel carries none of the
 // candidate-selection code). DENSE: prefill rows short enough that every
 // score of a work item fits in shared memory (see the epilogue). TOK: the
-// streaming prefill with one epilogue warpgroup per token (32 heads).
-template <int HI, bool SPLIT, bool DENSE, bool TOK>
-__global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
+// streaming prefill at 32 heads (four rows per item, the two warpgroups
+// taking the tiles in turn, candidate buffers shared by the eight warps).
+// STORE: prefill at 32 heads writing every score to a score array in global
+// memory (select_kernel takes the exact top-k afterwards).
+template <int HI, bool SPLIT, bool DENSE, bool TOK, bool STORE>
+__global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IdxParams p) {
-  static_assert(!TOK || (HI == 32 && !SPLIT && !DENSE), "the token-per-warpgroup mode is a 32-head prefill mode");
+  static_assert(!TOK || (HI == 32 && !SPLIT && !DENSE), "the streaming 32-head mode is a prefill mode");
+  static_assert(!STORE || (HI == 32 && !SPLIT && !DENSE && !TOK), "the score-array mode is a 32-head prefill mode");
   constexpr int TPW_MAX = 64 / HI;  // tokens per epilogue warpgroup held in registers
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* a_tiles = smem;
@@ -266,8 +273,8 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
   uint64_t* qb_x = ring_x + 2 * (kSplitStages - kStages);  // [full, empty] of query buffer 1
   auto q_full = [&](int qb) { return qb == 0 ? b_full : qb_x; };
   auto q_empty = [&](int qb) { return qb == 0 ? b_empty : qb_x + 1; };
-  uint64_t* wg_bar = qb_x + 2;  // TOK: one barrier per epilogue warpgroup (its four warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + kTokWarpgroups);
+  uint64_t* wg_bar = qb_x + 2;  // TOK: wg_bar[0] is the epilogue warps' meeting barrier
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + kTokBars);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -296,11 +303,10 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      // one warpgroup per buffer; TOK: every epilogue warp reads every buffer
-      mbar_init(&acc_empty[i], TOK ? 4 * kTokWarpgroups : (SPLIT || DENSE) ? 4 : kEpiThreads / 32);
+      mbar_init(&acc_empty[i], (SPLIT || DENSE || TOK || STORE) ? 4 : kEpiThreads / 32);  // one warpgroup per buffer
     }
-    for (int i = 0; i < kTokWarpgroups; ++i) mbar_init(&wg_bar[i], 4);
-    for (int i = 0; i < 8 * kTokWarpgroups; ++i) wcnt[i] = 0;  // TOK: per-token counters
+    for (int i = 0; i < kTokBars; ++i) mbar_init(&wg_bar[i], 8);
+    for (int i = 0; i < 16; ++i) wcnt[i] = 0;  // TOK: per-row counters
     mbar_init(b_full, 1);
     mbar_init(b_empty, kIssuers);
     mbar_init(q_full(1), 1);
@@ -469,54 +475,152 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
       mma_commit_warp(q_empty(qb));
     }
   } else if (warp >= 4) {
-    if constexpr (TOK) {
-      // ---------------------------------------------------------- epilogue, one warpgroup per token
-      // Warpgroup g (warps 4g+4 .. 4g+7) owns row g of every item (four rows at
-      // 32 heads, N = 128) and reads that row's 32 accumulator columns of every
-      // tile; its four warps cover the four TMEM lane quadrants (32 keys each).
-      // A key whose score reaches the row's threshold is appended to the row's
-      // candidate buffer at a position reserved with one shared-memory atomic
-      // per warp and tile: there is no barrier per tile. A warp whose
-      // reservation runs past the buffer's end keeps its entries in registers
-      // and requests a cut; the four warps of that warpgroup alone then meet on
-      // their own mbarrier (entered from wherever each warp is: while waiting
-      // for its next accumulator, or at the end of the item), cut the buffer to
-      // a superset of the row's top-k, raise the row's threshold and append the
-      // held entries. The other warpgroups keep scoring meanwhile, up to the
-      // depth of the accumulator ring. A warp waiting for an accumulator keeps
-      // watching for a cut request of its warpgroup, so no warp can hold the
-      // ring while its peers wait for it in a cut. At the end of an item a row
-      // with more than topk candidates goes to the workspace for finish_kernel
-      // (or, without room there, is selected here); the final index list of
-      // every row is in ascending index order.
-      const int ew = warp - 4;
-      const int g = ew >> 2;
-      const int q = warp & 3;
-      const int w4 = ew & 3;
-      const int tid_wg = w4 * 32 + lane;
-      const int cap = p.cap;
-      const int topk = p.topk;
-      uint32_t* kb = ckey + g * cap;
-      uint32_t* ib = cidx + g * cap;
-      // per-token state: [0] entries in the buffer, [1] threshold key, [2] cut
-      // requested, [3] items whose tiles this warpgroup's warps have finished
-      uint32_t* stw = wcnt + 8 * g;
-      volatile uint32_t* vst = stw;
-      uint32_t* hist_wg = hist + 768 * g;
-      uint32_t* red_wg = scratch + 16 * g;
-      const uint32_t lanemask_lt = (1u << lane) - 1u;
-      uint32_t bar_phase = 0;  // phases of wg_bar[g] this warp has completed
+    if constexpr (STORE) {
+      // ---------------------------------------------------------- epilogue (32 heads, score array)
+      // The two warpgroups take the key tiles in turn (warpgroup g the tiles of
+      // CTA tile-counter parity g, so each owns two of the four accumulator
+      // buffers). A warp loads the four rows' 32 columns of its TMEM lane
+      // quadrant (32 keys), releases the accumulator and writes the four rows'
+      // score keys to the score array: 128 contiguous bytes per row, nothing
+      // shared between warps. The weights of consecutive items alternate
+      // between two buffers, so the eight warps meet once per item.
+      constexpr int kRows = 4;  // rows per item (N = 128 at 32 heads)
+      const int ew = warp - 4;  // 0..7
+      const int wg = ew >> 2;
+      const int q = warp & 3;   // TMEM lane quadrant
+      const int tid_e = ew * 32 + lane;
+      uint32_t bar_phase = 0;
       bool ok = true;
-      bool hold = false;       // this lane keeps an entry that did not fit
-      uint32_t hkey = 0, hidx = 0;
-
-      // The four warps of the warpgroup meet (bounded; false once the kernel gives up).
       auto meet = [&]() -> bool {
         __syncwarp();
         bool r = true;
         if (lane == 0) {
-          mbar_arrive(&wg_bar[g]);
-          r = mbar_wait_spin(&wg_bar[g], bar_phase & 1u, abort_v, p.status);
+          mbar_arrive(&wg_bar[0]);
+          r = mbar_wait_spin(&wg_bar[0], bar_phase & 1u, abort_v, p.status);
+        }
+        ++bar_phase;
+        r = __shfl_sync(0xFFFFFFFFu, r, 0);
+        __syncwarp();
+        if (!r) ok = false;
+        return r;
+      };
+      uint32_t ac = 0, n_items_seen = 0;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      for (int k = 0; ok; ++k) {
+        Item it;
+        const int r = next_item(p, k, it, pref);
+        if (r < 0) break;
+        if (r == 0) continue;
+        if (it.trivial) {
+          // every key of every row is selected: 0..pos, then -1
+          for (int j = 0; j < it.nrows; ++j) {
+            const int n = it.pos0 + j + 1;
+            int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + j) * p.topk;
+            for (int e = tid_e; e < p.topk; e += 256) o[e] = e < n ? e : -1;
+          }
+          continue;
+        }
+        // the rows' head weights; the buffer of two items back is free: every
+        // warp has met at the previous item's start, after that item's tiles
+        float* wb = (n_items_seen & 1u) ? reinterpret_cast<float*>(hist) : wbuf;
+        ++n_items_seen;
+        if (tid_e < kRows * HI) {
+          const int j = tid_e / HI;
+          wb[tid_e] = j < it.nrows ? __ldg(p.w + static_cast<size_t>(it.row0 + j) * HI + (tid_e % HI)) : 0.0f;
+        }
+        if (!meet()) break;
+        const float4* wv4 = reinterpret_cast<const float4*>(wb);
+        const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
+        const uint32_t ac0 = ac;
+        const int nt = it.t1 - it.t0;
+        uint32_t* srow = p.scores + static_cast<int64_t>(it.srow) * p.score_stride;
+        for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt; tt += 2) {
+          const uint32_t gt = ac0 + tt;
+          const int buf = gt & 3;
+          if (__any_sync(0xFFFFFFFFu, !mbar_wait(&acc_full[buf], (gt >> 2) & 1u, abort_v, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t raw[kRows][32];
+#pragma unroll
+          for (int j = 0; j < kRows; ++j)
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN + j * HI), raw[j]);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          const int t = tile_at(it, tt);
+          const int s = t * kTileKeys + q * 32 + lane;
+          float ks = 1.0f;
+          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) {
+            float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int h = 0; h < HI; h += 8) {
+              const float4 wa = wv4[(j * HI + h) / 4], wb2 = wv4[(j * HI + h) / 4 + 1];
+              fma2(a[0], a[1], wa.x, wa.y, fmaxf(__uint_as_float(raw[j][h + 0]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 1]), 0.0f));
+              fma2(a[2], a[3], wa.z, wa.w, fmaxf(__uint_as_float(raw[j][h + 2]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 3]), 0.0f));
+              fma2(a[4], a[5], wb2.x, wb2.y, fmaxf(__uint_as_float(raw[j][h + 4]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 5]), 0.0f));
+              fma2(a[6], a[7], wb2.z, wb2.w, fmaxf(__uint_as_float(raw[j][h + 6]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 7]), 0.0f));
+            }
+            if (j < it.nrows && s < it.key_hi && s <= it.pos0 + j)
+              srow[static_cast<int64_t>(j) * p.score_stride + s] =
+                  score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+          }
+        }
+        ac = ac0 + nt;
+      }
+    } else if constexpr (TOK) {
+      // ---------------------------------------------------------- epilogue (32 heads, streaming prefill)
+      // The two warpgroups take the key tiles in turn (warpgroup g the tiles of
+      // CTA tile-counter parity g: accumulator buffers 0 and 2 belong to
+      // warpgroup 0, 1 and 3 to warpgroup 1), so the two halves of the
+      // accumulator ring run independently. A warp loads the four rows' 32
+      // columns of its TMEM lane quadrant (32 keys) at once, releases the
+      // accumulator and computes the four rows' scores as independent chains.
+      // A key whose score reaches its row's threshold is appended to the row's
+      // candidate buffer (shared by the eight warps: one atomic per warp, row
+      // and tile, no barrier per tile). A reservation that runs past the
+      // buffer's end is kept in registers and requests a cut of that row; the
+      // eight epilogue warps then meet on an mbarrier (each entering from
+      // wherever it is: waiting for its next accumulator, or at the end of the
+      // item), cut every requested buffer to a superset of its row's top-k,
+      // raise those rows' thresholds and append the held entries. At the end of
+      // an item a row with more than topk candidates goes to the workspace for
+      // finish_kernel (or is selected here when there is no room), and every
+      // row's index list ends in ascending index order.
+      constexpr int kRows = 4;          // rows per item (N = 128 at 32 heads)
+      constexpr int kE = 256;           // epilogue threads
+      const int ew = warp - 4;          // 0..7
+      const int wg = ew >> 2;
+      const int q = warp & 3;           // TMEM lane quadrant
+      const int tid_e = ew * 32 + lane;
+      const int cap = p.cap;
+      const int topk = p.topk;
+      // [0..3] entries per row, [4..7] row thresholds, [8] cut requests (a bit
+      // per row), [9] warps done with the tiles of their items
+      uint32_t* stw = wcnt;
+      volatile uint32_t* vst = stw;
+      const uint32_t lanemask_lt = (1u << lane) - 1u;
+      uint32_t bar_phase = 0;  // phases of the group barrier this warp has completed
+      bool ok = true;
+      uint32_t hold = 0;       // bit j: this lane keeps an entry of row j that did not fit
+      uint32_t hkey[kRows] = {0, 0, 0, 0}, hidx[kRows] = {0, 0, 0, 0};
+      uint32_t thr[kRows] = {0, 0, 0, 0};  // copies of the row thresholds (they change only in a cut)
+
+      // The eight epilogue warps meet (bounded; false once the kernel gives up).
+      auto meet = [&]() -> bool {
+        __syncwarp();
+        bool r = true;
+        if (lane == 0) {
+          mbar_arrive(&wg_bar[0]);
+          r = mbar_wait_spin(&wg_bar[0], bar_phase & 1u, abort_v, p.status);
         }
         ++bar_phase;
         r = __shfl_sync(0xFFFFFFFFu, r, 0);
@@ -525,17 +629,18 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
         return r;
       };
       auto sync = [&]() { meet(); };
-      // Keep the entries of [0, n) that pass `take`, in place, in a fixed order
-      // (rounds of 2048 entries, 16 per thread). Returns the count, or -1.
-      auto compact = [&](int n, auto take) -> int {
+      // Keep the entries of row j's buffer [0, n) that pass `take`, in place and
+      // in a fixed order (rounds of 2048 entries, 8 per thread). Returns the
+      // count, or -1 when a meeting failed.
+      auto compact = [&](uint32_t* kb, uint32_t* ib, int n, auto take) -> int {
         int base = 0;
         for (int r0 = 0, rnd = 0; r0 < n; r0 += 2048, ++rnd) {
-          uint32_t kk[16], ii[16];
-          bool tk16[16];
+          uint32_t kk[8], ii[8];
+          uint32_t tmask = 0;
           int c = 0;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int e0 = r0 + 4 * tid_wg + 512 * v;
+          for (int v = 0; v < 2; ++v) {
+            const int e0 = r0 + 4 * tid_e + 1024 * v;
             uint4 kv = make_uint4(0, 0, 0, 0), iv = make_uint4(0, 0, 0, 0);
             if (e0 < n) {
               kv = *reinterpret_cast<const uint4*>(kb + e0);
@@ -545,8 +650,9 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
             ii[4 * v + 0] = iv.x; ii[4 * v + 1] = iv.y; ii[4 * v + 2] = iv.z; ii[4 * v + 3] = iv.w;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              tk16[4 * v + u] = e0 + u < n && take(kk[4 * v + u], ii[4 * v + u]);
-              c += tk16[4 * v + u];
+              const bool t2 = e0 + u < n && take(kk[4 * v + u], ii[4 * v + u]);
+              tmask |= (t2 ? 1u : 0u) << (4 * v + u);
+              c += t2;
             }
           }
           int incl = c;
@@ -555,20 +661,20 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
             const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
             if (lane >= o) incl += t2;
           }
-          uint32_t* ws = red_wg + 8 + 4 * (rnd & 1);
-          if (lane == 31) ws[w4] = static_cast<uint32_t>(incl);
+          uint32_t* ws = scratch + 16 + 8 * (rnd & 1);
+          if (lane == 31) ws[ew] = static_cast<uint32_t>(incl);
           if (!meet()) return -1;
           int off = base, total = 0;
 #pragma unroll
-          for (int w2 = 0; w2 < 4; ++w2) {
+          for (int w2 = 0; w2 < 8; ++w2) {
             const int v = static_cast<int>(ws[w2]);
-            if (w2 < w4) off += v;
+            if (w2 < ew) off += v;
             total += v;
           }
           off += incl - c;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            if (!tk16[u]) continue;
+          for (int u = 0; u < 8; ++u) {
+            if (!((tmask >> u) & 1u)) continue;
             if (off < cap) {
               kb[off] = kk[u];
               ib[off] = ii[u];
@@ -579,134 +685,149 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
         }
         return base;
       };
-      // Cut the buffer of this warpgroup's row to a superset of its top-k and
-      // raise the threshold; then append the held entries. All four warps call
+      // Cut every requested row buffer to a superset of its row's top-k and raise
+      // the row's threshold; then append the held entries. All eight warps call
       // it (each from wherever it noticed the request).
       auto cut = [&]() -> bool {
         if (!meet()) return false;  // every warp's reservations and writes are done
-        const int n = min(static_cast<int>(vst[0]), cap);
-        // 1. the range of the buffer's keys (clears the histogram meanwhile)
-        uint32_t lo = 0xFFFFFFFFu, hi = 0;
-        for (int e0 = 4 * tid_wg; e0 < n; e0 += 512) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
-          const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+        const uint32_t mask = vst[8];
+        for (int j = 0; j < kRows; ++j) {
+          if (!((mask >> j) & 1u)) continue;
+          uint32_t* kb = ckey + j * cap;
+          uint32_t* ib = cidx + j * cap;
+          const int n = min(static_cast<int>(vst[j]), cap);
+          // 1. the range of the buffer's keys (the histogram is cleared meanwhile)
+          uint32_t lo = 0xFFFFFFFFu, hi = 0;
+          for (int e0 = 4 * tid_e; e0 < n; e0 += 4 * kE) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+            const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (e0 + u < n) {
-              lo = min(lo, v4[u]);
-              hi = max(hi, v4[u]);
-            }
-        }
-        lo = __reduce_min_sync(0xFFFFFFFFu, lo);
-        hi = __reduce_max_sync(0xFFFFFFFFu, hi);
-        if (lane == 0) {
-          red_wg[w4] = lo;
-          red_wg[4 + w4] = hi;
-        }
-        hist_wg[tid_wg] = 0;
-        hist_wg[tid_wg + 128] = 0;
-        if (!meet()) return false;
-        lo = min(min(red_wg[0], red_wg[1]), min(red_wg[2], red_wg[3]));
-        hi = max(max(red_wg[4], red_wg[5]), max(red_wg[6], red_wg[7]));
-        const uint32_t range = hi - lo;
-        const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
-        // 2. histogram of the keys over 256 bins of [lo, hi]
-        for (int e0 = 4 * tid_wg; e0 < n; e0 += 512) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
-          const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
+            for (int u = 0; u < 4; ++u)
+              if (e0 + u < n) {
+                lo = min(lo, v4[u]);
+                hi = max(hi, v4[u]);
+              }
+          }
+          lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+          hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+          if (lane == 0) {
+            scratch[ew] = lo;
+            scratch[8 + ew] = hi;
+          }
+          hist[tid_e] = 0;
+          if (!meet()) return false;
+          lo = 0xFFFFFFFFu;
+          hi = 0;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (e0 + u < n && v4[u] >= lo && v4[u] <= hi) smem_inc(&hist_wg[(v4[u] - lo) >> shift]);
-        }
-        if (!meet()) return false;
-        // 3. every warp: the bin holding the topk-th best key and the entries
-        //    from that bin up (lane l owns bins 255-8l down to 248-8l)
-        uint32_t c8[8], sum = 0;
+          for (int w2 = 0; w2 < 8; ++w2) {
+            lo = min(lo, scratch[w2]);
+            hi = max(hi, scratch[8 + w2]);
+          }
+          const uint32_t range = hi - lo;
+          const int shift = range >= 256u ? (32 - __clz(range)) - 8 : 0;
+          // 2. histogram of the keys over 256 bins of [lo, hi]
+          for (int e0 = 4 * tid_e; e0 < n; e0 += 4 * kE) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(kb + e0);
+            const uint32_t v4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c8[i] = hist_wg[255 - 8 * lane - i];
-          sum += c8[i];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += t2;
-        }
-        const uint32_t excl = incl - sum;
-        uint32_t mine = 0, kept = 0;
-        if (excl < static_cast<uint32_t>(topk) && incl >= static_cast<uint32_t>(topk)) {
-          uint32_t run = excl;
+            for (int u = 0; u < 4; ++u)
+              if (e0 + u < n && v4[u] >= lo && v4[u] <= hi) smem_inc(&hist[(v4[u] - lo) >> shift]);
+          }
+          if (!meet()) return false;
+          // 3. every warp: the bin holding the topk-th best key and the entries
+          //    from that bin up (lane l owns bins 255-8l down to 248-8l)
+          uint32_t c8[8], sum = 0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (run + c8[i] >= static_cast<uint32_t>(topk)) {
-              mine = 0x80000000u | (255u - 8u * lane - i);
-              kept = run + c8[i];
-              break;
+            c8[i] = hist[255 - 8 * lane - i];
+            sum += c8[i];
+          }
+          uint32_t incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t2;
+          }
+          const uint32_t excl = incl - sum;
+          uint32_t mine = 0, kept = 0;
+          if (excl < static_cast<uint32_t>(topk) && incl >= static_cast<uint32_t>(topk)) {
+            uint32_t run = excl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (run + c8[i] >= static_cast<uint32_t>(topk)) {
+                mine = 0x80000000u | (255u - 8u * lane - i);
+                kept = run + c8[i];
+                break;
+              }
+              run += c8[i];
             }
-            run += c8[i];
+          }
+          const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine != 0)) - 1;
+          uint32_t tk = 0, ti = 0xFFFFFFFFu;
+          bool exact = false;
+          if (src >= 0) {  // more than topk entries (always: a cut is requested when the buffer overflows)
+            const uint32_t bin = __shfl_sync(0xFFFFFFFFu, mine, src) & 0xFFu;
+            kept = __shfl_sync(0xFFFFFFFFu, kept, src);
+            tk = lo + (bin << shift);
+            // a bin too full (heavy ties) would free too little room: exact selection
+            exact = static_cast<int>(kept) > cap - 512;
+          }
+          if (!meet()) return false;  // the histogram is read; the exact selection reuses it
+          if (exact && n > topk) {
+            dense_select<kE>(kb, ib, n, topk, tid_e, hist, scratch, sync, tk, ti);
+            if (!ok) return false;
+          }
+          const uint32_t ctk = tk, cti = ti;
+          const int m = exact ? compact(kb, ib, n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, ctk, cti); })
+                              : compact(kb, ib, n, [&](uint32_t k2, uint32_t) { return k2 >= ctk; });
+          if (m < 0 || !meet()) return false;
+          // later keys from the cut value up are admitted: keys arrive in no
+          // particular order, so one equal to it may still win on its index
+          if (tid_e == 0) {
+            stw[j] = static_cast<uint32_t>(m);
+            stw[4 + j] = tk;
           }
         }
-        const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine != 0)) - 1;
-        uint32_t tk = 0, ti = 0xFFFFFFFFu;
-        bool exact = false;
-        if (src >= 0) {  // more than topk entries (always: a cut is requested when the buffer overflows)
-          const uint32_t bin = __shfl_sync(0xFFFFFFFFu, mine, src) & 0xFFu;
-          kept = __shfl_sync(0xFFFFFFFFu, kept, src);
-          tk = lo + (bin << shift);
-          // a bin too full (heavy ties) would free too little room: exact selection
-          exact = static_cast<int>(kept) > cap - 512;
-        }
-        if (!meet()) return false;  // the histogram is read; wg_select reuses it
-        if (exact && n > topk) {
-          wg_select(kb, ib, n, topk, tid_wg, hist_wg, red_wg, sync, tk, ti);
-          if (!ok) return false;
-        }
-        const uint32_t ctk = tk, cti = ti;
-        const int m = exact ? compact(n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, ctk, cti); })
-                            : compact(n, [&](uint32_t k2, uint32_t) { return k2 >= ctk; });
-        if (m < 0 || !meet()) return false;
-        // later keys from the cut value up are admitted: keys arrive in no
-        // particular order, so one equal to it may still win on its index
-        if (tid_wg == 0) {
-          stw[0] = static_cast<uint32_t>(m);
-          stw[1] = tk;
-          stw[2] = 0;
-        }
+        if (tid_e == 0) stw[8] = 0;
         if (!meet()) return false;
-        // 4. the held entries (at most one per lane) that still qualify
-        const bool re = hold && hkey >= tk;
-        hold = false;
-        const uint32_t mm = __ballot_sync(0xFFFFFFFFu, re);
-        if (mm) {
-          uint32_t old = 0;
-          if (lane == 0) old = atomicAdd(&stw[0], static_cast<uint32_t>(__popc(mm)));
-          old = __shfl_sync(0xFFFFFFFFu, old, 0);
-          const uint32_t pos = old + __popc(mm & lanemask_lt);
-          if (re) {
-            if (pos < static_cast<uint32_t>(cap)) {
-              kb[pos] = hkey;
-              ib[pos] = hidx;
-            } else {
-              set_status(p.status, kStatusTimeout);  // cannot happen: a cut frees >= 128 slots
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) thr[j] = vst[4 + j];
+        // 4. the held entries (at most one per lane and row) that still qualify
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const bool re = ((hold >> j) & 1u) && hkey[j] >= thr[j];
+          const uint32_t mm = __ballot_sync(0xFFFFFFFFu, re);
+          if (mm) {
+            uint32_t old = 0;
+            if (lane == 0) old = atomicAdd(&stw[j], static_cast<uint32_t>(__popc(mm)));
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            const uint32_t pos = old + __popc(mm & lanemask_lt);
+            if (re) {
+              if (pos < static_cast<uint32_t>(cap)) {
+                ckey[j * cap + pos] = hkey[j];
+                cidx[j * cap + pos] = hidx[j];
+              } else {
+                set_status(p.status, kStatusTimeout);  // cannot happen: a cut frees >= 512 slots
+              }
             }
           }
         }
+        hold = 0;
         return meet();
       };
-      // Ascending index order of the first m entries (bitonic network over the
-      // next power of two, padded with the largest index).
-      auto sort_by_index = [&](int m) -> bool {
+      // Ascending index order of the first m entries of a buffer (bitonic
+      // network over the next power of two, padded with the largest index).
+      auto sort_by_index = [&](uint32_t* kb, uint32_t* ib, int m) -> bool {
         int P = 1;
         while (P < m) P <<= 1;
-        for (int e = m + tid_wg; e < P; e += 128) {
+        for (int e = m + tid_e; e < P; e += kE) {
           ib[e] = 0xFFFFFFFFu;
           kb[e] = 0;
         }
         if (!meet()) return false;
         for (int size = 2; size <= P; size <<= 1)
           for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid_wg; i < P / 2; i += 128) {
+            for (int i = tid_e; i < P / 2; i += kE) {
               const int a = 2 * i - (i & (stride - 1));
               const int b = a + stride;
               const bool up = (a & size) == 0;
@@ -723,6 +844,38 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
           }
         return true;
       };
+      // Lane 0 polls until `ready()` or a cut request (served first: a warp
+      // that holds an entry has requested one); bounded over the whole wait.
+      auto wait_until = [&](auto ready) -> bool {
+        const long long t0 = clock64();
+        for (uint32_t itw = 0;; ++itw) {
+          uint32_t st2 = 0;
+          if (lane == 0) {
+            st2 = ready() ? 1u : 0u;
+            __threadfence_block();
+            if (vst[8]) st2 = 2u;  // a request is served before the wait ends
+            if (st2 != 1u && (itw & 15u) == 15u) {
+              if (*abort_v) {
+                st2 = 4u;
+              } else if (clock64() - t0 > kWaitLimitCycles) {
+                set_status(p.status, kStatusTimeout);
+                *abort_v = 1;
+                st2 = 4u;
+              }
+            }
+          }
+          st2 = __shfl_sync(0xFFFFFFFFu, st2, 0);
+          if (st2 & 4u) {
+            ok = false;
+            return false;
+          }
+          if (st2 & 2u) {
+            if (!cut()) return false;
+            continue;
+          }
+          if (st2 & 1u) return true;
+        }
+      };
 
       uint32_t ac = 0, items_done = 0;
       for (int k = 0; ok; ++k) {
@@ -730,203 +883,143 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
         const int r = next_item(p, k, it, pref);
         if (r < 0) break;
         if (r == 0) continue;
-        const bool active = g < it.nrows;
-        const int row = it.row0 + g;
         if (it.trivial) {
-          // every key of the row is selected: 0..pos, then -1
-          if (active) {
-            const int n = it.pos0 + g + 1;
-            int32_t* o = p.out_idx + static_cast<size_t>(row) * topk;
-            for (int e = tid_wg; e < topk; e += 128) o[e] = e < n ? e : -1;
-            if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;
+          // every key of every row is selected: 0..pos, then -1
+          for (int j = 0; j < it.nrows; ++j) {
+            const int n = it.pos0 + j + 1;
+            int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + j) * topk;
+            for (int e = tid_e; e < topk; e += kE) o[e] = e < n ? e : -1;
+            if (p.defer && tid_e == 0) p.cand_cnt[it.row0 + j] = -1;
           }
           continue;
         }
-        // the row's head weights, read back as float4 broadcasts per tile; the
-        // row's state starts empty (reset here, not at the end of the previous
-        // item: every warp reads the final count there before the last meeting)
-        float* wrow = wbuf + g * HI;
-        if (tid_wg < HI) wrow[tid_wg] = active ? __ldg(p.w + static_cast<size_t>(row) * HI + tid_wg) : 0.0f;
-        if (tid_wg == 0) {
-          stw[0] = 0;
-          stw[1] = 0;
+        // the rows' head weights (read back as float4 broadcasts); the rows'
+        // state starts empty (reset here, not at the end of the previous item:
+        // every warp reads the final counts there before the last meeting)
+        if (tid_e < kRows * HI) {
+          const int j = tid_e / HI;
+          wbuf[tid_e] = j < it.nrows ? __ldg(p.w + static_cast<size_t>(it.row0 + j) * HI + (tid_e % HI)) : 0.0f;
         }
+        if (tid_e < 2 * kRows) stw[tid_e] = 0;
         if (!meet()) break;
-        const float4* wv4 = reinterpret_cast<const float4*>(wrow);
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) thr[j] = 0;
+        const float4* wv4 = reinterpret_cast<const float4*>(wbuf);
         const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
         const uint32_t ac0 = ac;
         const int nt = it.t1 - it.t0;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * HI);
-        for (int tt = 0; tt < nt && ok; ++tt) {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt && ok; tt += 2) {
           const uint32_t gt = ac0 + tt;
           const int buf = gt & 3;
-          // wait for the tile's accumulator, serving cut requests meanwhile
-          {
-            // lane 0 polls; bit 1: a cut is requested (served first: a warp
-            // that holds an entry has requested one and must not take another
-            // tile before it is appended), bit 0: the accumulator is ready,
-            // bit 2: give up (the kernel aborts or the wait ran out)
-            const uint32_t par = (gt >> 2) & 1u;
-            const long long t0 = clock64();
-            for (uint32_t itw = 0;; ++itw) {
-              uint32_t st2 = 0;
-              if (lane == 0) {
-                st2 = vst[2] ? 2u : (mbar_test_wait(&acc_full[buf], par) ? 1u : 0u);
-                // the limit holds for the whole wait, cuts served included
-                if (st2 != 1u && (itw & 15u) == 15u) {
-                  if (*abort_v) {
-                    st2 = 4u;
-                  } else if (clock64() - t0 > kWaitLimitCycles) {
-                    set_status(p.status, kStatusTimeout);
-                    *abort_v = 1;
-                    st2 = 4u;
-                  }
-                }
-              }
-              st2 = __shfl_sync(0xFFFFFFFFu, st2, 0);
-              if (st2 & 4u) {
-                ok = false;
-                break;
-              }
-              if (st2 & 2u) {
-                if (!cut()) break;
-                continue;
-              }
-              if (st2 & 1u) break;
-            }
-            if (!ok) break;
-          }
+          const uint32_t par = (gt >> 2) & 1u;
+          if (!wait_until([&]() { return mbar_test_wait(&acc_full[buf], par); })) break;
           tc_fence_after();
+          uint32_t raw[kRows][32];
+#pragma unroll
+          for (int j = 0; j < kRows; ++j)
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN + j * HI), raw[j]);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
           const int t = tile_at(it, tt);
           const int s = t * kTileKeys + q * 32 + lane;
-          uint32_t key = 0;
-          if (active) {
-            uint32_t raw[32];
-            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN), raw);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            float ks = 1.0f;
-            if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          float ks = 1.0f;
+          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          uint32_t key[kRows];
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) {
             float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int h = 0; h < HI; h += 8) {
-              const float4 wa = wv4[h / 4], wb = wv4[h / 4 + 1];
-              fma2(a[0], a[1], wa.x, wa.y, fmaxf(__uint_as_float(raw[h + 0]), 0.0f),
-                   fmaxf(__uint_as_float(raw[h + 1]), 0.0f));
-              fma2(a[2], a[3], wa.z, wa.w, fmaxf(__uint_as_float(raw[h + 2]), 0.0f),
-                   fmaxf(__uint_as_float(raw[h + 3]), 0.0f));
-              fma2(a[4], a[5], wb.x, wb.y, fmaxf(__uint_as_float(raw[h + 4]), 0.0f),
-                   fmaxf(__uint_as_float(raw[h + 5]), 0.0f));
-              fma2(a[6], a[7], wb.z, wb.w, fmaxf(__uint_as_float(raw[h + 6]), 0.0f),
-                   fmaxf(__uint_as_float(raw[h + 7]), 0.0f));
+              const float4 wa = wv4[(j * HI + h) / 4], wb = wv4[(j * HI + h) / 4 + 1];
+              fma2(a[0], a[1], wa.x, wa.y, fmaxf(__uint_as_float(raw[j][h + 0]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 1]), 0.0f));
+              fma2(a[2], a[3], wa.z, wa.w, fmaxf(__uint_as_float(raw[j][h + 2]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 3]), 0.0f));
+              fma2(a[4], a[5], wb.x, wb.y, fmaxf(__uint_as_float(raw[j][h + 4]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 5]), 0.0f));
+              fma2(a[6], a[7], wb.z, wb.w, fmaxf(__uint_as_float(raw[j][h + 6]), 0.0f),
+                   fmaxf(__uint_as_float(raw[j][h + 7]), 0.0f));
             }
-            key = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
-          } else {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            key[j] = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
           }
-          const bool valid = active && s < it.key_hi && s <= it.pos0 + g;
-          const bool adm = valid && key >= vst[1];
-          const uint32_t m = __ballot_sync(0xFFFFFFFFu, adm);
-          if (m) {
+          // a warp that holds an entry requested a cut when it did not fit, and
+          // serves it before appending again (its hold slot for that row is taken)
+          if (__any_sync(0xFFFFFFFFu, hold != 0)) {
+            if (!cut()) break;
+          }
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) {
+            const bool adm = j < it.nrows && s < it.key_hi && s <= it.pos0 + j && key[j] >= thr[j];
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, adm);
+            if (!m) continue;
             uint32_t old = 0;
-            if (lane == 0) old = atomicAdd(&stw[0], static_cast<uint32_t>(__popc(m)));
+            if (lane == 0) old = atomicAdd(&stw[j], static_cast<uint32_t>(__popc(m)));
             old = __shfl_sync(0xFFFFFFFFu, old, 0);
             const uint32_t pos = old + __popc(m & lanemask_lt);
             if (adm) {
               if (pos < static_cast<uint32_t>(cap)) {
-                kb[pos] = key;
-                ib[pos] = static_cast<uint32_t>(s);
+                ckey[j * cap + pos] = key[j];
+                cidx[j * cap + pos] = static_cast<uint32_t>(s);
               } else {
-                hold = true;
-                hkey = key;
-                hidx = static_cast<uint32_t>(s);
+                hold |= 1u << j;
+                hkey[j] = key[j];
+                hidx[j] = static_cast<uint32_t>(s);
               }
             }
-            if (lane == 0 && old + __popc(m) > static_cast<uint32_t>(cap)) vst[2] = 1u;
+            if (lane == 0 && old + __popc(m) > static_cast<uint32_t>(cap)) atomicOr(&stw[8], 1u << j);
           }
         }
         ac = ac0 + nt;
         if (!ok) break;
-        // this warp is done with the item's tiles: wait for the other three,
-        // serving cut requests meanwhile (a request can only come from a tile)
+        // this warp is done with the item's tiles: wait for the other seven,
+        // serving cut requests meanwhile. The count is read before the request:
+        // a warp's request precedes its count (fenced), so a full count read
+        // first cannot miss a request read after it.
         __syncwarp();
         if (lane == 0) {
           __threadfence_block();
-          atomicAdd(&stw[3], 1u);
+          atomicAdd(&stw[9], 1u);
         }
         ++items_done;
-        {
-          // lane 0 polls; bit 1: a cut is requested (served first), bit 0: all
-          // four warps are done, bit 2: give up. The count is read before the
-          // request: a warp's request precedes its count (fenced), so a full
-          // count read first cannot miss a request read after it.
-          const long long t0 = clock64();
-          for (uint32_t itw = 0;; ++itw) {
-            uint32_t st2 = 0;
-            if (lane == 0) {
-              const uint32_t done = vst[3];
-              __threadfence_block();
-              if (vst[2]) st2 = 2u;
-              else if (static_cast<int>(done - 4u * items_done) >= 0) st2 = 1u;
-              // the limit holds for the whole wait, cuts served included
-              if (st2 != 1u && (itw & 15u) == 15u) {
-                if (*abort_v) {
-                  st2 = 4u;
-                } else if (clock64() - t0 > kWaitLimitCycles) {
-                  set_status(p.status, kStatusTimeout);
-                  *abort_v = 1;
-                  st2 = 4u;
-                }
-              }
-            }
-            st2 = __shfl_sync(0xFFFFFFFFu, st2, 0);
-            if (st2 & 4u) {
-              ok = false;
-              break;
-            }
-            if (st2 & 2u) {
-              if (!cut()) break;
-              continue;
-            }
-            if (st2 & 1u) break;
-          }
-        }
-        if (!ok || !meet()) break;  // every append and cut of the item is done
-        // the row's result: to the workspace for finish_kernel, or selected here
-        if (active) {
-          const int n = min(static_cast<int>(vst[0]), cap);
+        if (!wait_until([&]() { return static_cast<int>(vst[9] - 8u * items_done) >= 0; })) break;
+        if (!meet()) break;  // every append and cut of the item is done
+        // the rows' results: to the workspace for finish_kernel, or selected here
+        for (int j = 0; j < it.nrows; ++j) {
+          uint32_t* kb = ckey + j * cap;
+          uint32_t* ib = cidx + j * cap;
+          const int n = min(static_cast<int>(vst[j]), cap);
+          const int row = it.row0 + j;
           int32_t* o = p.out_idx + static_cast<size_t>(row) * topk;
           float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * topk : nullptr;
           if (n > topk && p.defer) {
             uint4* dk = reinterpret_cast<uint4*>(p.cand_key + static_cast<size_t>(row) * cap);
             uint4* di = reinterpret_cast<uint4*>(p.cand_idx + static_cast<size_t>(row) * cap);
-            for (int e = 4 * tid_wg; e < n; e += 512) {
+            for (int e = 4 * tid_e; e < n; e += 4 * kE) {
               dk[e >> 2] = *reinterpret_cast<const uint4*>(kb + e);
               di[e >> 2] = *reinterpret_cast<const uint4*>(ib + e);
             }
-            if (tid_wg == 0) p.cand_cnt[row] = n;
+            if (tid_e == 0) p.cand_cnt[row] = n;
           } else {
             int m = n;
             if (n > topk) {
               uint32_t tk = 0, ti = 0xFFFFFFFFu;
-              wg_select(kb, ib, n, topk, tid_wg, hist_wg, red_wg, sync, tk, ti);
+              dense_select<kE>(kb, ib, n, topk, tid_e, hist, scratch, sync, tk, ti);
               if (!ok) break;
-              m = compact(n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, tk, ti); });
+              m = compact(kb, ib, n, [&](uint32_t k2, uint32_t i2) { return selected(k2, i2, tk, ti); });
               if (m < 0 || !meet()) break;
             }
-            if (!sort_by_index(m)) break;
-            for (int e = tid_wg; e < topk; e += 128) {
+            if (!sort_by_index(kb, ib, m)) break;
+            for (int e = tid_e; e < topk; e += kE) {
               o[e] = e < m ? static_cast<int32_t>(ib[e]) : -1;
               if (os) os[e] = e < m ? key_score(kb[e]) : 0.0f;
             }
-            if (p.defer && tid_wg == 0) p.cand_cnt[row] = -1;
+            if (p.defer && tid_e == 0) p.cand_cnt[row] = -1;
           }
         }
-        if (!meet()) break;  // the buffer is free for the next item
+        if (!ok || !meet()) break;  // the buffers are free for the next item
       }
     } else {
     // ------------------------------------------------------------ epilogue
@@ -1648,12 +1741,16 @@ __global__ void __launch_bounds__(TOK ? kTokThreads : kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Parameters of select_kernel (split mode, step 2).
+// Parameters of select_kernel (split and score-array modes, step 2). Score
+// row i belongs to sequence i / block_rows, query row row_base + i % block_rows
+// of that sequence.
 struct SelectParams {
   const uint32_t* scores;
   int64_t score_stride;
-  const int32_t* seq_lens;
+  const int32_t* seq_lens;  // device, or null: one sequence of prefix_len + q_per_seq keys
+  int32_t prefix_len;
   int32_t q_per_seq, topk;
+  int32_t row_base, block_rows;
   int32_t* out_idx;
   float* out_scores;
 };
@@ -1733,9 +1830,11 @@ __device__ __forceinline__ void sel_top_scan(SelSmem& S, const uint32_t* hist, i
   __syncthreads();
 }
 
-// Split mode (decode), step 2: the exact top-k of one row's dense score array
-// (written by the scoring kernel for keys 0..pos). One CTA of 1024 threads per
-// row; scores are read from global memory (they stay in L2).
+// Split mode (decode) and score-array mode (prefill), step 2: the exact top-k
+// of one row's dense score array (written by the scoring kernel for keys
+// 0..pos). One CTA of 1024 threads per row; scores are read from global
+// memory (decode: they stay in L2; prefill: the first pass reads them from
+// HBM, the second finds most of them in L2).
 //  1. histogram of the top 12 key bits: the bin B holding the k-th best key
 //     splits the row into entries sure to be selected (higher bins),
 //     candidates (bin B) and the rest;
@@ -1749,11 +1848,14 @@ __device__ __forceinline__ void sel_top_scan(SelSmem& S, const uint32_t* hist, i
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
   extern __shared__ __align__(16) uint8_t sel_raw[];
   SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int seq = row / p.q_per_seq;
-  const int pos = p.seq_lens[seq] - p.q_per_seq + (row - seq * p.q_per_seq);
+  const int srow = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int seq = srow / p.block_rows;
+  const int r_in = p.row_base + (srow - seq * p.block_rows);
+  const int row = seq * p.q_per_seq + r_in;
+  const int len = p.seq_lens ? p.seq_lens[seq] : p.prefix_len + p.q_per_seq;
+  const int pos = len - p.q_per_seq + r_in;
   const int n = min(pos + 1, static_cast<int>(p.score_stride));  // keys 0..pos (with a score slot)
-  const uint32_t* keys = p.scores + static_cast<int64_t>(row) * p.score_stride;
+  const uint32_t* keys = p.scores + static_cast<int64_t>(srow) * p.score_stride;
   int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
   float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
   const int k = p.topk;
@@ -2072,7 +2174,18 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
   }
 }
 
-template <int HI, bool SPLIT, bool DENSE, bool TOK = false>
+bool set_select_attr() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess)
+      return false;
+    done = true;
+  }
+  return true;
+}
+
+template <int HI, bool SPLIT, bool DENSE, bool TOK = false, bool STORE = false>
 int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
   CUtensorMap map_k, map_q;
   const CUtensorMapDataType dt = prm.is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -2087,10 +2200,10 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
     return SMLA_ERR_CUDA;
   const size_t smem = kStages * kStageBytes + kMaxN * kIdxRowBytes + 2 * kBufEntries * 4 + kMaxN * 4 +
                       kHistWords * 4 + 64 * 4 + 256 * 4 + 128 * 4 + 16 * 4 + 256 * 4 +
-                      (2 * kSplitStages + 2 * kMaxAcc + 4 + kTokWarpgroups) * 8 + 16;
+                      (2 * kSplitStages + 2 * kMaxAcc + 4 + kTokBars) * 8 + 16;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT, DENSE, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(indexer_kernel<HI, SPLIT, DENSE, TOK, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     attr_done = true;
@@ -2101,7 +2214,7 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                          : prm.n_seqs <= kMaxPrefixSeqs ? static_cast<int>(std::min<int64_t>(split_tiles, 1 << 30))
                                                         : prm.n_items;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
-  indexer_kernel<HI, SPLIT, DENSE, TOK><<<grid, TOK ? kTokThreads : kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  indexer_kernel<HI, SPLIT, DENSE, TOK, STORE><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
@@ -2136,10 +2249,37 @@ int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len) {
   return (max_seq_len <= cap && topk <= cap) ? tq : 0;
 }
 
+// Score-array mode: prefill rows at 32 indexer heads longer than the dense
+// mode takes and short enough for select_kernel's bitmap. The rows go in
+// blocks (the same rows of every sequence) whose score array fits the space
+// given; the workspace size asks for blocks of up to kScoreArrayBudget bytes.
+constexpr size_t kScoreArrayBudget = size_t(4) << 30;
+constexpr int kMinStoreRows = 608;  // rows per block (per sequence) below which the streaming mode is used
+
+bool indexer_store_mode(int32_t q_per_seq, int32_t h_idx, int32_t topk, int32_t max_seq_len) {
+  return h_idx == 32 && !indexer_split_mode(q_per_seq, h_idx) && indexer_dense_tokens(h_idx, topk, max_seq_len) == 0 &&
+         max_seq_len <= kSelBmBits;
+}
+
+int64_t store_stride(int32_t max_seq_len) { return (static_cast<int64_t>(max_seq_len) + 31) / 32 * 32; }
+
+// rows per sequence of a block whose score array fits in `bytes` (a multiple of 4, at most q_per_seq)
+int32_t store_block_rows(int32_t n_seqs, int32_t q_per_seq, int32_t max_seq_len, size_t bytes) {
+  const size_t per_row = static_cast<size_t>(n_seqs) * static_cast<size_t>(store_stride(max_seq_len)) * 4;
+  const size_t r = bytes / per_row / 4 * 4;
+  return static_cast<int32_t>(std::min<size_t>(r, static_cast<size_t>(q_per_seq)));
+}
+
 size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk,
                                 int32_t max_seq_len) {
   if (indexer_split_mode(q_per_seq, h_idx) || n_rows <= 0) return 0;
   if (indexer_dense_tokens(h_idx, topk, max_seq_len) > 0) return 0;  // dense mode keeps no candidate lists
+  if (indexer_store_mode(q_per_seq, h_idx, topk, max_seq_len)) {
+    const int32_t n_seqs = n_rows / q_per_seq;
+    const int32_t rows = std::max(std::min(q_per_seq, kMinStoreRows),
+                                  store_block_rows(n_seqs, q_per_seq, max_seq_len, kScoreArrayBudget));
+    return static_cast<size_t>(n_seqs) * rows * static_cast<size_t>(store_stride(max_seq_len)) * 4;
+  }
   const int tq = indexer_tokens_per_cta(h_idx, topk, false, q_per_seq);
   if (tq <= 0) return 0;
   const size_t cap = kBufEntries / tq;
@@ -2189,6 +2329,8 @@ int launch_indexer(const IndexerLaunch& L) {
   prm.tmem_cols = cols;
   prm.out_idx = L.out_idx;
   prm.out_scores = L.out_scores;
+  prm.row_base = 0;
+  prm.block_rows = L.q_per_seq;
   uint8_t* ws = static_cast<uint8_t*>(L.workspace);
   prm.status = reinterpret_cast<uint32_t*>(ws);
   const size_t rows = static_cast<size_t>(prm.n_rows);
@@ -2204,6 +2346,31 @@ int launch_indexer(const IndexerLaunch& L) {
     // same order (start tiles spread over 8 tiles), so a key range larger than
     // L2 is read from HBM about once per wave of items instead of once per CTA
     if (!dense && L.h_idx == 32) prm.rot_span = 8;
+    // score-array mode when the space given holds a large enough row block
+    if (!dense && indexer_store_mode(L.q_per_seq, L.h_idx, L.topk, L.max_seq_len) && L.cand &&
+        (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
+      const int32_t block = store_block_rows(L.n_seqs, L.q_per_seq, L.max_seq_len, L.cand_bytes);
+      if (block > 0 && block >= std::min(L.q_per_seq, kMinStoreRows)) {
+        prm.scores = static_cast<uint32_t*>(L.cand);
+        prm.score_stride = store_stride(L.max_seq_len);
+        SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.prefix_len, L.q_per_seq, L.topk,
+                        0, 0, L.out_idx, L.out_scores};
+        if (!set_select_attr()) return SMLA_ERR_CUDA;
+        for (int32_t r0 = 0; r0 < L.q_per_seq; r0 += block) {
+          prm.row_base = r0;
+          prm.block_rows = std::min(block, L.q_per_seq - r0);
+          prm.n_groups = (prm.block_rows + tq - 1) / tq;
+          prm.n_items = L.n_seqs * prm.n_groups;
+          const int rc = launch_indexer_t<32, false, false, false, true>(L, prm);
+          if (rc != SMLA_OK) return rc;
+          sp.row_base = r0;
+          sp.block_rows = prm.block_rows;
+          select_kernel<<<L.n_seqs * prm.block_rows, kSelThreads, sizeof(SelSmem), L.stream>>>(sp);
+          if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+        }
+        return SMLA_OK;
+      }
+    }
     const size_t cand = indexer_group_cand_bytes(prm.n_rows, L.q_per_seq, L.h_idx, L.topk, L.max_seq_len);
     if (L.cand && cand > 0 && L.cand_bytes >= cand && (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
       prm.defer = 1;
@@ -2252,14 +2419,9 @@ int launch_indexer(const IndexerLaunch& L) {
     finish_kernel<<<prm.n_rows, kFinishThreads, fsmem, L.stream>>>(fp);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
   }
-  SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.q_per_seq, L.topk, L.out_idx, L.out_scores};
-  static bool sel_attr = false;
-  if (!sel_attr) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess)
-      return SMLA_ERR_CUDA;
-    sel_attr = true;
-  }
+  SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, 0, L.q_per_seq, L.topk, 0, L.q_per_seq,
+                  L.out_idx, L.out_scores};
+  if (!set_select_attr()) return SMLA_ERR_CUDA;
   select_kernel<<<prm.n_rows, kSelThreads, sizeof(SelSmem), L.stream>>>(sp);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;

@@ -46,6 +46,22 @@ def run_prefill(dev, chunk=0, want_idx=True, sm_scale=None):
     return idx, out, lse
 
 
+def indexer_ws(n_rows: int, kind: str, device="cuda"):
+    """A workspace for smla_indexer_topk at 32 indexer heads that picks the
+    selection mode of rows longer than 16,384 keys: "cand" holds the per-row
+    candidate buffers (4 query rows per work item share 16,384 entries: 4,096
+    (key, index) pairs per row, plus a count per row) but no score-array block,
+    so the streaming mode defers the final selection; "min" is the status word
+    alone, so the streaming mode selects inside the scoring kernel."""
+    if kind == "cand":
+        n = 256 + n_rows * 4096 * 8 + (n_rows * 4 + 255) // 256 * 256
+    elif kind == "min":
+        n = 256
+    else:
+        raise ValueError(kind)
+    return smla.workspace(n, device)
+
+
 def compare_idx(gidx: np.ndarray, ridx: np.ndarray):
     """Index sets must match exactly (order inside a row is unspecified)."""
     g = np.sort(gidx, axis=1)

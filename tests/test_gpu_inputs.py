@@ -9,7 +9,8 @@ import torch
 import indexer_top_sparse_score_gb300 as smla
 import oracle
 from indexer_top_sparse_score_gb300 import workloads as wl
-from tests.gpu_common import Guarded, compare_idx, compare_out, run_prefill, sampled_oracle, stratified_rows
+from tests.gpu_common import (Guarded, compare_idx, compare_out, indexer_ws, run_prefill, sampled_oracle,
+                              stratified_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,11 +42,12 @@ def _with_key_scale(prob, seed=13):
                       prob.prefix_len, prob.n_tokens)
 
 
-@pytest.mark.parametrize("mode", ["dense", "streaming", "decode"])
+@pytest.mark.parametrize("mode", ["dense", "scores", "streaming", "decode"])
 def test_indexer_key_scale(mode):
     """A non-NULL per-key indexer scale: index sets and returned scores exact in
-    the dense (rows <= 16,384 keys) and streaming group modes and the decode
-    (split) mode; attention outputs within tolerance."""
+    the dense (rows <= 16,384 keys), score-array and streaming (a workspace too
+    small for the score array) group modes and the decode (split) mode;
+    attention outputs within tolerance."""
     if mode == "decode":
         spec = wl.scaled(wl.SPECS["decode"], n_seqs=6, len_min=3000, len_max=40000, seed=61)
     else:
@@ -67,8 +69,9 @@ def test_indexer_key_scale(mode):
         rows = np.arange(0, spec.n_tokens, 11)
         L = spec.prefix_len + spec.n_tokens
         seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+        ws = indexer_ws(spec.n_tokens, "cand") if mode == "streaming" else None
         gidx, gsc, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
-                                          spec.topk, want_scores=True)
+                                          spec.topk, want_scores=True, ws=ws)
         assert smla.read_status(ws)[0] == 0
         _, out, lse = run_prefill(dev, want_idx=False)
     ridx, rsc, rout, rlse, _, bad = o.rows(rows)

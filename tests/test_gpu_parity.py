@@ -12,7 +12,7 @@ import torch
 import indexer_top_sparse_score_gb300 as smla
 import oracle
 from indexer_top_sparse_score_gb300 import workloads as wl
-from tests.gpu_common import (compare_idx, compare_out, host_cache, run_prefill, sampled_oracle,
+from tests.gpu_common import (compare_idx, compare_out, host_cache, indexer_ws, run_prefill, sampled_oracle,
                               stratified_rows)
 
 pytestmark = pytest.mark.gpu
@@ -208,13 +208,16 @@ def test_repeat_calls_same_sets():
     assert (oa.float() - ob.float()).abs().max().item() < 1e-2
 
 
-@pytest.mark.parametrize("prefix", [6000, 17000], ids=["dense", "streaming"])
+@pytest.mark.parametrize("sel", ["dense", "scores", "streaming", "in_kernel"])
 @pytest.mark.parametrize("mode", ["constant", "binary"])
-def test_indexer_heavy_ties(mode, prefix):
+def test_indexer_heavy_ties(mode, sel):
     """Ties everywhere: constant keys (all scores equal -> the lowest k indices) and
     keys in {0,1} (few distinct scores); the lower index must win every tie. Rows
     of at most 16,384 keys take the dense group mode (every score in shared
-    memory), longer rows the streaming candidate buffers."""
+    memory); longer rows the score array with the full workspace, the streaming
+    candidate buffers with a workspace too small for the score array, and the
+    selection inside the scoring kernel with the status word alone."""
+    prefix = 6000 if sel == "dense" else 17000
     spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=700, prefix_len=prefix, shuffled=True)
     prob = wl.make(spec, "cpu")
     k = prob.cache.k_idx
@@ -228,14 +231,50 @@ def test_indexer_heavy_ties(mode, prefix):
     dev = prob.to("cuda")
     L = spec.prefix_len + spec.n_tokens
     seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    ws = indexer_ws(spec.n_tokens, {"streaming": "cand", "in_kernel": "min"}[sel]) \
+        if sel in ("streaming", "in_kernel") else None
     gidx, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
-                                 spec.topk)
+                                 spec.topk, ws=ws)
     assert smla.read_status(ws)[0] == 0
     rows = np.arange(0, spec.n_tokens, 23)
     ridx, *_ = oracle.Oracle(prob).rows(rows, attend=False)
     compare_idx(_host(gidx)[rows], ridx)
     if mode == "constant":
         assert (np.sort(_host(gidx)[rows], axis=1) == np.arange(spec.topk)[None, :]).all()
+
+
+@pytest.mark.parametrize("case", ["one_seq", "two_seqs"])
+def test_indexer_score_array_row_blocks(case):
+    """The score-array mode in several row blocks (a workspace holding one
+    block of 700 rows, or 608 rows of each of two sequences): the rows of every
+    block match the oracle, the rows at block boundaries included, and the
+    index sets equal those of a call with the full workspace (one block)."""
+    if case == "one_seq":
+        spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=2000, prefix_len=18000, shuffled=True)
+        prob = wl.make(spec, "cpu")
+        dev = prob.to("cuda")
+        n_seqs, qps, block = 1, spec.n_tokens, 700
+        max_len = spec.prefix_len + spec.n_tokens
+        seq_lens = torch.tensor([max_len], dtype=torch.int32, device="cuda")
+        rows = sorted({0, 1, 699, 700, 701, 1399, 1400, 1999} | set(range(3, 2000, 97)))
+    else:
+        spec = wl.scaled(wl.SPECS["decode"], n_seqs=2, q_per_seq=900, len_min=18000, len_max=26000, seed=7)
+        prob = wl.make(spec, "cpu")
+        dev = prob.to("cuda")
+        n_seqs, qps, block = 2, 900, 608
+        seq_lens = dev.seq_lens
+        max_len = int(seq_lens.max())
+        rows = sorted({0, 607, 608, 899, 900, 1507, 1508, 1799} | set(range(5, 1800, 89)))
+    stride = (max_len + 31) // 32 * 32
+    ws = smla.workspace(256 + n_seqs * block * stride * 4, "cuda")
+    gidx, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, max_len, qps, dev.q_idx, dev.w, spec.topk,
+                                 ws=ws)
+    assert smla.read_status(ws)[0] == 0
+    full, ws2 = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, max_len, qps, dev.q_idx, dev.w, spec.topk)
+    assert smla.read_status(ws2)[0] == 0
+    assert torch.equal(torch.sort(gidx, dim=1).values, torch.sort(full, dim=1).values)
+    ridx, *_ = oracle.Oracle(prob).rows(np.array(rows), attend=False)
+    compare_idx(_host(gidx)[rows], ridx)
 
 
 @pytest.mark.parametrize("mode", ["constant", "binary"])
