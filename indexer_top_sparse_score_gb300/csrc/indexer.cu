@@ -2071,6 +2071,295 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
 }
 
 // ---------------------------------------------------------------------------
+// Step 2 of the split and score-array modes for rows of at most kSelBmBits
+// keys: the same exact top-k as select_kernel with one full read of the row.
+//  1. a sample (32 runs of 128 keys spread over the row) gives a key t_lo
+//     that about 1.25 k + 4 sqrt(k) keys of the row reach, were the sample
+//     representative (one 4096-bin histogram of the sample's key range);
+//  2. one pass stages every key >= t_lo (and its position) in shared memory,
+//     one atomic per warp and 128 keys;
+//  3. when between k and kSsCand keys were staged, they hold the row's top-k:
+//     the k-th key follows from 12-bit digits over their key range, and among
+//     keys equal to it the lowest positions win (ranked by counting when few);
+//     otherwise (the sample misjudged the row) the exact radix selection runs
+//     over the whole row in global memory;
+//  4. the selected positions are marked in a bitmap of the row and written
+//     out in ascending order.
+// 512 threads and ~96 KB of shared memory: two rows per SM at a time, so one
+// row's pass over HBM overlaps the other's selection.
+constexpr int kSsThreads = 512;
+constexpr int kSsWarps = kSsThreads / 32;
+constexpr int kSsCand = 6144;       // staged candidates
+constexpr int kSsRuns = 32;         // sampled runs of 128 keys
+constexpr int kSsSample = kSsRuns * 128;
+constexpr int kSsBins = 4096;       // 12-bit digits
+static_assert(kSsSample <= kSsCand, "the sample is held in the candidate space");
+
+struct SsSmem {
+  uint32_t bm[kSelBmBits / 32];  // selected positions of the row
+  uint32_t cand_key[kSsCand], cand_idx[kSsCand];
+  uint32_t hist[kSsBins];        // digit histogram; tie list; dense_select's 3 x 256 words
+  uint32_t red[2 * kSsWarps];
+  uint32_t wsum[kSsWarps];
+  uint32_t n_cand, bin, above, thr_idx;
+};
+
+// Block-wide minimum and maximum of v over all threads (every thread gets them).
+__device__ __forceinline__ void ss_minmax(SsSmem& S, uint32_t& lo, uint32_t& hi, int tid) {
+  const int lane = tid & 31, w = tid >> 5;
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane == 0) {
+    S.red[w] = lo;
+    S.red[kSsWarps + w] = hi;
+  }
+  __syncthreads();
+  lo = 0xFFFFFFFFu;
+  hi = 0;
+#pragma unroll
+  for (int i = 0; i < kSsWarps; ++i) {
+    lo = min(lo, S.red[i]);
+    hi = max(hi, S.red[kSsWarps + i]);
+  }
+  __syncthreads();  // red is reused
+}
+
+// Histogram of (key - lo) >> shift over kSsBins bins for the keys in [lo, hi]
+// of keys[0, n) (shared memory), then the top-down scan: the bin holding the
+// r-th largest and the number of keys in higher bins (S.bin, S.above).
+__device__ __forceinline__ void ss_digit(SsSmem& S, const uint32_t* keys, int n, uint32_t lo, uint32_t hi,
+                                         int shift, uint32_t r, int tid) {
+  const int lane = tid & 31, w = tid >> 5;
+  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;
+  __syncthreads();
+  for (int e = tid; e < n; e += kSsThreads) {
+    const uint32_t v = keys[e];
+    if (v >= lo && v <= hi) atomicAdd(&S.hist[(v - lo) >> shift], 1u);
+  }
+  __syncthreads();
+  constexpr int kPer = kSsBins / kSsThreads;  // bins per thread, from the top
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    c[i] = S.hist[kSsBins - 1 - (kPer * tid + i)];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) S.wsum[w] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum;
+  for (int w2 = 0; w2 < w; ++w2) run += S.wsum[w2];
+  if (run < r && run + sum >= r) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (run + c[i] >= r) {
+        S.bin = static_cast<uint32_t>(kSsBins - 1 - (kPer * tid + i));
+        S.above = run;
+        break;
+      }
+      run += c[i];
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int ss_shift(uint32_t lo, uint32_t hi) {
+  const uint32_t range = hi - lo;
+  return range >= static_cast<uint32_t>(kSsBins) ? (32 - __clz(range)) - 12 : 0;
+}
+
+__global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) uint8_t ss_raw[];
+  SsSmem& S = *reinterpret_cast<SsSmem*>(ss_raw);
+  const int srow = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int seq = srow / p.block_rows;
+  const int r_in = p.row_base + (srow - seq * p.block_rows);
+  const int row = seq * p.q_per_seq + r_in;
+  const int len = p.seq_lens ? p.seq_lens[seq] : p.prefix_len + p.q_per_seq;
+  const int pos = len - p.q_per_seq + r_in;
+  const int n = min(pos + 1, static_cast<int>(p.score_stride));  // keys 0..pos (with a score slot)
+  const uint32_t* keys = p.scores + static_cast<int64_t>(srow) * p.score_stride;
+  int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
+  float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
+  const int k = p.topk;
+  if (n <= k) {
+    for (int e = tid; e < k; e += kSsThreads) {
+      o[e] = e < n ? e : -1;
+      if (os) os[e] = e < n ? key_score(keys[e]) : 0.0f;
+    }
+    return;
+  }
+  auto sync = []() { __syncthreads(); };
+  const int nw = (n + 31) / 32;
+  for (int b = tid; b < nw; b += kSsThreads) S.bm[b] = 0;
+  if (tid == 0) S.n_cand = 0;
+  // 1. a key that about 1.25 k + 4 sqrt(k) keys reach, from the sample
+  uint32_t t_lo = 0;
+  if (n > kSsCand) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
+    for (int e = tid; e < kSsSample / 4; e += kSsThreads) {
+      const int run = e >> 5, u = e & 31;
+      const int start = static_cast<int>(static_cast<int64_t>(n - 128) * run / (kSsRuns - 1)) & ~3;
+      const uint4 v = *reinterpret_cast<const uint4*>(keys + start + 4 * u);
+      *reinterpret_cast<uint4*>(&S.cand_key[4 * e]) = v;
+      lo = min(min(lo, min(v.x, v.y)), min(v.z, v.w));
+      hi = max(max(hi, max(v.x, v.y)), max(v.z, v.w));
+    }
+    ss_minmax(S, lo, hi, tid);  // also orders the sample's stores before the histogram
+    const float expect = static_cast<float>(k) * kSsSample / static_cast<float>(n);
+    const int r = static_cast<int>(ceilf(1.25f * expect + 4.0f * sqrtf(expect) + 16.0f));
+    if (r < kSsSample) {
+      const int shift = ss_shift(lo, hi);
+      ss_digit(S, S.cand_key, kSsSample, lo, hi, shift, static_cast<uint32_t>(r), tid);
+      t_lo = lo + (S.bin << shift);  // the r-th largest sampled key's bin, from its lower edge
+    }
+  }
+  __syncthreads();  // the bitmap and count are cleared; the sample's space takes the candidates
+  // 2. every key >= t_lo to the staging space, in 128-key warp segments
+  uint32_t c_hi = 0;
+  {
+    constexpr int U = 4;
+    for (int s0 = w * 128; s0 < n; s0 += U * kSsThreads * 4) {
+      uint4 kv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e0 = s0 + u * kSsThreads * 4 + 4 * lane;
+        kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e0 = s0 + u * kSsThreads * 4 + 4 * lane;
+        const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+        uint32_t take = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) take |= (e0 + q < n && kk[q] >= t_lo ? 1u : 0u) << q;
+        if (!__ballot_sync(0xFFFFFFFFu, take != 0)) continue;
+        const uint32_t c = __popc(take);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += t2;
+        }
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&S.n_cand, incl);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if ((take >> q) & 1u) {
+            c_hi = max(c_hi, kk[q]);
+            if (base < static_cast<uint32_t>(kSsCand)) {
+              S.cand_key[base] = kk[q];
+              S.cand_idx[base] = static_cast<uint32_t>(e0 + q);
+            }
+            ++base;
+          }
+      }
+    }
+  }
+  uint32_t c_lo = t_lo;
+  ss_minmax(S, c_lo, c_hi, tid);  // every thread's stores and count precede what follows
+  const int nc = static_cast<int>(S.n_cand);
+  uint32_t tk = 0, ti = 0xFFFFFFFFu;
+  bool exact_row = true;  // false: selected over the staged keys
+  if (nc >= k && nc <= kSsCand) {
+    exact_row = false;
+    if (nc > k) {
+      // 3. the k-th key: 12-bit digits over the staged keys' range
+      uint32_t lo = t_lo, hi = c_hi, r = static_cast<uint32_t>(k), m = 0;
+      while (true) {
+        const int shift = ss_shift(lo, hi);
+        ss_digit(S, S.cand_key, nc, lo, hi, shift, r, tid);
+        const uint32_t b = S.bin;
+        r -= S.above;
+        m = S.hist[b];
+        const uint64_t nlo = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(b) << shift);
+        const uint64_t nhi = nlo + ((1ull << shift) - 1ull);
+        lo = static_cast<uint32_t>(nlo);
+        hi = static_cast<uint32_t>(nhi < hi ? nhi : hi);
+        __syncthreads();  // S.bin, S.above and the histogram are read
+        if (shift == 0) break;
+      }
+      tk = lo;
+      if (r < m) {
+        // m staged keys equal tk, the r lowest positions win
+        if (m <= static_cast<uint32_t>(kSsBins) && m <= 1024u) {
+          if (tid == 0) S.n_cand = 0;
+          __syncthreads();
+          for (int e = tid; e < nc; e += kSsThreads)
+            if (S.cand_key[e] == tk) S.hist[atomicAdd(&S.n_cand, 1u)] = S.cand_idx[e];
+          __syncthreads();
+          for (int t = tid; t < static_cast<int>(m); t += kSsThreads) {
+            const uint32_t mine = S.hist[t];
+            uint32_t below = 0;
+            for (uint32_t j = 0; j < m; ++j) below += S.hist[j] < mine;
+            if (below == r - 1) S.thr_idx = mine;
+          }
+          __syncthreads();
+          ti = S.thr_idx;
+        } else {
+          dense_select<kSsThreads>(S.cand_key, S.cand_idx, nc, k, tid, S.hist, S.red, sync, tk, ti);
+        }
+      }
+    }
+    for (int e = tid; e < nc; e += kSsThreads) {
+      const uint32_t i = S.cand_idx[e];
+      if (selected(S.cand_key[e], i, tk, ti)) atomicOr(&S.bm[i >> 5], 1u << (i & 31));
+    }
+  }
+  if (exact_row) {
+    // 3'. the whole row from global memory; bitmap word = 8 lanes x 4 keys
+    dense_select<kSsThreads>(keys, nullptr, n, k, tid, S.hist, S.red, sync, tk, ti);
+    for (int s0 = w * 128; s0 < n; s0 += kSsThreads * 4) {
+      const int e0 = s0 + 4 * lane;
+      const uint4 k4 = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      uint32_t bits = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti)) bits |= 1u << ((e0 + q) & 31);
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
+      if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
+    }
+  }
+  __syncthreads();
+  // 4. ascending positions: thread t owns a run of bitmap words
+  const int per = (nw + kSsThreads - 1) / kSsThreads;
+  const int w0 = tid * per, w1 = min(nw, w0 + per);
+  uint32_t cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(S.bm[i]);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o2 = 1; o2 < 32; o2 <<= 1) {
+    const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+    if (lane >= o2) incl += t2;
+  }
+  if (lane == 31) S.wsum[w] = incl;
+  __syncthreads();
+  uint32_t at = incl - cnt;
+  for (int w2 = 0; w2 < w; ++w2) at += S.wsum[w2];
+  for (int i = w0; i < w1; ++i) {
+    uint32_t bits = S.bm[i];
+    while (bits) {
+      const int e = i * 32 + __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (at < static_cast<uint32_t>(k)) {
+        o[at] = e;
+        if (os) os[at] = key_score(keys[e]);
+      }
+      ++at;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Group mode, deferred rows: the exact top-k of one row's candidate buffer
 // (copied out by the indexer when it held more than topk entries). One
 // 128-thread CTA per row; the buffer is staged in shared memory and selected
@@ -2178,11 +2467,22 @@ bool set_select_attr() {
   static bool done = false;
   if (!done) {
     if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess)
+                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess ||
+        cudaFuncSetAttribute(select_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SsSmem))) != cudaSuccess)
       return false;
     done = true;
   }
   return true;
+}
+
+// step 2 of the split and score-array modes over n_rows score rows of at most
+// max_keys keys each
+int launch_select(const SelectParams& sp, int n_rows, int32_t max_keys, cudaStream_t stream) {
+  if (!set_select_attr()) return SMLA_ERR_CUDA;
+  if (max_keys <= kSelBmBits) select_sampled_kernel<<<n_rows, kSsThreads, sizeof(SsSmem), stream>>>(sp);
+  else select_kernel<<<n_rows, kSelThreads, sizeof(SelSmem), stream>>>(sp);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
 template <int HI, bool SPLIT, bool DENSE, bool TOK = false, bool STORE = false>
@@ -2355,7 +2655,6 @@ int launch_indexer(const IndexerLaunch& L) {
         prm.score_stride = store_stride(L.max_seq_len);
         SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.prefix_len, L.q_per_seq, L.topk,
                         0, 0, L.out_idx, L.out_scores};
-        if (!set_select_attr()) return SMLA_ERR_CUDA;
         for (int32_t r0 = 0; r0 < L.q_per_seq; r0 += block) {
           prm.row_base = r0;
           prm.block_rows = std::min(block, L.q_per_seq - r0);
@@ -2365,8 +2664,8 @@ int launch_indexer(const IndexerLaunch& L) {
           if (rc != SMLA_OK) return rc;
           sp.row_base = r0;
           sp.block_rows = prm.block_rows;
-          select_kernel<<<L.n_seqs * prm.block_rows, kSelThreads, sizeof(SelSmem), L.stream>>>(sp);
-          if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+          const int rs = launch_select(sp, L.n_seqs * prm.block_rows, L.max_seq_len, L.stream);
+          if (rs != SMLA_OK) return rs;
         }
         return SMLA_OK;
       }
@@ -2421,10 +2720,7 @@ int launch_indexer(const IndexerLaunch& L) {
   }
   SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, 0, L.q_per_seq, L.topk, 0, L.q_per_seq,
                   L.out_idx, L.out_scores};
-  if (!set_select_attr()) return SMLA_ERR_CUDA;
-  select_kernel<<<prm.n_rows, kSelThreads, sizeof(SelSmem), L.stream>>>(sp);
-  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
-  return SMLA_OK;
+  return launch_select(sp, prm.n_rows, L.max_seq_len, L.stream);
 }
 
 }  // namespace smla
