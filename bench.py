@@ -205,9 +205,10 @@ class PrefillStep:
         return smla.read_status_chunks(self.ws, len(self.chunks))[0]
 
     def launches(self):
-        """Kernels one step launches: per chunk the indexer, the deferred
-        selection (rows too long for the in-kernel selection), the f16 shadow
-        (BF16 caches) and the attention."""
+        """Kernels one step launches: per chunk the indexer, the selection
+        kernel of rows longer than 16,384 keys (over the score array up to
+        262,144 keys, over deferred candidate buffers beyond; one row block per
+        chunk at these sizes), the f16 shadow (BF16 caches) and the attention."""
         n = 0
         for P, T in self.chunks:
             n += 2 + (self.spec.kv_dtype == "bf16")

@@ -52,6 +52,7 @@ constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
+constexpr int kStoreThreads = 640;  // score-array mode: 16 epilogue warps
 // Streaming prefill with 32 indexer heads (see the epilogue): the eight
 // epilogue warps meet on one mbarrier of the kTokBars slots.
 constexpr int kTokBars = 4;
@@ -239,7 +240,7 @@ __device__ __forceinline__ void smem_inc(uint32_t* p) {
 // STORE: prefill at 32 heads writing every score to a score array in global
 // memory (select_kernel takes the exact top-k afterwards).
 template <int HI, bool SPLIT, bool DENSE, bool TOK, bool STORE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IdxParams p) {
   static_assert(!TOK || (HI == 32 && !SPLIT && !DENSE), "the streaming 32-head mode is a prefill mode");
@@ -303,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], (SPLIT || DENSE || TOK || STORE) ? 4 : kEpiThreads / 32);  // one warpgroup per buffer
+      // one warpgroup per buffer; the score-array mode: every epilogue warp
+      mbar_init(&acc_empty[i], STORE ? (kStoreThreads - 128) / 32 : (SPLIT || DENSE || TOK) ? 4 : kEpiThreads / 32);
     }
     for (int i = 0; i < kTokBars; ++i) mbar_init(&wg_bar[i], 8);
     for (int i = 0; i < 16; ++i) wcnt[i] = 0;  // TOK: per-row counters
@@ -477,64 +479,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     if constexpr (STORE) {
       // ---------------------------------------------------------- epilogue (32 heads, score array)
-      // The two warpgroups take the key tiles in turn (warpgroup g the tiles of
-      // CTA tile-counter parity g, so each owns two of the four accumulator
-      // buffers). A warp loads the four rows' 32 columns of its TMEM lane
-      // quadrant (32 keys), releases the accumulator and writes the four rows'
-      // score keys to the score array: 128 contiguous bytes per row, nothing
-      // shared between warps. The weights of consecutive items alternate
-      // between two buffers, so the eight warps meet once per item.
-      constexpr int kRows = 4;  // rows per item (N = 128 at 32 heads)
-      const int ew = warp - 4;  // 0..7
-      const int wg = ew >> 2;
+      // Sixteen epilogue warps: warpgroup r takes row r of every item (its 32
+      // head weights in registers) and warp (r, q) the 32 keys of TMEM lane
+      // quadrant q of every tile. A warp loads its row's 32 columns, releases
+      // the accumulator (all sixteen warps release each one) and writes its 32
+      // score keys to the row's score array: 128 contiguous bytes, nothing
+      // shared between warps.
+      const int ew = warp - 4;  // 0..15
+      const int rr = ew >> 2;   // row of the item
       const int q = warp & 3;   // TMEM lane quadrant
-      const int tid_e = ew * 32 + lane;
-      uint32_t bar_phase = 0;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(rr * HI);
+      uint32_t ac = 0;
       bool ok = true;
-      auto meet = [&]() -> bool {
-        __syncwarp();
-        bool r = true;
-        if (lane == 0) {
-          mbar_arrive(&wg_bar[0]);
-          r = mbar_wait_spin(&wg_bar[0], bar_phase & 1u, abort_v, p.status);
-        }
-        ++bar_phase;
-        r = __shfl_sync(0xFFFFFFFFu, r, 0);
-        __syncwarp();
-        if (!r) ok = false;
-        return r;
-      };
-      uint32_t ac = 0, n_items_seen = 0;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
       for (int k = 0; ok; ++k) {
         Item it;
         const int r = next_item(p, k, it, pref);
         if (r < 0) break;
         if (r == 0) continue;
         if (it.trivial) {
-          // every key of every row is selected: 0..pos, then -1
-          for (int j = 0; j < it.nrows; ++j) {
-            const int n = it.pos0 + j + 1;
-            int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + j) * p.topk;
-            for (int e = tid_e; e < p.topk; e += 256) o[e] = e < n ? e : -1;
+          // every key of the row is selected: 0..pos, then -1
+          if (rr < it.nrows) {
+            const int n = it.pos0 + rr + 1;
+            int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + rr) * p.topk;
+            for (int e = (ew & 3) * 32 + lane; e < p.topk; e += 128) o[e] = e < n ? e : -1;
           }
           continue;
         }
-        // the rows' head weights; the buffer of two items back is free: every
-        // warp has met at the previous item's start, after that item's tiles
-        float* wb = (n_items_seen & 1u) ? reinterpret_cast<float*>(hist) : wbuf;
-        ++n_items_seen;
-        if (tid_e < kRows * HI) {
-          const int j = tid_e / HI;
-          wb[tid_e] = j < it.nrows ? __ldg(p.w + static_cast<size_t>(it.row0 + j) * HI + (tid_e % HI)) : 0.0f;
-        }
-        if (!meet()) break;
-        const float4* wv4 = reinterpret_cast<const float4*>(wb);
+        const bool active = rr < it.nrows;  // the last item of a sequence may have fewer rows
+        float wr[HI];
+#pragma unroll
+        for (int h = 0; h < HI; ++h) wr[h] = active ? __ldg(p.w + static_cast<size_t>(it.row0 + rr) * HI + h) : 0.0f;
+        uint32_t* out_row = p.scores + static_cast<int64_t>(it.srow + rr) * p.score_stride;
+        const int pos = it.pos0 + rr;  // the row sees keys 0..pos
         const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
         const uint32_t ac0 = ac;
         const int nt = it.t1 - it.t0;
-        uint32_t* srow = p.scores + static_cast<int64_t>(it.srow) * p.score_stride;
-        for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt; tt += 2) {
+        for (int tt = 0; tt < nt; ++tt) {
           const uint32_t gt = ac0 + tt;
           const int buf = gt & 3;
           if (__any_sync(0xFFFFFFFFu, !mbar_wait(&acc_full[buf], (gt >> 2) & 1u, abort_v, p.status))) {
@@ -542,37 +522,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t raw[kRows][32];
-#pragma unroll
-          for (int j = 0; j < kRows; ++j)
-            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN + j * HI), raw[j]);
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN), raw);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          if (!active) continue;
           const int t = tile_at(it, tt);
           const int s = t * kTileKeys + q * 32 + lane;
           float ks = 1.0f;
-          if (p.k_scale && s < it.key_hi) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          if (p.k_scale && s <= pos) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int j = 0; j < kRows; ++j) {
-            float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int h = 0; h < HI; h += 8) {
-              const float4 wa = wv4[(j * HI + h) / 4], wb2 = wv4[(j * HI + h) / 4 + 1];
-              fma2(a[0], a[1], wa.x, wa.y, fmaxf(__uint_as_float(raw[j][h + 0]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 1]), 0.0f));
-              fma2(a[2], a[3], wa.z, wa.w, fmaxf(__uint_as_float(raw[j][h + 2]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 3]), 0.0f));
-              fma2(a[4], a[5], wb2.x, wb2.y, fmaxf(__uint_as_float(raw[j][h + 4]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 5]), 0.0f));
-              fma2(a[6], a[7], wb2.z, wb2.w, fmaxf(__uint_as_float(raw[j][h + 6]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 7]), 0.0f));
-            }
-            if (j < it.nrows && s < it.key_hi && s <= it.pos0 + j)
-              srow[static_cast<int64_t>(j) * p.score_stride + s] =
-                  score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+          for (int h = 0; h < HI; h += 8) {
+            fma2(a[0], a[1], wr[h + 0], wr[h + 1], fmaxf(__uint_as_float(raw[h + 0]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 1]), 0.0f));
+            fma2(a[2], a[3], wr[h + 2], wr[h + 3], fmaxf(__uint_as_float(raw[h + 2]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 3]), 0.0f));
+            fma2(a[4], a[5], wr[h + 4], wr[h + 5], fmaxf(__uint_as_float(raw[h + 4]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 5]), 0.0f));
+            fma2(a[6], a[7], wr[h + 6], wr[h + 7], fmaxf(__uint_as_float(raw[h + 6]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 7]), 0.0f));
           }
+          if (s <= pos)
+            out_row[s] = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
         }
         ac = ac0 + nt;
       }
@@ -2514,7 +2488,8 @@ int launch_indexer_t(const IndexerLaunch& L, const IdxParams& prm) {
                          : prm.n_seqs <= kMaxPrefixSeqs ? static_cast<int>(std::min<int64_t>(split_tiles, 1 << 30))
                                                         : prm.n_items;
   const int grid = std::max(1, std::min(num_sms(), grid_items));
-  indexer_kernel<HI, SPLIT, DENSE, TOK, STORE><<<grid, kThreads, smem, L.stream>>>(map_k, map_q, prm);
+  indexer_kernel<HI, SPLIT, DENSE, TOK, STORE><<<grid, STORE ? kStoreThreads : kThreads, smem, L.stream>>>(map_k, map_q,
+                                                                                                   prm);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
