@@ -257,7 +257,11 @@ def chunk_bounds(n_tokens: int, chunk) -> list:
 class HostPrefill:
     """Prefill from pinned HOST buffers: q, q_idx and w are copied in and out /
     lse copied back chunk by chunk, on two copy streams, so the copies of one
-    chunk overlap the kernels of its neighbours. Each chunk of query tokens is
+    chunk overlap the kernels of its neighbours. The kernels run on a stream
+    of the object's own, joined to the caller's stream by one event at each
+    end: work on the legacy default stream waits for every other blocking
+    stream, so running the kernels there would hold each chunk's copies back
+    until the kernels before them end. Each chunk of query tokens is
     one smla_sparse_mla_prefill call with the earlier tokens as its prefix (the
     cache already holds every token's rows), which gives the same rows the
     single call would. `chunk` is a chunk size, or a list of chunk sizes that
@@ -289,15 +293,18 @@ class HostPrefill:
                    for a, b in self.chunks)
         self.ws = workspace(need + STATUS_BYTES * len(self.chunks), device)
         self.s_in, self.s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        self.s_comp = torch.cuda.Stream(device)
         n = len(self.chunks)
         self.ev_in = [torch.cuda.Event() for _ in range(n)]
         self.ev_comp = [torch.cuda.Event() for _ in range(n)]
         self.ev_out = [torch.cuda.Event() for _ in range(n)]
 
     def run(self, q_h, q_idx_h, w_h, out_h, lse_h, stream=None):
-        comp = torch.cuda.current_stream() if stream is None else stream
+        caller = torch.cuda.current_stream() if stream is None else stream
+        comp = self.s_comp
         start = torch.cuda.Event()
-        start.record(comp)
+        start.record(caller)
+        comp.wait_event(start)
         self.s_in.wait_event(start)
         self.s_out.wait_event(start)
         for c, (a, b) in enumerate(self.chunks):
@@ -319,7 +326,10 @@ class HostPrefill:
                 lse_h[a:b].copy_(self.lse[a:b], non_blocking=True)
                 self.ev_out[c].record(self.s_out)
         for c in range(len(self.chunks)):
-            comp.wait_event(self.ev_out[c])  # the call ends on `stream` once every result is on the host
+            caller.wait_event(self.ev_out[c])  # the call ends on `stream` once every result is on the host
+        done = torch.cuda.Event()
+        done.record(comp)
+        caller.wait_event(done)
 
     def read_status(self, stream=None):
         """(status code, raw bits) over every chunk of the last run() (waits on
