@@ -16,25 +16,36 @@
 //               = k_I_tile . q_I^T with tcgen05 (kind::f8f6f4 for e4m3,
 //               kind::f16 for bf16), fp32 accumulators in a ring of up to
 //               four TMEM buffers (warp 2 also allocates TMEM);
-//   warps 4-11  two epilogue warpgroups; each thread owns one key (TMEM lane)
-//               and computes the ReLU + head-weighted sum in registers, then
-//               streams the keys that beat the token's threshold into a
-//               per-token candidate buffer in shared memory. A full buffer is
-//               compacted to its exact top-k by a radix select, which also
-//               raises the threshold. The T x N score matrix never leaves the
-//               SM.
+//   warps 4..   the epilogue: each thread owns one key (TMEM lane) and
+//               computes the ReLU + head-weighted sum of its query rows in
+//               registers (fp32, packed FMAs).
 // Work items: prefill ("group mode") takes TQ consecutive rows of one
 // sequence against all their keys; items are handed out in head/tail pairs
 // (the i-th cheapest with the i-th most expensive, the "V" pairing of the
 // page's PCP section applied across SMs) so every CTA gets the same mix of
-// short and long causal rows. When every row has at most 16,384 keys
-// ("dense" group mode, two rows per item) the candidate space holds each
-// row's full score array instead of a candidate buffer: scores are stored at
-// their key's position, with no admission test or compaction while the tiles
-// stream, and the exact top-k of each row is taken from shared memory at the
-// end of the item. Decode ("split mode") takes all rows of one sequence
-// against one block of 8192 keys and writes every score to the row's score
-// array; select_kernel then takes each row's exact top-k.
+// short and long causal rows. How a row's top-k is taken depends on its
+// length:
+//   dense      rows of at most 16,384 keys (two rows per item): every score
+//              goes to the row's array in shared memory at its key's
+//              position; the exact top-k is taken there at the end of the
+//              item. The score matrix never leaves the SM.
+//   score      32 indexer heads, rows of up to 262,144 keys (four rows per
+//   array      item, sixteen epilogue warps, one row per warpgroup): every
+//              score goes to a per-row array in global memory with coalesced
+//              stores, nothing shared between warps; select_sampled_kernel
+//              then takes each row's exact top-k with one read of the row.
+//              Rows go in blocks whose array fits the workspace.
+//   streaming  other long rows, or a workspace too small for a score-array
+//              block: scores that beat the row's threshold go to a candidate
+//              buffer in shared memory; a full buffer is cut to a superset
+//              of the row's top-k by a radix pass, which raises the
+//              threshold (at 32 heads the two warpgroups take the tiles in
+//              turn and the eight warps share the four rows' buffers). The
+//              final exact selection runs in finish_kernel, or here when the
+//              workspace has no room for the buffers.
+// Decode ("split mode") takes all rows of one sequence against one block of
+// key tiles and writes every score to the row's score array; the selection
+// kernel then takes each row's exact top-k.
 #include <algorithm>
 
 #include "common.cuh"

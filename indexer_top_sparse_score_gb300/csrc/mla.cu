@@ -16,18 +16,19 @@
 // filled in five groups ({0,1} {2,3} {4,5} {6,7} {8}). PV slice d frees
 // group d, so the next block's chunks load while PV is still running; the
 // rope chunk (8) holds P^T once QK has read it.
-//   warps 8-15  gather producers: key -> page -> pool row, row pieces into the
-//               swizzled tile (cp.async from an f16 copy of the rows, or load +
-//               widen bf16/e4m3 -> f16), per-row logit/probability scales; they
-//               also widen the query to f16 once per query row;
 //   warp 0      MMA issuer (one thread);
-//   warps 4-7   softmax, one thread per selected row: logits of all heads of
+//   warps 4-11  softmax, one thread per selected row and half of the heads
+//               (two warps per TMEM lane quadrant): logits of its heads for
 //               its row, online softmax in the log2 domain against a per-head
 //               reference max that is only raised (and O, l rescaled) when a
 //               logit exceeds it by more than 2^8, P^T row to shared memory,
 //               per-row partial sums of P in TMEM; at the end of a query row
 //               the partial sums are reduced across rows and O^T is
-//               normalised and written out.
+//               normalised and written out;
+//   warps 12-15 gather producers: key -> page -> pool row, row pieces into the
+//               swizzled tile (cp.async from an f16 copy of the rows, or load +
+//               widen bf16/e4m3 -> f16), per-row logit/probability scales; they
+//               also widen the query to f16 once per query row.
 // All MMA operands are f16: e4m3 -> f16 is exact and bf16 -> f16 is exact in
 // the f16 normal range, and f16 gives the probabilities 11 significant bits
 // (bf16 would give 8, which alone costs ~1e-3 relative output error). For
