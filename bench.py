@@ -87,6 +87,13 @@ def measured_traffic(kernel, summary):
     return None
 
 
+def stage_traffic(kernels, summary):
+    """Summed DRAM bytes per launch of the kernels of one stage, or None if any
+    is missing or stale."""
+    parts = [measured_traffic(k, summary) for k in kernels]
+    return None if any(x is None for x in parts) else sum(parts)
+
+
 def dist_setup(n_gpus):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
@@ -208,10 +215,11 @@ class PrefillStep:
         """Kernels one step launches: per chunk the indexer, the selection
         kernel of rows longer than 16,384 keys (over the score array up to
         262,144 keys, over deferred candidate buffers beyond; one row block per
-        chunk at these sizes), the f16 shadow (BF16 caches) and the attention."""
+        chunk at these sizes), the f16 copy of the rows (BF16 and per-token FP8
+        caches) and the attention."""
         n = 0
         for P, T in self.chunks:
-            n += 2 + (self.spec.kv_dtype == "bf16")
+            n += 2 + (self.spec.kv_dtype in ("bf16", "fp8"))  # the f16 copy: BF16 and per-token FP8 caches
             if P + T > 16384:
                 n += 1
         return n
@@ -510,6 +518,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle rows of the CPU baseline (0: the default)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: use this many query tokens instead of the workload's")
+    ap.add_argument("--prefix", type=int, default=-1,
+                    help="profiling only: use this prefix length (with --tokens: one chunk of the workload at that "
+                         "position)")
     ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the host-buffer pass")
     ap.add_argument("--no-extras", action="store_true",
                     help="profiling only: skip the extra workloads (16K prefill, 1M prefix, decode)")
@@ -536,6 +547,8 @@ def main():
     spec = wl.SPECS[args.workload]
     if args.tokens:
         spec = wl.scaled(spec, n_tokens=args.tokens)
+    if args.prefix >= 0:
+        spec = wl.scaled(spec, prefix_len=args.prefix)
     dev = wl.make(spec, "cuda")
     T, H, k, P = spec.n_tokens, spec.n_heads, spec.topk, spec.prefix_len
     ps = PrefillStep(spec, dev)
@@ -584,11 +597,11 @@ def main():
                 "achieved": kernels["indexer_topk"]["tflops_fp8"], "peak": 2 * pk["bf16_sust"],
                 "peak_src": f"{pk['src']} bf16 sustained x2 (the nominal fp8/bf16 ratio; the kernel runs inside "
                             "a long step)",
-                "traffic": measured_traffic("indexer_kernel", f"dram_traffic_{spec.name}.md")}
+                "traffic": stage_traffic(("indexer_kernel", "select_sampled_kernel"), f"dram_traffic_{spec.name}.md")}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["per_launch"] = (f"achieved = the stage's algorithmic FLOPs over the step's {n_launch} calls / their summed "
                           "event time (the indexer stage times the scoring kernel and the selection kernel together)")
-    if args.tokens:
+    if args.tokens or args.prefix >= 0:
         roof["traffic"] = None
 
     launches_per_step = ps.launches()
