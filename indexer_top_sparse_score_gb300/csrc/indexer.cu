@@ -63,8 +63,7 @@ constexpr int kStageBytes = kTileKeys * kIdxRowBytes;  // 16 KB
 constexpr int kMaxN = 128;                             // TQ * H_I
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 384;
-constexpr int kStoreRowsPerWarp = 1;                                    // score-array mode: rows per epilogue warp
-constexpr int kStoreThreads = 128 + 32 * 4 * (4 / kStoreRowsPerWarp);    // 4 rows x 4 lane quadrants
+constexpr int kStoreThreads = 640;  // score-array mode: 16 epilogue warps, one query row per warpgroup
 // Streaming prefill with 32 indexer heads (see the epilogue): the eight
 // epilogue warps meet on one mbarrier of the kTokBars slots.
 constexpr int kTokBars = 4;
@@ -491,17 +490,16 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
   } else if (warp >= 4) {
     if constexpr (STORE) {
       // ---------------------------------------------------------- epilogue (32 heads, score array)
-      // Warpgroup g takes rows kR*g .. kR*g + kR - 1 of every item (their head
-      // weights in registers) and warp (g, q) the 32 keys of TMEM lane
-      // quadrant q of every tile. A warp loads its rows' 32 columns each,
-      // releases the accumulator (every epilogue warp releases each one) and
-      // writes its 32 score keys per row to the rows' score arrays: 128
-      // contiguous bytes per row, nothing shared between warps.
-      constexpr int kR = kStoreRowsPerWarp;
-      const int ew = warp - 4;
-      const int r0 = (ew >> 2) * kR;  // first row of this warp in the item
-      const int q = warp & 3;         // TMEM lane quadrant
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(r0 * HI);
+      // Sixteen epilogue warps: warpgroup r takes row r of every item (its 32
+      // head weights in registers) and warp (r, q) the 32 keys of TMEM lane
+      // quadrant q of every tile. A warp loads its row's 32 columns, releases
+      // the accumulator (all sixteen warps release each one) and writes its 32
+      // score keys to the row's score array: 128 contiguous bytes, nothing
+      // shared between warps.
+      const int ew = warp - 4;  // 0..15
+      const int rr = ew >> 2;   // row of the item
+      const int q = warp & 3;   // TMEM lane quadrant
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(rr * HI);
       uint32_t ac = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -511,24 +509,19 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
         if (r == 0) continue;
         if (it.trivial) {
           // every key of the row is selected: 0..pos, then -1
-#pragma unroll
-          for (int j = 0; j < kR; ++j)
-            if (r0 + j < it.nrows) {
-              const int n = it.pos0 + r0 + j + 1;
-              int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + r0 + j) * p.topk;
-              for (int e = (ew & 3) * 32 + lane; e < p.topk; e += 128) o[e] = e < n ? e : -1;
-            }
+          if (rr < it.nrows) {
+            const int n = it.pos0 + rr + 1;
+            int32_t* o = p.out_idx + static_cast<size_t>(it.row0 + rr) * p.topk;
+            for (int e = (ew & 3) * 32 + lane; e < p.topk; e += 128) o[e] = e < n ? e : -1;
+          }
           continue;
         }
-        const int nact = min(kR, it.nrows - r0);  // rows of this warp that exist (the last item may have fewer)
-        float wr[kR][HI];
+        const bool active = rr < it.nrows;  // the last item of a sequence may have fewer rows
+        float wr[HI];
 #pragma unroll
-        for (int j = 0; j < kR; ++j)
-#pragma unroll
-          for (int h = 0; h < HI; ++h)
-            wr[j][h] = j < nact ? __ldg(p.w + static_cast<size_t>(it.row0 + r0 + j) * HI + h) : 0.0f;
-        uint32_t* out_row = p.scores + static_cast<int64_t>(it.srow + r0) * p.score_stride;
-        const int pos = it.pos0 + r0;  // row r0 + j sees keys 0..pos + j
+        for (int h = 0; h < HI; ++h) wr[h] = active ? __ldg(p.w + static_cast<size_t>(it.row0 + rr) * HI + h) : 0.0f;
+        uint32_t* out_row = p.scores + static_cast<int64_t>(it.srow + rr) * p.score_stride;
+        const int pos = it.pos0 + rr;  // the row sees keys 0..pos
         const int32_t* pt = p.page_tables + static_cast<size_t>(it.seq) * p.max_pages;
         const uint32_t ac0 = ac;
         const int nt = it.t1 - it.t0;
@@ -540,38 +533,31 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t raw[kR][32];
-#pragma unroll
-          for (int j = 0; j < kR; ++j)
-            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN + j * HI), raw[j]);
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(buf * kMaxN), raw);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
-          if (nact <= 0) continue;
+          if (!active) continue;
           const int t = tile_at(it, tt);
           const int s = t * kTileKeys + q * 32 + lane;
           float ks = 1.0f;
-          if (p.k_scale && s <= pos + nact - 1)
-            ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          if (p.k_scale && s <= pos) ks = __ldg(p.k_scale + page_of(p, pt, s / kPage) * kPage + (s % kPage));
+          float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int j = 0; j < kR; ++j) {
-            float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int h = 0; h < HI; h += 8) {
-              fma2(a[0], a[1], wr[j][h + 0], wr[j][h + 1], fmaxf(__uint_as_float(raw[j][h + 0]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 1]), 0.0f));
-              fma2(a[2], a[3], wr[j][h + 2], wr[j][h + 3], fmaxf(__uint_as_float(raw[j][h + 2]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 3]), 0.0f));
-              fma2(a[4], a[5], wr[j][h + 4], wr[j][h + 5], fmaxf(__uint_as_float(raw[j][h + 4]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 5]), 0.0f));
-              fma2(a[6], a[7], wr[j][h + 6], wr[j][h + 7], fmaxf(__uint_as_float(raw[j][h + 6]), 0.0f),
-                   fmaxf(__uint_as_float(raw[j][h + 7]), 0.0f));
-            }
-            if (j < nact && s <= pos + j)
-              out_row[static_cast<int64_t>(j) * p.score_stride + s] =
-                  score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
+          for (int h = 0; h < HI; h += 8) {
+            fma2(a[0], a[1], wr[h + 0], wr[h + 1], fmaxf(__uint_as_float(raw[h + 0]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 1]), 0.0f));
+            fma2(a[2], a[3], wr[h + 2], wr[h + 3], fmaxf(__uint_as_float(raw[h + 2]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 3]), 0.0f));
+            fma2(a[4], a[5], wr[h + 4], wr[h + 5], fmaxf(__uint_as_float(raw[h + 4]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 5]), 0.0f));
+            fma2(a[6], a[7], wr[h + 6], wr[h + 7], fmaxf(__uint_as_float(raw[h + 6]), 0.0f),
+                 fmaxf(__uint_as_float(raw[h + 7]), 0.0f));
           }
+          if (s <= pos)
+            out_row[s] = score_key((((a[0] + a[4]) + (a[1] + a[5])) + ((a[2] + a[6]) + (a[3] + a[7]))) * ks);
         }
         ac = ac0 + nt;
       }
@@ -2092,6 +2078,8 @@ constexpr int kSsCand = 6144;       // staged candidates
 constexpr int kSsRuns = 32;         // sampled runs of 128 keys
 constexpr int kSsSample = kSsRuns * 128;
 constexpr int kSsBins = 4096;       // 12-bit digits
+constexpr int kSsPass = 4 * kSsThreads * 4;  // keys per iteration of the staging pass
+constexpr int kSsPrefetchAhead = 2;          // iterations of the row prefetched into L2 ahead of the pass
 static_assert(kSsSample <= kSsCand, "the sample is held in the candidate space");
 
 struct SsSmem {
@@ -2194,6 +2182,19 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     return;
   }
   auto sync = []() { __syncthreads(); };
+  // the staging pass reads the whole row once: its next iterations are
+  // prefetched into L2 ahead of it (one bulk prefetch per iteration), the first
+  // ones while the sample is taken
+  const uint32_t row_bytes = static_cast<uint32_t>(n) * 4u;
+  auto prefetch_pass = [&](int it) {
+    const uint32_t off = static_cast<uint32_t>(it) * kSsPass * 4u;
+    if (tid == 0 && off < row_bytes) {
+      const uint32_t len = min(static_cast<uint32_t>(kSsPass) * 4u, (row_bytes - off + 15u) & ~15u);
+      prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(keys) + off, len);
+    }
+  };
+#pragma unroll
+  for (int it = 0; it < kSsPrefetchAhead; ++it) prefetch_pass(it);
   const int nw = (n + 31) / 32;
   for (int b = tid; b < nw; b += kSsThreads) S.bm[b] = 0;
   if (tid == 0) S.n_cand = 0;
@@ -2223,7 +2224,9 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   uint32_t c_hi = 0;
   {
     constexpr int U = 4;
-    for (int s0 = w * 128; s0 < n; s0 += U * kSsThreads * 4) {
+    static_assert(U * kSsThreads * 4 == kSsPass, "one pass iteration");
+    for (int s0 = w * 128, it = 0; s0 < n; s0 += U * kSsThreads * 4, ++it) {
+      prefetch_pass(it + kSsPrefetchAhead);
       uint4 kv[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
