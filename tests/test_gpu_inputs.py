@@ -140,11 +140,14 @@ def _check_guarded(out, lse, idx):
     assert not bool((idx.view == IDX_CANARY).any()), "index entry left unwritten"
 
 
-@pytest.mark.parametrize("case", ["dense", "streaming", "tiny"])
+@pytest.mark.parametrize("case", ["dense", "scores", "streaming", "tiny"])
 def test_prefill_writes_only_its_outputs(case):
     """Prefill through the product entry into outputs framed by canaries: nothing
     is written before or after out, lse and out_idx, every element inside them is
-    written, and sampled rows (including the last) match the oracle."""
+    written, and sampled rows (including the last) match the oracle. Rows of
+    more than 16,384 keys take the score array with the full workspace, and the
+    streaming candidate buffers with a workspace that holds those buffers but no
+    score-array block."""
     if case == "tiny":
         spec = wl.scaled(wl.SPECS["tiny"], n_tokens=333, prefix_len=100, shuffled=True)
     else:
@@ -152,9 +155,16 @@ def test_prefill_writes_only_its_outputs(case):
                          shuffled=True, kv_dtype="fp8")
     dev = wl.make(spec, "cuda")
     T, H, k = spec.n_tokens, spec.n_heads, spec.topk
+    ws = None
+    if case == "streaming":
+        # status | index list | f16 copy of the FP8 rows and their scales | candidate buffers
+        r256 = lambda b: (b + 255) // 256 * 256
+        n_keys = spec.prefix_len + T
+        ws = smla.workspace(256 + r256(T * k * 4) + r256(n_keys * 1152) + r256(n_keys * 4)
+                            + T * 4096 * 8 + r256(T * 4))
     out, lse, idx = _guarded_outputs(T, H, k)
     _, _, _, ws = smla.sparse_mla_prefill(dev.cache, dev.page_table, spec.prefix_len, dev.q, dev.q_idx, dev.w, k,
-                                          spec.sm_scale, out=out.view, lse=lse.view, out_idx=idx.view)
+                                          spec.sm_scale, out=out.view, lse=lse.view, out_idx=idx.view, ws=ws)
     assert smla.read_status(ws)[0] == 0
     _check_guarded(out, lse, idx)
     rows = np.array(sorted({0, T // 2, T - 2, T - 1}), dtype=np.int64)
