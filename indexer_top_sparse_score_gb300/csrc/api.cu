@@ -144,8 +144,8 @@ int smla_indexer_topk(const smla_paged_cache* cache, const int32_t* page_tables,
   const bool split = indexer_split_mode(q_per_seq, h_idx);
   if (indexer_tokens_per_cta(h_idx, topk, split, q_per_seq) <= 0) return SMLA_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return SMLA_ERR_WORKSPACE;
-  // required: status word (+ split-mode lists); the group-mode candidate
-  // buffers behind it are used when they fit
+  // required: status word (+ split-mode lists); the group-mode score array
+  // or candidate buffers behind it are used when they fit
   const size_t ws_min = round256(indexer_workspace_bytes(n_seqs, max_seq_len, q_per_seq, h_idx, topk));
   if (workspace_bytes < ws_min) return SMLA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -240,7 +240,8 @@ int smla_sparse_mla_prefill(const smla_paged_cache* cache, const int32_t* page_t
   int32_t* idx = out_idx ? out_idx : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   IndexerLaunch IL{cache, page_table, pages, 1, n_tokens, nullptr, prefix_len, static_cast<int32_t>(total), q_idx,
                    w, h_idx, topk, idx, nullptr, workspace, workspace_bytes, st};
-  // layout: status | index list | f16 shadow (BF16 and FP8 caches) | deferred candidate buffers
+  // layout: status | index list | f16 copy of the rows (BF16 and per-token FP8 caches) |
+  // the indexer's score array or deferred candidate buffers
   const size_t shadow_bytes = mla_shadow_bytes(static_cast<int32_t>(total), cache->kv_dtype);
   const size_t cand_off = ws_min + shadow_bytes;
   if (workspace_bytes > cand_off) {

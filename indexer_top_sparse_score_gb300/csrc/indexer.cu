@@ -55,7 +55,7 @@ namespace smla {
 
 namespace {
 
-constexpr int kStages = 4;         // key-tile ring in group mode (the candidate buffers need the rest)
+constexpr int kStages = 4;         // key-tile ring in group mode (the candidate / score buffers need the rest)
 constexpr int kSplitStages = 10;   // split mode keeps no candidates: 6 more stages and a second
                                    // query tile in their space
 constexpr int kTileKeys = 128;
@@ -67,7 +67,7 @@ constexpr int kStoreThreads = 640;  // score-array mode: 16 epilogue warps, one 
 // Streaming prefill with 32 indexer heads (see the epilogue): the eight
 // epilogue warps meet on one mbarrier of the kTokBars slots.
 constexpr int kTokBars = 4;
-constexpr int kHistWords = 3 * 256 * 4;  // selection histograms
+constexpr int kHistWords = 3 * 256 * 4;  // selection histograms (room for every mode's layout)
 constexpr int kMaxAcc = 4;                            // TMEM accumulator buffers at most
 constexpr int kIssuers = 2;                           // MMA issuer warps
 static_assert(kStages % kIssuers == 0 && kSplitStages % kIssuers == 0 && kMaxAcc % kIssuers == 0,
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
   uint32_t* ckey = reinterpret_cast<uint32_t*>(b_tile + kMaxN * kIdxRowBytes);
   uint32_t* cidx = ckey + kBufEntries;
   float* wbuf = reinterpret_cast<float*>(cidx + kBufEntries);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]; dense [2][4][256]; TOK [4][3][256]
-  uint32_t* scratch = hist + kHistWords;                        // [2][16]; TOK [4][16]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + kMaxN);  // [2][3][256]; dense [2][4][256]; 32-head streaming [3][256]
+  uint32_t* scratch = hist + kHistWords;                        // [2][16]; 32-head streaming [2][16]
   int32_t* cnt = reinterpret_cast<int32_t*>(scratch + 64);      // [2 tile parities][128 tokens]
   uint32_t* theta = reinterpret_cast<uint32_t*>(cnt + 256);     // [128]
   uint32_t* wsum = theta + 128;                                 // [2][2][4]

@@ -34,8 +34,10 @@ struct IndexerLaunch {
   void* workspace;          // status word + candidate lists (split mode)
   size_t workspace_bytes;
   cudaStream_t stream;
-  // group mode: room for the per-row candidate buffers of rows whose final
-  // selection is deferred to finish_kernel (null or too small: select in-kernel)
+  // group mode, rows longer than the dense mode takes: room for the score array
+  // of a block of rows (score-array mode), else for the per-row candidate buffers
+  // whose final selection is deferred to finish_kernel (null or too small for
+  // either: the selection stays in the scoring kernel)
   void* cand = nullptr;
   size_t cand_bytes = 0;
 };
@@ -90,7 +92,8 @@ int indexer_tokens_per_cta(int32_t h_idx, int32_t topk, bool split, int32_t q_pe
 int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len);
 size_t indexer_workspace_bytes(int32_t n_seqs, int32_t max_seq_len, int32_t q_per_seq, int32_t h_idx,
                                int32_t topk);
-// Group mode: bytes of the deferred per-row candidate buffers (0 if split mode).
+// Group mode: bytes of the score array (one block of rows) or of the deferred
+// per-row candidate buffers, whichever the rows use (0 if split or dense mode).
 size_t indexer_group_cand_bytes(int32_t n_rows, int32_t q_per_seq, int32_t h_idx, int32_t topk,
                                 int32_t max_seq_len);
 
