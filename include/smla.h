@@ -125,13 +125,14 @@ int smla_version(void);
  * Workspace: the returned size. When several query rows share the key stream
  * (long per-sequence batches), 256 bytes already suffice. With max_seq_len at
  * most 16384 (8192 at h_idx = 4) every row's scores fit in shared memory and
- * the exact top-k is taken there. Longer sequences at h_idx = 32 of at most
- * 262144 keys: the rest of the workspace holds a score array (4 bytes per key
- * up to max_seq_len rounded up to 32, per query row) that the scoring kernel
- * fills and a per-row kernel selects from; rows are processed in blocks (the
- * same rows of every sequence) of which the returned size holds one of up to
- * 4 GiB, or at least 608 rows per sequence. Other long sequences, or a
- * workspace too small for such a block: per-row candidate buffers (up to
+ * the exact top-k is taken there. Longer sequences at h_idx = 32: the rest of
+ * the workspace holds a score array (4 bytes per key up to max_seq_len rounded
+ * up to 32, per query row) that the scoring kernel fills and a per-row kernel
+ * selects from; rows are processed in equal blocks (the same rows of every
+ * sequence) of which the returned size holds one of up to 16 GiB, or at least
+ * 608 rows per sequence; a smaller workspace gives smaller blocks. Other head
+ * counts, or a workspace too small for a 608-row block: per-row candidate
+ * buffers (up to
  * 16384 / rows-per-work-item (key, index) pairs of 8 bytes, plus a count per
  * row) whose final exact selection then runs in a separate light kernel
  * instead of stalling the scoring pipeline; with less room still the

@@ -29,13 +29,13 @@
 //              goes to the row's array in shared memory at its key's
 //              position; the exact top-k is taken there at the end of the
 //              item. The score matrix never leaves the SM.
-//   score      32 indexer heads, rows of up to 262,144 keys (four rows per
-//   array      item, sixteen epilogue warps, one row per warpgroup): every
+//   score      32 indexer heads, longer rows (four rows per item, sixteen
+//   array      epilogue warps, one row per warpgroup): every
 //              score goes to a per-row array in global memory with coalesced
 //              stores, nothing shared between warps; select_sampled_kernel
 //              then takes each row's exact top-k with one read of the row.
 //              Rows go in blocks whose array fits the workspace.
-//   streaming  other long rows, or a workspace too small for a score-array
+//   streaming  other head counts, or a workspace too small for a score-array
 //              block: scores that beat the row's threshold go to a candidate
 //              buffer in shared memory; a full buffer is cut to a superset
 //              of the row's top-k by a radix pass, which raises the
@@ -249,7 +249,7 @@ __device__ __forceinline__ void smem_inc(uint32_t* p) {
 // streaming prefill at 32 heads (four rows per item, the two warpgroups
 // taking the tiles in turn, candidate buffers shared by the eight warps).
 // STORE: prefill at 32 heads writing every score to a score array in global
-// memory (select_kernel takes the exact top-k afterwards).
+// memory (select_sampled_kernel takes the exact top-k afterwards).
 template <int HI, bool SPLIT, bool DENSE, bool TOK, bool STORE>
 __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
@@ -1443,7 +1443,7 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
         // decode: the two warpgroups take the tiles in turn (each accumulator
         // buffer belongs to one warpgroup) and each covers every query row of
         // its tile, TPW_MAX rows per pass; every score goes to the row's
-        // score array, and select_kernel takes the exact top-k afterwards
+        // score array, and select_sampled_kernel takes the exact top-k afterwards
         const uint32_t ac0 = ac;
         const int nt = it.t1 - it.t0;
         for (int tt = (wg - static_cast<int>(ac0 & 1u) + 2) & 1; tt < nt; tt += 2) {
@@ -1726,7 +1726,7 @@ __global__ void __launch_bounds__(STORE ? kStoreThreads : kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Parameters of select_kernel (split and score-array modes, step 2). Score
+// Parameters of select_sampled_kernel (split and score-array modes, step 2). Score
 // row i belongs to sequence i / block_rows, query row row_base + i % block_rows
 // of that sequence.
 struct SelectParams {
@@ -1740,327 +1740,16 @@ struct SelectParams {
   float* out_scores;
 };
 
-constexpr int kSelThreads = 1024;
-constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelShift = 20;                  // first radix digit: key bits 31..20
-constexpr int kSelBins = 1 << (32 - kSelShift);
-constexpr int kSelCand = 8192;                 // first-digit bin entries held in shared memory
-constexpr int kSelTies = 1024;                 // equal keys ranked by index in shared memory
-constexpr int kSelBmBits = 1 << 18;            // rows up to this many keys mark their selection in a bitmap
-
-// shared memory of select_kernel (dynamic)
-struct SelSmem {
-  uint32_t hist[kSelBins];
-  uint32_t bm[kSelBmBits / 32];  // selected positions of the row
-  uint32_t cand_key[kSelCand], cand_idx[kSelCand];
-  uint32_t tie[kSelTies];
-  uint32_t hist3[768];
-  uint32_t red[2 * kSelWarps];
-  uint32_t wsum[kSelWarps];
-  uint32_t n_cand, bin, above, thr_idx;
-};
-
-// Every entry of the row, a warp-uniform number of times per warp: warp w
-// takes 128-entry segments (lane l entries 4l..4l+3, one bitmap word per 8
-// lanes), four segments in flight. f(k4, e0) gets the lane's four keys.
-template <typename F>
-__device__ __forceinline__ void sel_each(const uint32_t* keys, int n, int w, int lane, F f) {
-  constexpr int U = 4;
-  for (int s0 = w * 128; s0 < n; s0 += U * kSelThreads * 4) {
-    uint4 kv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int e0 = s0 + u * kSelThreads * 4 + 4 * lane;
-      kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) f(kv[u], s0 + u * kSelThreads * 4 + 4 * lane);
-  }
-}
-
-// Top-down scan of a histogram of nbins (a multiple of kSelThreads or at most
-// kSelThreads) bins: the bin holding the k-th largest entry and the number of
-// entries in higher bins, left in S.bin / S.above. All threads call it.
-__device__ __forceinline__ void sel_top_scan(SelSmem& S, const uint32_t* hist, int nbins, uint32_t k, int tid) {
-  const int lane = tid & 31, w = tid >> 5;
-  const int per = nbins >= kSelThreads ? nbins / kSelThreads : 1;
-  uint32_t c[4] = {0, 0, 0, 0}, sum = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = per * tid + i;
-    if (i < per && j < nbins) c[i] = hist[nbins - 1 - j];
-    sum += c[i];
-  }
-  uint32_t incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) S.wsum[w] = incl;
-  __syncthreads();
-  uint32_t run = incl - sum;
-  for (int w2 = 0; w2 < w; ++w2) run += S.wsum[w2];
-  if (run < k && run + sum >= k) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (run + c[i] >= k) {
-        S.bin = static_cast<uint32_t>(nbins - 1 - (per * tid + i));
-        S.above = run;
-        break;
-      }
-      run += c[i];
-    }
-  }
-  __syncthreads();
-}
-
-// Split mode (decode) and score-array mode (prefill), step 2: the exact top-k
-// of one row's dense score array (written by the scoring kernel for keys
-// 0..pos). One CTA of 1024 threads per row; scores are read from global
-// memory (decode: they stay in L2; prefill: the first pass reads them from
-// HBM, the second finds most of them in L2).
-//  1. histogram of the top 12 key bits: the bin B holding the k-th best key
-//     splits the row into entries sure to be selected (higher bins),
-//     candidates (bin B) and the rest;
-//  2. one pass marks the sure entries in a bitmap of the row's positions and
-//     stages the candidates (key, index) in shared memory;
-//  3. two more digits (bits 19..8, 7..0) over the candidates give the exact
-//     k-th key; among equal keys the lower indices win, ranked by counting;
-//  4. the bitmap is written out as the ascending list of selected positions.
-// Rows too long for the bitmap, or whose bin B is too crowded to stage, take
-// the exact radix selection over the whole row instead (dense_select).
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
-  extern __shared__ __align__(16) uint8_t sel_raw[];
-  SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
-  const int srow = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int seq = srow / p.block_rows;
-  const int r_in = p.row_base + (srow - seq * p.block_rows);
-  const int row = seq * p.q_per_seq + r_in;
-  const int len = p.seq_lens ? p.seq_lens[seq] : p.prefix_len + p.q_per_seq;
-  const int pos = len - p.q_per_seq + r_in;
-  const int n = min(pos + 1, static_cast<int>(p.score_stride));  // keys 0..pos (with a score slot)
-  const uint32_t* keys = p.scores + static_cast<int64_t>(srow) * p.score_stride;
-  int32_t* o = p.out_idx + static_cast<size_t>(row) * p.topk;
-  float* os = p.out_scores ? p.out_scores + static_cast<size_t>(row) * p.topk : nullptr;
-  const int k = p.topk;
-  if (n <= k) {
-    // every key is selected: 0..n-1 in order, then -1
-    for (int e = tid; e < k; e += kSelThreads) {
-      o[e] = e < n ? e : -1;
-      if (os) os[e] = e < n ? key_score(keys[e]) : 0.0f;
-    }
-    return;
-  }
-  auto sync = []() { __syncthreads(); };
-  const bool use_bm = n <= kSelBmBits;
-  // 1. first-digit histogram
-  for (int b = tid; b < kSelBins; b += kSelThreads) S.hist[b] = 0;
-  if (use_bm)
-    for (int b = tid; b < (n + 31) / 32; b += kSelThreads) S.bm[b] = 0;
-  if (tid == 0) S.n_cand = 0;
-  __syncthreads();
-  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
-    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (e0 + q < n) atomicAdd(&S.hist[kk[q] >> kSelShift], 1u);
-  });
-  __syncthreads();
-  sel_top_scan(S, S.hist, kSelBins, static_cast<uint32_t>(k), tid);
-  const uint32_t b1 = S.bin;
-  const uint32_t n_b1 = S.hist[b1];
-  const int r1 = k - static_cast<int>(S.above);  // rank (1-based) of the k-th best inside bin b1
-  int r = r1;
-  uint32_t tk = 0, ti = 0xFFFFFFFFu;
-  bool staged = use_bm && n_b1 <= static_cast<uint32_t>(kSelCand);
-  if (staged) {
-    // 2. sure entries into the bitmap (each word belongs to one warp segment),
-    //    candidates into shared memory
-    sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
-      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-      uint32_t bits = 0, nc = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t b = kk[q] >> kSelShift;
-        if (e0 + q < n) {
-          bits |= (b > b1 ? 1u : 0u) << ((e0 + q) & 31);
-          nc += b == b1;
-        }
-      }
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
-      if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
-      if (__ballot_sync(0xFFFFFFFFu, nc != 0)) {
-        uint32_t incl = nc;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
-          if (lane >= o2) incl += t2;
-        }
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&S.n_cand, incl);
-        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - nc;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (e0 + q < n && (kk[q] >> kSelShift) == b1) {
-            S.cand_key[base] = kk[q];
-            S.cand_idx[base] = static_cast<uint32_t>(e0 + q);
-            ++base;
-          }
-      }
-    });
-    __syncthreads();
-    // 3. exact k-th key among the candidates: digits 19..8, then 7..0
-    const int nc = static_cast<int>(n_b1);
-    uint32_t prefix = b1 << kSelShift;
-    for (int d = 0; d < 2; ++d) {
-      const int shift = d == 0 ? 8 : 0;
-      const int nb = d == 0 ? 4096 : 256;
-      const uint32_t pmask = d == 0 ? 0xFFF00000u : 0xFFFFFF00u;
-      for (int b = tid; b < nb; b += kSelThreads) S.hist[b] = 0;
-      __syncthreads();
-      for (int e = tid; e < nc; e += kSelThreads) {
-        const uint32_t kk = S.cand_key[e];
-        if ((kk & pmask) == prefix) atomicAdd(&S.hist[(kk >> shift) & (nb - 1)], 1u);
-      }
-      __syncthreads();
-      sel_top_scan(S, S.hist, nb, static_cast<uint32_t>(r), tid);
-      prefix |= S.bin << shift;
-      r -= static_cast<int>(S.above);
-    }
-    tk = prefix;
-    const int m = static_cast<int>(S.hist[tk & 255u]);  // entries with key == tk; the r lowest indices win
-    if (r < m) {
-      if (m <= kSelTies) {
-        if (tid == 0) S.n_cand = 0;
-        __syncthreads();
-        for (int e0 = 0; e0 < nc; e0 += kSelThreads) {
-          const int e = e0 + tid;
-          const bool eq = e < nc && S.cand_key[e] == tk;
-          const uint32_t mb = __ballot_sync(0xFFFFFFFFu, eq);
-          uint32_t base = 0;
-          if (mb && lane == 0) base = atomicAdd(&S.n_cand, static_cast<uint32_t>(__popc(mb)));
-          base = __shfl_sync(0xFFFFFFFFu, base, 0);
-          if (eq) S.tie[base + __popc(mb & ((1u << lane) - 1u))] = S.cand_idx[e];
-        }
-        __syncthreads();
-        if (tid < m) {
-          const uint32_t mine = S.tie[tid];
-          int below = 0;
-          for (int j = 0; j < m; ++j) below += S.tie[j] < mine;
-          if (below == r - 1) S.thr_idx = mine;
-        }
-        __syncthreads();
-        ti = S.thr_idx;
-      } else {
-        // many equal keys: exact selection over all candidates (r1 < nc)
-        for (int e = nc + tid; e < (nc + 3) / 4 * 4; e += kSelThreads) S.cand_key[e] = 0;  // 16-byte tail
-        __syncthreads();
-        dense_select<kSelThreads>(S.cand_key, S.cand_idx, nc, r1, tid, S.hist3, S.red, sync, tk, ti);
-      }
-    }
-    for (int e = tid; e < nc; e += kSelThreads) {
-      const uint32_t i = S.cand_idx[e];
-      if (selected(S.cand_key[e], i, tk, ti)) atomicOr(&S.bm[i >> 5], 1u << (i & 31));
-    }
-  } else {
-    // the whole row: exact radix selection from global memory
-    dense_select<kSelThreads>(keys, nullptr, n, k, tid, S.hist3, S.red, sync, tk, ti);
-    if (use_bm)
-      sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
-        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-        uint32_t bits = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti)) bits |= 1u << ((e0 + q) & 31);
-        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
-        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
-        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
-        if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
-      });
-  }
-  __syncthreads();
-  if (use_bm) {
-    // 4. ascending positions: thread t owns a run of bitmap words
-    const int nw = (n + 31) / 32;
-    const int per = (nw + kSelThreads - 1) / kSelThreads;
-    const int w0 = tid * per, w1 = min(nw, w0 + per);
-    uint32_t cnt = 0;
-    for (int i = w0; i < w1; ++i) cnt += __popc(S.bm[i]);
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-      const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
-      if (lane >= o2) incl += t2;
-    }
-    if (lane == 31) S.wsum[w] = incl;
-    __syncthreads();
-    uint32_t at = incl - cnt;
-    for (int w2 = 0; w2 < w; ++w2) at += S.wsum[w2];
-    for (int i = w0; i < w1; ++i) {
-      uint32_t bits = S.bm[i];
-      while (bits) {
-        const int e = i * 32 + __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (at < static_cast<uint32_t>(k)) {
-          o[at] = e;
-          if (os) os[at] = key_score(keys[e]);
-        }
-        ++at;
-      }
-    }
-    return;
-  }
-  // rows longer than the bitmap: selected entries in a fixed order (warp w
-  // takes the 128-entry segments w, w + 32, ...): count, then write
-  int mine = 0;
-  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
-    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) mine += e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti);
-  });
-  mine = __reduce_add_sync(0xFFFFFFFFu, mine);
-  if (lane == 0) S.wsum[w] = mine;
-  __syncthreads();
-  int base = 0;
-  for (int w2 = 0; w2 < w; ++w2) base += static_cast<int>(S.wsum[w2]);
-  sel_each(keys, n, w, lane, [&](uint4 k4, int e0) {
-    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-    bool t4[4];
-    int c = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      t4[q] = e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti);
-      c += t4[q];
-    }
-    int incl = c;
-#pragma unroll
-    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-      const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
-      if (lane >= o2) incl += t2;
-    }
-    int q0 = base + incl - c;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (t4[q]) {
-        if (q0 < k) {
-          o[q0] = e0 + q;
-          if (os) os[q0] = key_score(kk[q]);
-        }
-        ++q0;
-      }
-    base += __shfl_sync(0xFFFFFFFFu, incl, 31);
-  });
-}
+// rows up to this many keys mark their selection in a bitmap (longer rows sort it)
+constexpr int kSelBmBits = 1 << 18;
 
 // ---------------------------------------------------------------------------
-// Step 2 of the split and score-array modes for rows of at most kSelBmBits
-// keys: the same exact top-k as select_kernel with one full read of the row.
-//  1. a sample (32 runs of 128 keys spread over the row) gives a key t_lo
-//     that about 1.25 k + 4 sqrt(k) keys of the row reach, were the sample
-//     representative (one 4096-bin histogram of the sample's key range);
+// Step 2 of the split and score-array modes: each row's exact top-k with one
+// full read of the row.
+//  1. a sample (32 to 96 runs of 128 keys spread over the row, more for longer
+//     rows) gives a key t_lo that about e + 3 sqrt(e) of the sampled keys
+//     reach, e being the number expected among the row's top k (one 4096-bin
+//     histogram of the sample's key range);
 //  2. one pass stages every key >= t_lo (and its position) in shared memory,
 //     one atomic per warp and 128 keys;
 //  3. when between k and kSsCand keys were staged, they hold the row's top-k:
@@ -2069,18 +1758,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
 //     otherwise (the sample misjudged the row) the exact radix selection runs
 //     over the whole row in global memory;
 //  4. the selected positions are marked in a bitmap of the row and written
-//     out in ascending order.
+//     out in ascending order (rows longer than the bitmap: the k positions are
+//     collected in shared memory and sorted).
 // 512 threads and ~96 KB of shared memory: two rows per SM at a time, so one
 // row's pass over HBM overlaps the other's selection.
 constexpr int kSsThreads = 512;
 constexpr int kSsWarps = kSsThreads / 32;
 constexpr int kSsCand = 6144;       // staged candidates
-constexpr int kSsRuns = 32;         // sampled runs of 128 keys
-constexpr int kSsSample = kSsRuns * 128;
+constexpr int kSsMinRuns = 32, kSsMaxRuns = 96;  // sampled runs of 128 keys
+constexpr int kSsSampleMax = kSsMaxRuns * 128;   // held in the two candidate arrays
 constexpr int kSsBins = 4096;       // 12-bit digits
 constexpr int kSsPass = 4 * kSsThreads * 4;  // keys per iteration of the staging pass
 constexpr int kSsPrefetchAhead = 2;          // iterations of the row prefetched into L2 ahead of the pass
-static_assert(kSsSample <= kSsCand, "the sample is held in the candidate space");
+static_assert(kSsSampleMax <= 2 * kSsCand, "the sample is held in the candidate space");
 
 struct SsSmem {
   uint32_t bm[kSelBmBits / 32];  // selected positions of the row
@@ -2088,7 +1778,7 @@ struct SsSmem {
   uint32_t hist[kSsBins];        // digit histogram; tie list; dense_select's 3 x 256 words
   uint32_t red[2 * kSsWarps];
   uint32_t wsum[kSsWarps];
-  uint32_t n_cand, bin, above, thr_idx;
+  uint32_t n_cand, bin, above, thr_idx, n_sel;
 };
 
 // Block-wide minimum and maximum of v over all threads (every thread gets them).
@@ -2195,27 +1885,35 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   };
 #pragma unroll
   for (int it = 0; it < kSsPrefetchAhead; ++it) prefetch_pass(it);
+  const bool use_bm = n <= kSelBmBits;  // else the selected positions are sorted in shared memory
   const int nw = (n + 31) / 32;
-  for (int b = tid; b < nw; b += kSsThreads) S.bm[b] = 0;
-  if (tid == 0) S.n_cand = 0;
+  if (use_bm)
+    for (int b = tid; b < nw; b += kSsThreads) S.bm[b] = 0;
+  if (tid == 0) {
+    S.n_cand = 0;
+    S.n_sel = 0;
+  }
   // 1. a key that about 1.25 k + 4 sqrt(k) keys reach, from the sample
   uint32_t t_lo = 0;
   if (n > kSsCand) {
+    const int runs = min(kSsMaxRuns, max(kSsMinRuns, n / 2048));
+    const int n_sample = runs * 128;
+    uint32_t* sample = S.cand_key;  // cand_key and cand_idx, one after the other
     uint32_t lo = 0xFFFFFFFFu, hi = 0;
-    for (int e = tid; e < kSsSample / 4; e += kSsThreads) {
+    for (int e = tid; e < n_sample / 4; e += kSsThreads) {
       const int run = e >> 5, u = e & 31;
-      const int start = static_cast<int>(static_cast<int64_t>(n - 128) * run / (kSsRuns - 1)) & ~3;
+      const int start = static_cast<int>(static_cast<int64_t>(n - 128) * run / (runs - 1)) & ~3;
       const uint4 v = *reinterpret_cast<const uint4*>(keys + start + 4 * u);
-      *reinterpret_cast<uint4*>(&S.cand_key[4 * e]) = v;
+      *reinterpret_cast<uint4*>(&sample[4 * e]) = v;
       lo = min(min(lo, min(v.x, v.y)), min(v.z, v.w));
       hi = max(max(hi, max(v.x, v.y)), max(v.z, v.w));
     }
     ss_minmax(S, lo, hi, tid);  // also orders the sample's stores before the histogram
-    const float expect = static_cast<float>(k) * kSsSample / static_cast<float>(n);
-    const int r = static_cast<int>(ceilf(1.25f * expect + 4.0f * sqrtf(expect) + 16.0f));
-    if (r < kSsSample) {
+    const float expect = static_cast<float>(k) * static_cast<float>(n_sample) / static_cast<float>(n);
+    const int r = static_cast<int>(ceilf(1.1f * expect + 3.0f * sqrtf(expect) + 3.0f));
+    if (r < n_sample) {
       const int shift = ss_shift(lo, hi);
-      ss_digit(S, S.cand_key, kSsSample, lo, hi, shift, static_cast<uint32_t>(r), tid);
+      ss_digit(S, sample, n_sample, lo, hi, shift, static_cast<uint32_t>(r), tid);
       t_lo = lo + (S.bin << shift);  // the r-th largest sampled key's bin, from its lower edge
     }
   }
@@ -2309,29 +2007,85 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
         }
       }
     }
+    __syncthreads();  // the selection's scratch (S.hist) is free
     for (int e = tid; e < nc; e += kSsThreads) {
       const uint32_t i = S.cand_idx[e];
-      if (selected(S.cand_key[e], i, tk, ti)) atomicOr(&S.bm[i >> 5], 1u << (i & 31));
+      if (!selected(S.cand_key[e], i, tk, ti)) continue;
+      if (use_bm) {
+        atomicOr(&S.bm[i >> 5], 1u << (i & 31));
+      } else {
+        const uint32_t at = atomicAdd(&S.n_sel, 1u);
+        if (at < static_cast<uint32_t>(kSsBins)) S.hist[at] = i;
+      }
     }
   }
   if (exact_row) {
     // 3'. the whole row from global memory; bitmap word = 8 lanes x 4 keys
     dense_select<kSsThreads>(keys, nullptr, n, k, tid, S.hist, S.red, sync, tk, ti);
+    __syncthreads();  // the selection's scratch (S.hist) is free
     for (int s0 = w * 128; s0 < n; s0 += kSsThreads * 4) {
       const int e0 = s0 + 4 * lane;
       const uint4 k4 = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
       const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-      uint32_t bits = 0;
+      uint32_t take = 0;  // bit q: entry e0 + q is selected
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti)) bits |= 1u << ((e0 + q) & 31);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
-      bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
-      if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
+        if (e0 + q < n && selected(kk[q], static_cast<uint32_t>(e0 + q), tk, ti)) take |= 1u << q;
+      if (use_bm) {
+        uint32_t bits = take << (e0 & 31);  // bitmap word = 8 lanes x 4 keys
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+        bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 4);
+        if ((lane & 7) == 0 && e0 < n) S.bm[e0 >> 5] = bits;
+      } else {
+        const uint32_t c = __popc(take);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += t2;
+        }
+        uint32_t base = 0;
+        if (lane == 31 && incl) base = atomicAdd(&S.n_sel, incl);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if ((take >> q) & 1u) {
+            if (base < static_cast<uint32_t>(kSsBins)) S.hist[base] = static_cast<uint32_t>(e0 + q);
+            ++base;
+          }
+      }
     }
   }
   __syncthreads();
+  if (!use_bm) {
+    // 4'. ascending positions: bitonic sort of the k collected positions
+    // (padded with the largest value to a power of two)
+    const int m = min(static_cast<int>(S.n_sel), kSsBins);
+    int P2 = 1;
+    while (P2 < m) P2 <<= 1;
+    for (int e = m + tid; e < P2; e += kSsThreads) S.hist[e] = 0xFFFFFFFFu;
+    __syncthreads();
+    for (int size = 2; size <= P2; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P2 / 2; i += kSsThreads) {
+          const int a = 2 * i - (i & (stride - 1));
+          const int b2 = a + stride;
+          const bool up = (a & size) == 0;
+          const uint32_t va = S.hist[a], vb = S.hist[b2];
+          if ((va > vb) == up) {
+            S.hist[a] = vb;
+            S.hist[b2] = va;
+          }
+        }
+        __syncthreads();
+      }
+    for (int e = tid; e < k; e += kSsThreads) {
+      o[e] = e < m ? static_cast<int32_t>(S.hist[e]) : -1;
+      if (os) os[e] = e < m ? key_score(keys[S.hist[e]]) : 0.0f;
+    }
+    return;
+  }
   // 4. ascending positions: thread t owns a run of bitmap words
   const int per = (nw + kSsThreads - 1) / kSsThreads;
   const int w0 = tid * per, w1 = min(nw, w0 + per);
@@ -2468,9 +2222,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
 bool set_select_attr() {
   static bool done = false;
   if (!done) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(SelSmem))) != cudaSuccess ||
-        cudaFuncSetAttribute(select_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(select_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(SsSmem))) != cudaSuccess)
       return false;
     done = true;
@@ -2478,12 +2230,10 @@ bool set_select_attr() {
   return true;
 }
 
-// step 2 of the split and score-array modes over n_rows score rows of at most
-// max_keys keys each
-int launch_select(const SelectParams& sp, int n_rows, int32_t max_keys, cudaStream_t stream) {
+// step 2 of the split and score-array modes over n_rows score rows
+int launch_select(const SelectParams& sp, int n_rows, cudaStream_t stream) {
   if (!set_select_attr()) return SMLA_ERR_CUDA;
-  if (max_keys <= kSelBmBits) select_sampled_kernel<<<n_rows, kSsThreads, sizeof(SsSmem), stream>>>(sp);
-  else select_kernel<<<n_rows, kSelThreads, sizeof(SelSmem), stream>>>(sp);
+  select_sampled_kernel<<<n_rows, kSsThreads, sizeof(SsSmem), stream>>>(sp);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
@@ -2553,15 +2303,15 @@ int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len) {
 }
 
 // Score-array mode: prefill rows at 32 indexer heads longer than the dense
-// mode takes and short enough for select_kernel's bitmap. The rows go in
-// blocks (the same rows of every sequence) whose score array fits the space
-// given; the workspace size asks for blocks of up to kScoreArrayBudget bytes.
-constexpr size_t kScoreArrayBudget = size_t(4) << 30;
+// mode takes. The rows go in blocks (the same rows of every sequence) whose
+// score array fits the space given, all blocks of one call the same size
+// (so each spreads its work items evenly over the SMs); the workspace size asks
+// for blocks of up to kScoreArrayBudget bytes.
+constexpr size_t kScoreArrayBudget = size_t(16) << 30;
 constexpr int kMinStoreRows = 608;  // rows per block (per sequence) below which the streaming mode is used
 
 bool indexer_store_mode(int32_t q_per_seq, int32_t h_idx, int32_t topk, int32_t max_seq_len) {
-  return h_idx == 32 && !indexer_split_mode(q_per_seq, h_idx) && indexer_dense_tokens(h_idx, topk, max_seq_len) == 0 &&
-         max_seq_len <= kSelBmBits;
+  return h_idx == 32 && !indexer_split_mode(q_per_seq, h_idx) && indexer_dense_tokens(h_idx, topk, max_seq_len) == 0;
 }
 
 int64_t store_stride(int32_t max_seq_len) { return (static_cast<int64_t>(max_seq_len) + 31) / 32 * 32; }
@@ -2652,8 +2402,11 @@ int launch_indexer(const IndexerLaunch& L) {
     // score-array mode when the space given holds a large enough row block
     if (!dense && indexer_store_mode(L.q_per_seq, L.h_idx, L.topk, L.max_seq_len) && L.cand &&
         (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
-      const int32_t block = store_block_rows(L.n_seqs, L.q_per_seq, L.max_seq_len, L.cand_bytes);
+      int32_t block = store_block_rows(L.n_seqs, L.q_per_seq, L.max_seq_len, L.cand_bytes);
       if (block > 0 && block >= std::min(L.q_per_seq, kMinStoreRows)) {
+        // equal blocks: as few as fit, each a multiple of 4 rows
+        const int32_t n_blocks = (L.q_per_seq + block - 1) / block;
+        block = std::min(block, ((L.q_per_seq + n_blocks - 1) / n_blocks + 3) / 4 * 4);
         prm.scores = static_cast<uint32_t*>(L.cand);
         prm.score_stride = store_stride(L.max_seq_len);
         SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.prefix_len, L.q_per_seq, L.topk,
@@ -2667,7 +2420,7 @@ int launch_indexer(const IndexerLaunch& L) {
           if (rc != SMLA_OK) return rc;
           sp.row_base = r0;
           sp.block_rows = prm.block_rows;
-          const int rs = launch_select(sp, L.n_seqs * prm.block_rows, L.max_seq_len, L.stream);
+          const int rs = launch_select(sp, L.n_seqs * prm.block_rows, L.stream);
           if (rs != SMLA_OK) return rs;
         }
         return SMLA_OK;
@@ -2723,7 +2476,7 @@ int launch_indexer(const IndexerLaunch& L) {
   }
   SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, 0, L.q_per_seq, L.topk, 0, L.q_per_seq,
                   L.out_idx, L.out_scores};
-  return launch_select(sp, prm.n_rows, L.max_seq_len, L.stream);
+  return launch_select(sp, prm.n_rows, L.stream);
 }
 
 }  // namespace smla

@@ -107,30 +107,34 @@ def test_workspace_sizes(L):
     assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 1) == \
         256 + 16384 * 2048 * 4 + 16384 * 576 * 2 + r256(16384 * 4)
     assert L.smla_sparse_mla_prefill_workspace_size(0, 16384, 64, 32, 2048, 2) == 256 + 16384 * 2048 * 4
-    # longer rows at 32 indexer heads (up to 262144 keys): a score array, 4 bytes
-    # per key up to max_seq_len rounded up to 32, for a block of rows of every
-    # sequence: all rows while the array stays within 4 GiB
+    # longer rows at 32 indexer heads: a score array, 4 bytes per key up to
+    # max_seq_len rounded up to 32, for a block of rows of every sequence: all
+    # rows while the array stays within 16 GiB
     T, P = 8192, 20000
     stride = (P + T + 31) // 32 * 32
     scores = T * stride * 4
     assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 2) == 256 + T * 2048 * 4 + scores
     assert L.smla_sparse_mla_prefill_workspace_size(P, T, 64, 32, 2048, 1) == \
         256 + T * 2048 * 4 + r256((P + T) * 1152) + r256((P + T) * 4) + scores
-    # one call over 131072 new tokens: blocks of 8192 rows x 131072 keys (4 GiB)
+    # one call over 131072 new tokens: blocks of 32768 rows x 131072 keys (16 GiB)
     assert L.smla_sparse_mla_prefill_workspace_size(0, 131072, 64, 32, 2048, 2) == \
-        256 + 131072 * 2048 * 4 + 8192 * 131072 * 4
+        256 + 131072 * 2048 * 4 + 32768 * 131072 * 4
+    # 8192 tokens after a 1M prefix: 4260 rows of 1,056,768 keys fit in 16 GiB
+    stride1m = (1048576 + 8192 + 31) // 32 * 32
+    assert L.smla_sparse_mla_prefill_workspace_size(1048576, 8192, 64, 32, 2048, 2) == \
+        256 + 8192 * 2048 * 4 + ((16 << 30) // (stride1m * 4) // 4 * 4) * stride1m * 4
     # the indexer alone: status word + the score array (two sequences: the same
     # rows of both in one block)
     assert L.smla_indexer_topk_workspace_size(1, 16384, 16384, 32, 2048) == 256
     assert L.smla_indexer_topk_workspace_size(1, P + T, T, 32, 2048) == 256 + scores
     assert L.smla_indexer_topk_workspace_size(2, 30000, 4096, 32, 2048) == 256 + 2 * 4096 * 30016 * 4
-    # other head counts, or rows beyond 262144 keys: candidate buffers of rows
-    # whose final selection is deferred: 4 query rows per work item (at 16 or 32
-    # heads) share 16384 entries, so 4096 (key, index) pairs per row, plus one
-    # count per row
+    # other head counts: candidate buffers of rows whose final selection is
+    # deferred: 4 query rows per work item (at 16 heads) share 16384 entries, so
+    # 4096 (key, index) pairs per row, plus one count per row
     cand = T * 4096 * 8 + T * 4
     assert L.smla_indexer_topk_workspace_size(1, P + T, T, 16, 2048) == 256 + cand
-    assert L.smla_indexer_topk_workspace_size(1, 300000 + T, T, 32, 2048) == 256 + cand
+    stride3 = (300000 + T + 31) // 32 * 32
+    assert L.smla_indexer_topk_workspace_size(1, 300000 + T, T, 32, 2048) == 256 + T * stride3 * 4
     # decode: a score per (row, key) up to max_seq_len, the index list, then
     # room for the fp32 partial outputs (and lse) of rows split into up to 4 parts
     rows, k = 128, 2048

@@ -277,6 +277,58 @@ def test_indexer_score_array_row_blocks(case):
     compare_idx(_host(gidx)[rows], ridx)
 
 
+@pytest.mark.parametrize("keys", ["random", "constant"])
+def test_indexer_rows_beyond_the_bitmap(keys):
+    """Rows of more than 262,144 keys in the score-array mode: the selection
+    kernel collects the k positions in shared memory and sorts them instead of
+    marking a bitmap of the row. Random keys take the sampled path, all-equal
+    keys (every score tied) the exact fallback over the whole row; index sets
+    exact against the oracle, returned in ascending order."""
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=400, prefix_len=270000, shuffled=True)
+    prob = wl.make(spec, "cpu")
+    if keys == "constant":
+        k = prob.cache.k_idx
+        row = k.view(-1, spec.d_idx)[0].clone()
+        k.view(-1, spec.d_idx)[:] = row
+    dev = prob.to("cuda")
+    L = spec.prefix_len + spec.n_tokens
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    gidx, gsc, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
+                                      spec.topk, want_scores=True)
+    assert smla.read_status(ws)[0] == 0
+    g = _host(gidx)
+    assert (np.diff(g, axis=1) > 0).all(), "indices not ascending"
+    rows = np.array([0, 1, 133, 398, 399], dtype=np.int64)
+    o = oracle.Oracle(prob)
+    ridx, rsc, *_ = o.rows(rows, attend=False)
+    compare_idx(g[rows], ridx)
+    if keys == "constant":
+        assert (g == np.arange(spec.topk)[None, :]).all()
+    gs = _host(gsc)
+    for r in range(len(rows)):
+        full = o.scores(int(rows[r]))
+        assert np.array_equal(gs[rows[r]], full[g[rows[r]]])
+
+
+def test_decode_rows_beyond_the_bitmap():
+    """Decode sequences of 270K-300K keys (split mode, the selection's sorted
+    output): every row's index set and the attention match the oracle."""
+    spec = wl.scaled(wl.SPECS["decode"], n_seqs=2, len_min=270000, len_max=300000, seed=29)
+    prob = wl.make(spec, "cpu")
+    dev = prob.to("cuda")
+    max_len = int(dev.seq_lens.max())
+    out, lse, gidx, ws = smla.sparse_mla_decode(dev.cache, dev.page_table, dev.seq_lens, max_len, spec.q_per_seq,
+                                                dev.q, dev.q_idx, dev.w, spec.topk, spec.sm_scale,
+                                                out_idx=torch.empty((spec.n_seqs * spec.q_per_seq, spec.topk),
+                                                                    dtype=torch.int32, device="cuda"))
+    assert smla.read_status(ws)[0] == 0
+    rows = np.arange(spec.n_seqs * spec.q_per_seq)
+    ridx, _, rout, rlse, _, bad = oracle.Oracle(prob).rows(rows)
+    assert not bad.any()
+    compare_idx(_host(gidx), ridx)
+    compare_out(_host(out.float()), rout, _host(lse), rlse, spec.kv_dtype)
+
+
 @pytest.mark.parametrize("mode", ["constant", "binary"])
 def test_decode_indexer_heavy_ties(mode):
     """Decode shape (split mode) with ties everywhere, rows from 2.5K to 20K keys:
