@@ -2304,9 +2304,9 @@ int indexer_dense_tokens(int32_t h_idx, int32_t topk, int32_t max_seq_len) {
 
 // Score-array mode: prefill rows at 32 indexer heads longer than the dense
 // mode takes. The rows go in blocks (the same rows of every sequence) whose
-// score array fits the space given, all blocks of one call the same size
-// (so each spreads its work items evenly over the SMs); the workspace size asks
-// for blocks of up to kScoreArrayBudget bytes.
+// score array fits the space given, each a whole number of waves of work
+// items over the SMs when it can be; the workspace size asks for blocks of up
+// to kScoreArrayBudget bytes.
 constexpr size_t kScoreArrayBudget = size_t(16) << 30;
 constexpr int kMinStoreRows = 608;  // rows per block (per sequence) below which the streaming mode is used
 
@@ -2404,9 +2404,17 @@ int launch_indexer(const IndexerLaunch& L) {
         (reinterpret_cast<uintptr_t>(L.cand) & 15u) == 0) {
       int32_t block = store_block_rows(L.n_seqs, L.q_per_seq, L.max_seq_len, L.cand_bytes);
       if (block > 0 && block >= std::min(L.q_per_seq, kMinStoreRows)) {
-        // equal blocks: as few as fit, each a multiple of 4 rows
-        const int32_t n_blocks = (L.q_per_seq + block - 1) / block;
-        block = std::min(block, ((L.q_per_seq + n_blocks - 1) / n_blocks + 3) / 4 * 4);
+        if (block < L.q_per_seq) {
+          // several blocks: each a whole number of waves (two items of 4 rows
+          // per SM) when that fits, else equal blocks of a multiple of 4 rows
+          const int32_t wave = 8 * num_sms();
+          if (block >= wave) {
+            block = block / wave * wave;
+          } else {
+            const int32_t n_blocks = (L.q_per_seq + block - 1) / block;
+            block = std::min(block, ((L.q_per_seq + n_blocks - 1) / n_blocks + 3) / 4 * 4);
+          }
+        }
         prm.scores = static_cast<uint32_t*>(L.cand);
         prm.score_stride = store_stride(L.max_seq_len);
         SelectParams sp{prm.scores, prm.score_stride, L.seq_lens, L.prefix_len, L.q_per_seq, L.topk,

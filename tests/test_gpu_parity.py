@@ -246,9 +246,10 @@ def test_indexer_heavy_ties(mode, sel):
 @pytest.mark.parametrize("case", ["one_seq", "two_seqs"])
 def test_indexer_score_array_row_blocks(case):
     """The score-array mode in several row blocks (a workspace holding one
-    block of 700 rows, or 608 rows of each of two sequences): the rows of every
-    block match the oracle, the rows at block boundaries included, and the
-    index sets equal those of a call with the full workspace (one block)."""
+    block of 700 rows, or 608 rows of each of two sequences; blocks smaller
+    than a wave of work items are made equal): the rows of every block match
+    the oracle, the rows at block boundaries included, and the index sets
+    equal those of a call with the full workspace (one block)."""
     if case == "one_seq":
         spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=2000, prefix_len=18000, shuffled=True)
         prob = wl.make(spec, "cpu")
@@ -256,7 +257,8 @@ def test_indexer_score_array_row_blocks(case):
         n_seqs, qps, block = 1, spec.n_tokens, 700
         max_len = spec.prefix_len + spec.n_tokens
         seq_lens = torch.tensor([max_len], dtype=torch.int32, device="cuda")
-        rows = sorted({0, 1, 699, 700, 701, 1399, 1400, 1999} | set(range(3, 2000, 97)))
+        # room for 700 rows: three equal blocks of 668, 668 and 664 rows
+        rows = sorted({0, 1, 667, 668, 669, 1335, 1336, 1999} | set(range(3, 2000, 97)))
     else:
         spec = wl.scaled(wl.SPECS["decode"], n_seqs=2, q_per_seq=900, len_min=18000, len_max=26000, seed=7)
         prob = wl.make(spec, "cpu")
@@ -264,7 +266,8 @@ def test_indexer_score_array_row_blocks(case):
         n_seqs, qps, block = 2, 900, 608
         seq_lens = dev.seq_lens
         max_len = int(seq_lens.max())
-        rows = sorted({0, 607, 608, 899, 900, 1507, 1508, 1799} | set(range(5, 1800, 89)))
+        # room for 608 rows of each sequence: two equal blocks of 452 and 448 rows
+        rows = sorted({0, 451, 452, 899, 900, 1351, 1352, 1799} | set(range(5, 1800, 89)))
     stride = (max_len + 31) // 32 * 32
     ws = smla.workspace(256 + n_seqs * block * stride * 4, "cuda")
     gidx, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, max_len, qps, dev.q_idx, dev.w, spec.topk,
