@@ -212,16 +212,28 @@ class PrefillStep:
         return smla.read_status_chunks(self.ws, len(self.chunks))[0]
 
     def launches(self):
-        """Kernels one step launches: per chunk the indexer, the selection
-        kernel of rows longer than 16,384 keys (over the score array up to
-        262,144 keys, over deferred candidate buffers beyond; one row block per
-        chunk at these sizes), the f16 copy of the rows (BF16 and per-token FP8
-        caches) and the attention."""
+        """Kernels one step launches: per chunk the indexer and, for rows longer
+        than 16,384 keys, the selection kernel once per row block of the score
+        array (the library's rule: blocks of the rows that 16 GiB holds, in
+        whole waves of 8 rows per SM when several are needed), the f16 copy of
+        the rows (BF16 and per-token FP8 caches) and the attention."""
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
         n = 0
         for P, T in self.chunks:
-            n += 2 + (self.spec.kv_dtype in ("bf16", "fp8"))  # the f16 copy: BF16 and per-token FP8 caches
+            n += 2 + (self.spec.kv_dtype in ("bf16", "fp8"))  # indexer, attention, the f16 copy
             if P + T > 16384:
-                n += 1
+                stride = (P + T + 31) // 32 * 32
+                fit = max(min(T, 608), min(T, (16 << 30) // (stride * 4) // 4 * 4))
+                block = fit
+                if fit < T:
+                    wave = 8 * sms
+                    if fit >= wave:
+                        block = fit // wave * wave
+                    else:
+                        nb = -(-T // fit)
+                        block = min(fit, (-(-T // nb) + 3) // 4 * 4)
+                blocks = -(-T // block)
+                n += 2 * blocks - 1  # one indexer per block (one counted above), one selection per block
         return n
 
 
