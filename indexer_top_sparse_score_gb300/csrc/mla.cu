@@ -453,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) mbar_arrive(&M.q_full);
       }
       // keys three blocks ahead and page ids two ahead (each consumed a block
-      // after it was requested); the pool rows of the next block are
-      // prefetched into L2 while this block is copied
+      // after it was requested); the rows of the next block (pool or f16
+      // copy) are prefetched into L2 while this block is copied
       const int key0 = fetch_key(0);
       int key1 = fetch_key(1), key2 = fetch_key(2);
       int loc = locate(key0, fetch_page(key0));
@@ -465,7 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!TILE && p.fmt == kFmtTokenFp8 && loc >= 0) ks = __ldg((p.shadow ? p.shadow_scale : p.kv_scale) + loc);
         const int key3 = fetch_key(b + 3);
         const int loc1 = locate(key1, pg1);
-        if (!p.shadow && loc1 >= 0) prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
+        if (loc1 >= 0) {  // the f16 copy of a long sequence is larger than L2
+          if (p.shadow) prefetch_l2_lines(p.shadow + static_cast<int64_t>(loc1) * kDqk, 2 * kDqk);
+          else prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
+        }
         const int pg2 = fetch_page(key2);
         const uint32_t ph_e = (g & 1) ^ 1;  // slot of block g free: PV of block g-1 done
         auto meta = [&]() {
