@@ -82,6 +82,7 @@ struct MlaParams {
   const uint16_t* shadow;  // f16 rows by logical position, or null
   const float* shadow_scale;  // per-token FP8 scales by logical position (FP8 cache with a shadow)
   int32_t shadow_rows;
+  int32_t shadow_prefetch;  // the f16 copy is larger than half of L2: prefetch each next block's rows
   // split rows: each row's blocks are cut into n_parts items of part_blocks
   // blocks; each item writes a normalised fp32 partial output and its lse
   int32_t n_parts, part_blocks;
@@ -465,9 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!TILE && p.fmt == kFmtTokenFp8 && loc >= 0) ks = __ldg((p.shadow ? p.shadow_scale : p.kv_scale) + loc);
         const int key3 = fetch_key(b + 3);
         const int loc1 = locate(key1, pg1);
-        if (loc1 >= 0) {  // the f16 copy of a long sequence is larger than L2
-          if (p.shadow) prefetch_l2_lines(p.shadow + static_cast<int64_t>(loc1) * kDqk, 2 * kDqk);
-          else prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
+        if (loc1 >= 0) {
+          if (p.shadow) {
+            if (p.shadow_prefetch) prefetch_l2_lines(p.shadow + static_cast<int64_t>(loc1) * kDqk, 2 * kDqk);
+          } else {
+            prefetch_l2_lines(p.kv + static_cast<int64_t>(loc1) * row_bytes, row_bytes);
+          }
         }
         const int pg2 = fetch_page(key2);
         const uint32_t ph_e = (g & 1) ^ 1;  // slot of block g free: PV of block g-1 done
@@ -1085,6 +1089,8 @@ int launch_mla(const MlaLaunch& L) {
   prm.status = L.status;
   prm.shadow = static_cast<const uint16_t*>(L.shadow);
   prm.shadow_rows = L.shadow_rows;
+  // a copy that fits in half of L2 stays there; a larger one is prefetched a block ahead
+  prm.shadow_prefetch = static_cast<size_t>(L.shadow_rows) * kDqk * 2 > (size_t(64) << 20);
   if (L.shadow && prm.fmt == kFmtTokenFp8) prm.shadow_scale = shadow_scales(L.shadow, L.shadow_rows);
   prm.n_parts = 1;
   prm.part_blocks = (L.topk + kBlk - 1) / kBlk;
