@@ -1900,13 +1900,26 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     const int n_sample = runs * 128;
     uint32_t* sample = S.cand_key;  // cand_key and cand_idx, one after the other
     uint32_t lo = 0xFFFFFFFFu, hi = 0;
-    for (int e = tid; e < n_sample / 4; e += kSsThreads) {
-      const int run = e >> 5, u = e & 31;
-      const int start = static_cast<int>(static_cast<int64_t>(n - 128) * run / (runs - 1)) & ~3;
-      const uint4 v = *reinterpret_cast<const uint4*>(keys + start + 4 * u);
-      *reinterpret_cast<uint4*>(&sample[4 * e]) = v;
-      lo = min(min(lo, min(v.x, v.y)), min(v.z, v.w));
-      hi = max(max(hi, max(v.x, v.y)), max(v.z, v.w));
+    constexpr int kSp = kSsSampleMax / 4 / kSsThreads;  // 16-byte sample loads per thread, all issued first
+    uint4 sv[kSp];
+#pragma unroll
+    for (int j = 0; j < kSp; ++j) {
+      const int e = tid + j * kSsThreads;
+      if (e < n_sample / 4) {
+        const int run = e >> 5, u = e & 31;
+        const int start = static_cast<int>(static_cast<int64_t>(n - 128) * run / (runs - 1)) & ~3;
+        sv[j] = *reinterpret_cast<const uint4*>(keys + start + 4 * u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kSp; ++j) {
+      const int e = tid + j * kSsThreads;
+      if (e < n_sample / 4) {
+        const uint4 v = sv[j];
+        *reinterpret_cast<uint4*>(&sample[4 * e]) = v;
+        lo = min(min(lo, min(v.x, v.y)), min(v.z, v.w));
+        hi = max(max(hi, max(v.x, v.y)), max(v.z, v.w));
+      }
     }
     ss_minmax(S, lo, hi, tid);  // also orders the sample's stores before the histogram
     const float expect = static_cast<float>(k) * static_cast<float>(n_sample) / static_cast<float>(n);
@@ -1918,47 +1931,69 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
   }
   __syncthreads();  // the bitmap and count are cleared; the sample's space takes the candidates
-  // 2. every key >= t_lo to the staging space, in 128-key warp segments
+  // 2. every key >= t_lo to the staging space. A lane takes 16 keys per
+  //    iteration (four 16-byte loads, each coalesced over the warp) and the warp
+  //    appends its lanes' hits with one prefix sum and one shared atomic: about
+  //    k / n of the keys pass, so nearly every 128-key segment holds one, and
+  //    the append, not the load, sets the pass's instruction count
   uint32_t c_hi = 0;
   {
     constexpr int U = 4;
-    static_assert(U * kSsThreads * 4 == kSsPass, "one pass iteration");
-    for (int s0 = w * 128, it = 0; s0 < n; s0 += U * kSsThreads * 4, ++it) {
+    constexpr int kStride = kSsThreads * 4;  // keys between a lane's loads
+    static_assert(U * kStride == kSsPass, "one pass iteration");
+    for (int b0 = 0, it = 0; b0 < n; b0 += kSsPass, ++it) {
       prefetch_pass(it + kSsPrefetchAhead);
+      const int s0 = b0 + w * 128 + 4 * lane;  // load u covers keys s0 + u * kStride + 0..3
+      const bool full = b0 + kSsPass <= n;
       uint4 kv[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int e0 = s0 + u * kSsThreads * 4 + 4 * lane;
-        kv[u] = e0 < n ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
+        const int e0 = s0 + u * kStride;
+        kv[u] = (full || e0 < n) ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
       }
+      uint32_t take = 0;  // bit 4u + q: key s0 + u * kStride + q passes
+      if (full) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          take |= (kv[u].x >= t_lo ? 1u : 0u) << (4 * u);
+          take |= (kv[u].y >= t_lo ? 2u : 0u) << (4 * u);
+          take |= (kv[u].z >= t_lo ? 4u : 0u) << (4 * u);
+          take |= (kv[u].w >= t_lo ? 8u : 0u) << (4 * u);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e0 = s0 + u * kStride;
+          const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) take |= (e0 + q < n && kk[q] >= t_lo ? 1u : 0u) << (4 * u + q);
+        }
+      }
+      if (!__any_sync(0xFFFFFFFFu, take != 0)) continue;
+      const uint32_t c = __popc(take);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+        if (lane >= o2) incl += t2;
+      }
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(&S.n_cand, incl);
+      base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int e0 = s0 + u * kSsThreads * 4 + 4 * lane;
-        const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-        uint32_t take = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) take |= (e0 + q < n && kk[q] >= t_lo ? 1u : 0u) << q;
-        if (!__ballot_sync(0xFFFFFFFFu, take != 0)) continue;
-        const uint32_t c = __popc(take);
-        uint32_t incl = c;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
-          if (lane >= o2) incl += t2;
-        }
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&S.n_cand, incl);
-        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if ((take >> q) & 1u) {
-            c_hi = max(c_hi, kk[q]);
-            if (base < static_cast<uint32_t>(kSsCand)) {
-              S.cand_key[base] = kk[q];
-              S.cand_idx[base] = static_cast<uint32_t>(e0 + q);
-            }
-            ++base;
+        uint32_t t = (take >> (4 * u)) & 0xFu;
+        while (t) {
+          const int q = __ffs(t) - 1;
+          t &= t - 1;
+          const uint32_t key = q & 2 ? (q & 1 ? kv[u].w : kv[u].z) : (q & 1 ? kv[u].y : kv[u].x);
+          c_hi = max(c_hi, key);
+          if (base < static_cast<uint32_t>(kSsCand)) {
+            S.cand_key[base] = key;
+            S.cand_idx[base] = static_cast<uint32_t>(s0 + u * kStride + q);
           }
+          ++base;
+        }
       }
     }
   }
