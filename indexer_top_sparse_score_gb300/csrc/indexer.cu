@@ -1751,15 +1751,21 @@ constexpr int kSelBmBits = 1 << 18;
 //     reach, e being the number expected among the row's top k (one 4096-bin
 //     histogram of the sample's key range);
 //  2. one pass stages every key >= t_lo (and its position) in shared memory,
-//     one atomic per warp and 128 keys;
-//  3. when between k and kSsCand keys were staged, they hold the row's top-k:
-//     the k-th key follows from 12-bit digits over their key range, and among
-//     keys equal to it the lowest positions win (ranked by counting when few);
-//     otherwise (the sample misjudged the row) the exact radix selection runs
-//     over the whole row in global memory;
-//  4. the selected positions are marked in a bitmap of the row and written
-//     out in ascending order (rows longer than the bitmap: the k positions are
-//     collected in shared memory and sorted).
+//     one atomic per warp and 512 keys;
+//  3. when between k and kSsCand keys were staged, they hold the row's top-k.
+//     A 4096-bin histogram of the staged keys over [t_lo, the sample's largest
+//     key] (larger keys in the top bin) gives the bin of the k-th staged key;
+//     when that bin holds
+//     at most 32 keys (nearly always: ~1.4 k keys over 4096 bins), one warp
+//     ranks them by (key descending, position ascending) and the entry of the
+//     needed rank is the threshold. Otherwise the k-th key follows from 12-bit
+//     digits over the staged keys' range, and among keys equal to it the
+//     lowest positions win (ranked by counting when few). When fewer than k or
+//     more than kSsCand keys were staged (the sample misjudged the row) the
+//     exact radix selection runs over the whole row in global memory;
+//  4. the selected positions are marked in a bitmap of the row, gathered in
+//     ascending order in shared memory and written out coalesced (rows longer
+//     than the bitmap: the k positions are collected and sorted).
 // 512 threads and ~96 KB of shared memory: two rows per SM at a time, so one
 // row's pass over HBM overlaps the other's selection.
 constexpr int kSsThreads = 512;
@@ -1778,10 +1784,13 @@ struct SsSmem {
   uint32_t hist[kSsBins];        // digit histogram; tie list; dense_select's 3 x 256 words
   uint32_t red[2 * kSsWarps];
   uint32_t wsum[kSsWarps];
-  uint32_t n_cand, bin, above, thr_idx, n_sel;
+  uint32_t lst_key[32], lst_idx[32];  // the staged keys of the k-th key's bin
+  uint32_t n_cand, bin, above, thr_key, thr_idx, n_sel, n_lst;
 };
 
 // Block-wide minimum and maximum of v over all threads (every thread gets them).
+// Also a barrier for what each thread wrote before it; S.red is read after
+// it, so the next writer of S.red must follow another barrier.
 __device__ __forceinline__ void ss_minmax(SsSmem& S, uint32_t& lo, uint32_t& hi, int tid) {
   const int lane = tid & 31, w = tid >> 5;
   lo = __reduce_min_sync(0xFFFFFFFFu, lo);
@@ -1798,22 +1807,12 @@ __device__ __forceinline__ void ss_minmax(SsSmem& S, uint32_t& lo, uint32_t& hi,
     lo = min(lo, S.red[i]);
     hi = max(hi, S.red[kSsWarps + i]);
   }
-  __syncthreads();  // red is reused
 }
 
-// Histogram of (key - lo) >> shift over kSsBins bins for the keys in [lo, hi]
-// of keys[0, n) (shared memory), then the top-down scan: the bin holding the
-// r-th largest and the number of keys in higher bins (S.bin, S.above).
-__device__ __forceinline__ void ss_digit(SsSmem& S, const uint32_t* keys, int n, uint32_t lo, uint32_t hi,
-                                         int shift, uint32_t r, int tid) {
+// The top-down scan of the counted histogram S.hist: the bin holding the r-th
+// largest key and the number of keys in higher bins (S.bin, S.above).
+__device__ __forceinline__ void ss_scan(SsSmem& S, uint32_t r, int tid) {
   const int lane = tid & 31, w = tid >> 5;
-  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;
-  __syncthreads();
-  for (int e = tid; e < n; e += kSsThreads) {
-    const uint32_t v = keys[e];
-    if (v >= lo && v <= hi) atomicAdd(&S.hist[(v - lo) >> shift], 1u);
-  }
-  __syncthreads();
   constexpr int kPer = kSsBins / kSsThreads;  // bins per thread, from the top
   uint32_t c[kPer], sum = 0;
 #pragma unroll
@@ -1843,6 +1842,20 @@ __device__ __forceinline__ void ss_digit(SsSmem& S, const uint32_t* keys, int n,
     }
   }
   __syncthreads();
+}
+
+// Histogram of (key - lo) >> shift over kSsBins bins for the keys in [lo, hi]
+// of keys[0, n) (shared memory), then ss_scan.
+__device__ __forceinline__ void ss_digit(SsSmem& S, const uint32_t* keys, int n, uint32_t lo, uint32_t hi,
+                                         int shift, uint32_t r, int tid) {
+  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;
+  __syncthreads();
+  for (int e = tid; e < n; e += kSsThreads) {
+    const uint32_t v = keys[e];
+    if (v >= lo && v <= hi) atomicAdd(&S.hist[(v - lo) >> shift], 1u);
+  }
+  __syncthreads();
+  ss_scan(S, r, tid);
 }
 
 __device__ __forceinline__ int ss_shift(uint32_t lo, uint32_t hi) {
@@ -1888,13 +1901,16 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   const bool use_bm = n <= kSelBmBits;  // else the selected positions are sorted in shared memory
   const int nw = (n + 31) / 32;
   if (use_bm)
-    for (int b = tid; b < nw; b += kSsThreads) S.bm[b] = 0;
+    for (int b = tid; b < ((nw + 3) & ~3); b += kSsThreads) S.bm[b] = 0;
   if (tid == 0) {
     S.n_cand = 0;
     S.n_sel = 0;
+    S.n_lst = 0;
   }
-  // 1. a key that about 1.25 k + 4 sqrt(k) keys reach, from the sample
+  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;  // the sample's count
+  // 1. a key that about 1.1 e + 3 sqrt(e) + 3 of the sampled keys reach
   uint32_t t_lo = 0;
+  int h_shift = -1;  // >= 0: the pass counts the staged keys in bins of 2^h_shift from t_lo
   if (n > kSsCand) {
     const int runs = min(kSsMaxRuns, max(kSsMinRuns, n / 2048));
     const int n_sample = runs * 128;
@@ -1921,16 +1937,21 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
         hi = max(max(hi, max(v.x, v.y)), max(v.z, v.w));
       }
     }
-    ss_minmax(S, lo, hi, tid);  // also orders the sample's stores before the histogram
+    ss_minmax(S, lo, hi, tid);  // also orders the sample's stores and the cleared bins before the count
     const float expect = static_cast<float>(k) * static_cast<float>(n_sample) / static_cast<float>(n);
     const int r = static_cast<int>(ceilf(1.1f * expect + 3.0f * sqrtf(expect) + 3.0f));
     if (r < n_sample) {
       const int shift = ss_shift(lo, hi);
-      ss_digit(S, sample, n_sample, lo, hi, shift, static_cast<uint32_t>(r), tid);
+      for (int e = tid; e < n_sample; e += kSsThreads) atomicAdd(&S.hist[(sample[e] - lo) >> shift], 1u);
+      __syncthreads();
+      ss_scan(S, static_cast<uint32_t>(r), tid);
       t_lo = lo + (S.bin << shift);  // the r-th largest sampled key's bin, from its lower edge
+      h_shift = ss_shift(t_lo, hi);
+      // cleared for the staged keys' count (the scan read the bins before its last barrier)
+      for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;
     }
   }
-  __syncthreads();  // the bitmap and count are cleared; the sample's space takes the candidates
+  __syncthreads();  // the bitmap, bins and counts are cleared; the sample's space takes the candidates
   // 2. every key >= t_lo to the staging space. A lane takes 16 keys per
   //    iteration (four 16-byte loads, each coalesced over the warp) and the warp
   //    appends its lanes' hits with one prefix sum and one shared atomic: about
@@ -1998,14 +2019,59 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
   }
   uint32_t c_lo = t_lo;
-  ss_minmax(S, c_lo, c_hi, tid);  // every thread's stores and count precede what follows
+  ss_minmax(S, c_lo, c_hi, tid);  // every thread's stores and appends precede what follows
   const int nc = static_cast<int>(S.n_cand);
   uint32_t tk = 0, ti = 0xFFFFFFFFu;
   bool exact_row = true;  // false: selected over the staged keys
   if (nc >= k && nc <= kSsCand) {
     exact_row = false;
-    if (nc > k) {
-      // 3. the k-th key: 12-bit digits over the staged keys' range
+    bool found = nc == k;  // all staged keys
+    if (!found && h_shift >= 0) {
+      // 3. the k-th staged key's bin: the staged keys counted in bins of
+      //    2^h_shift from t_lo (larger keys than the sample's in the top bin)
+      auto bin_of = [&](uint32_t key) { return min((key - t_lo) >> h_shift, static_cast<uint32_t>(kSsBins - 1)); };
+      for (int e = tid; e < nc; e += kSsThreads) atomicAdd(&S.hist[bin_of(S.cand_key[e])], 1u);
+      __syncthreads();
+      ss_scan(S, static_cast<uint32_t>(k), tid);
+      const uint32_t b = S.bin;
+      const uint32_t r = static_cast<uint32_t>(k) - S.above;  // entries needed from bin b, 1..m
+      const uint32_t m = S.hist[b];
+      if (m <= 32u) {
+        // the bin's m entries to a list; lane j of warp 0 ranks entry j by
+        // (key descending, position ascending): rank r - 1 is the threshold
+        for (int e = tid; e < nc; e += kSsThreads) {
+          const uint32_t key = S.cand_key[e];
+          if (bin_of(key) == b) {
+            const uint32_t at = atomicAdd(&S.n_lst, 1u);
+            if (at < 32u) {
+              S.lst_key[at] = key;
+              S.lst_idx[at] = S.cand_idx[e];
+            }
+          }
+        }
+        __syncthreads();
+        if (w == 0 && static_cast<uint32_t>(lane) < m) {
+          const uint32_t mk = S.lst_key[lane], mi = S.lst_idx[lane];
+          uint32_t rank = 0;
+          for (uint32_t j = 0; j < m; ++j) {
+            const uint32_t kj = S.lst_key[j], ij = S.lst_idx[j];
+            rank += (kj > mk || (kj == mk && ij < mi)) ? 1u : 0u;
+          }
+          if (rank == r - 1u) {
+            S.thr_key = mk;
+            S.thr_idx = mi;
+          }
+        }
+        __syncthreads();
+        tk = S.thr_key;
+        ti = S.thr_idx;
+        found = true;
+      } else {
+        __syncthreads();  // the bins are read before the digits below clear them
+      }
+    }
+    if (!found) {
+      // 3'. the k-th key: 12-bit digits over the staged keys' range
       uint32_t lo = t_lo, hi = c_hi, r = static_cast<uint32_t>(k), m = 0;
       while (true) {
         const int shift = ss_shift(lo, hi);
@@ -2038,6 +2104,7 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
           __syncthreads();
           ti = S.thr_idx;
         } else {
+          __syncthreads();  // S.red (read by ss_minmax) is rewritten by the selection
           dense_select<kSsThreads>(S.cand_key, S.cand_idx, nc, k, tid, S.hist, S.red, sync, tk, ti);
         }
       }
@@ -2055,7 +2122,8 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
   }
   if (exact_row) {
-    // 3'. the whole row from global memory; bitmap word = 8 lanes x 4 keys
+    // 3''. the whole row from global memory; bitmap word = 8 lanes x 4 keys
+    __syncthreads();  // S.red (read by ss_minmax) is rewritten by the selection
     dense_select<kSsThreads>(keys, nullptr, n, k, tid, S.hist, S.red, sync, tk, ti);
     __syncthreads();  // the selection's scratch (S.hist) is free
     for (int s0 = w * 128; s0 < n; s0 += kSsThreads * 4) {
@@ -2121,11 +2189,18 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
     return;
   }
-  // 4. ascending positions: thread t owns a run of bitmap words
-  const int per = (nw + kSsThreads - 1) / kSsThreads;
-  const int w0 = tid * per, w1 = min(nw, w0 + per);
+  // 4. ascending positions: thread t owns a run of bitmap words and places its
+  //    positions in shared memory (the candidate space, free now), from where
+  //    the row's k entries are written out coalesced
+  //    (runs of a multiple of 4 words, read 16 bytes at a time; the bitmap's
+  //    words past nw are zero: cleared up to a multiple of 4 words)
+  const int per = ((nw + kSsThreads - 1) / kSsThreads + 3) & ~3;
+  const int w0 = tid * per, w1 = min((nw + 3) & ~3, w0 + per);
   uint32_t cnt = 0;
-  for (int i = w0; i < w1; ++i) cnt += __popc(S.bm[i]);
+  for (int i = w0; i < w1; i += 4) {
+    const uint4 b4 = *reinterpret_cast<const uint4*>(&S.bm[i]);
+    cnt += __popc(b4.x) + __popc(b4.y) + __popc(b4.z) + __popc(b4.w);
+  }
   uint32_t incl = cnt;
 #pragma unroll
   for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -2134,19 +2209,35 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   }
   if (lane == 31) S.wsum[w] = incl;
   __syncthreads();
-  uint32_t at = incl - cnt;
-  for (int w2 = 0; w2 < w; ++w2) at += S.wsum[w2];
-  for (int i = w0; i < w1; ++i) {
-    uint32_t bits = S.bm[i];
-    while (bits) {
-      const int e = i * 32 + __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (at < static_cast<uint32_t>(k)) {
-        o[at] = e;
-        if (os) os[at] = key_score(keys[e]);
+  uint32_t at = incl - cnt, total = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < kSsWarps; ++w2) {
+    const uint32_t v = S.wsum[w2];
+    if (w2 < w) at += v;
+    total += v;
+  }
+  uint32_t* out_pos = S.cand_key;
+  static_assert(kSsCand >= 2048, "the candidate space holds the k <= 2048 positions");
+  for (int i = w0; i < w1; i += 4) {
+    const uint4 b4 = *reinterpret_cast<const uint4*>(&S.bm[i]);
+    const uint32_t wb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t bits = wb[j];
+      while (bits) {
+        const uint32_t e = static_cast<uint32_t>(i + j) * 32u + static_cast<uint32_t>(__ffs(bits) - 1);
+        bits &= bits - 1;
+        if (at < static_cast<uint32_t>(k)) out_pos[at] = e;
+        ++at;
       }
-      ++at;
     }
+  }
+  __syncthreads();
+  for (int e = tid; e < k; e += kSsThreads) {
+    const bool has = static_cast<uint32_t>(e) < total;
+    const uint32_t v = has ? out_pos[e] : 0u;
+    o[e] = has ? static_cast<int32_t>(v) : -1;
+    if (os) os[e] = has ? key_score(keys[v]) : 0.0f;
   }
 }
 
