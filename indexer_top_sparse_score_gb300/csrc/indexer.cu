@@ -1900,24 +1900,15 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   for (int it = 0; it < kSsPrefetchAhead; ++it) prefetch_pass(it);
   const bool use_bm = n <= kSelBmBits;  // else the selected positions are sorted in shared memory
   const int nw = (n + 31) / 32;
-  if (use_bm)
-    for (int b = tid; b < ((nw + 3) & ~3); b += kSsThreads) S.bm[b] = 0;
-  if (tid == 0) {
-    S.n_cand = 0;
-    S.n_sel = 0;
-    S.n_lst = 0;
-  }
-  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;  // the sample's count
-  // 1. a key that about 1.1 e + 3 sqrt(e) + 3 of the sampled keys reach
-  uint32_t t_lo = 0;
-  int h_shift = -1;  // >= 0: the pass counts the staged keys in bins of 2^h_shift from t_lo
-  if (n > kSsCand) {
-    const int runs = min(kSsMaxRuns, max(kSsMinRuns, n / 2048));
-    const int n_sample = runs * 128;
-    uint32_t* sample = S.cand_key;  // cand_key and cand_idx, one after the other
-    uint32_t lo = 0xFFFFFFFFu, hi = 0;
-    constexpr int kSp = kSsSampleMax / 4 / kSsThreads;  // 16-byte sample loads per thread, all issued first
-    uint4 sv[kSp];
+  // 1. a key that about 1.1 e + 3 sqrt(e) + 3 of the sampled keys reach; the
+  //    sample's loads are issued first, the shared state is cleared while they
+  //    are in flight
+  const bool sampled = n > kSsCand;
+  const int runs = min(kSsMaxRuns, max(kSsMinRuns, n / 2048));
+  const int n_sample = runs * 128;
+  constexpr int kSp = kSsSampleMax / 4 / kSsThreads;  // 16-byte sample loads per thread
+  uint4 sv[kSp];
+  if (sampled) {
 #pragma unroll
     for (int j = 0; j < kSp; ++j) {
       const int e = tid + j * kSsThreads;
@@ -1927,6 +1918,20 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
         sv[j] = *reinterpret_cast<const uint4*>(keys + start + 4 * u);
       }
     }
+  }
+  if (use_bm)
+    for (int b = tid; b < ((nw + 3) & ~3); b += kSsThreads) S.bm[b] = 0;
+  if (tid == 0) {
+    S.n_cand = 0;
+    S.n_sel = 0;
+    S.n_lst = 0;
+  }
+  for (int b = tid; b < kSsBins; b += kSsThreads) S.hist[b] = 0;  // the sample's count
+  uint32_t t_lo = 0;
+  int h_shift = -1;  // >= 0: the staged keys are counted in bins of 2^h_shift from t_lo
+  if (sampled) {
+    uint32_t* sample = S.cand_key;  // cand_key and cand_idx, one after the other
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
 #pragma unroll
     for (int j = 0; j < kSp; ++j) {
       const int e = tid + j * kSsThreads;
@@ -1957,7 +1962,6 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   //    appends its lanes' hits with one prefix sum and one shared atomic: about
   //    k / n of the keys pass, so nearly every 128-key segment holds one, and
   //    the append, not the load, sets the pass's instruction count
-  uint32_t c_hi = 0;
   {
     constexpr int U = 4;
     constexpr int kStride = kSsThreads * 4;  // keys between a lane's loads
@@ -2008,7 +2012,6 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
           const int q = __ffs(t) - 1;
           t &= t - 1;
           const uint32_t key = q & 2 ? (q & 1 ? kv[u].w : kv[u].z) : (q & 1 ? kv[u].y : kv[u].x);
-          c_hi = max(c_hi, key);
           if (base < static_cast<uint32_t>(kSsCand)) {
             S.cand_key[base] = key;
             S.cand_idx[base] = static_cast<uint32_t>(s0 + u * kStride + q);
@@ -2018,8 +2021,7 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
       }
     }
   }
-  uint32_t c_lo = t_lo;
-  ss_minmax(S, c_lo, c_hi, tid);  // every thread's stores and appends precede what follows
+  __syncthreads();  // every thread's stores and appends precede what follows
   const int nc = static_cast<int>(S.n_cand);
   uint32_t tk = 0, ti = 0xFFFFFFFFu;
   bool exact_row = true;  // false: selected over the staged keys
@@ -2072,6 +2074,9 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
     if (!found) {
       // 3'. the k-th key: 12-bit digits over the staged keys' range
+      uint32_t c_lo = t_lo, c_hi = 0;
+      for (int e = tid; e < nc; e += kSsThreads) c_hi = max(c_hi, S.cand_key[e]);
+      ss_minmax(S, c_lo, c_hi, tid);
       uint32_t lo = t_lo, hi = c_hi, r = static_cast<uint32_t>(k), m = 0;
       while (true) {
         const int shift = ss_shift(lo, hi);
@@ -2192,13 +2197,19 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   // 4. ascending positions: thread t owns a run of bitmap words and places its
   //    positions in shared memory (the candidate space, free now), from where
   //    the row's k entries are written out coalesced
-  //    (runs of a multiple of 4 words, read 16 bytes at a time; the bitmap's
-  //    words past nw are zero: cleared up to a multiple of 4 words)
-  const int per = ((nw + kSsThreads - 1) / kSsThreads + 3) & ~3;
-  const int w0 = tid * per, w1 = min((nw + 3) & ~3, w0 + per);
+  //    (runs of 4 words or more are a multiple of 4 words, read 16 bytes at a
+  //    time; the bitmap's words past nw are zero: cleared up to a multiple of 4)
+  const int per1 = (nw + kSsThreads - 1) / kSsThreads;
+  const bool vec = per1 >= 4;
+  const int step = vec ? 4 : 1;
+  const int per = vec ? (per1 + 3) & ~3 : per1;
+  const int w0 = tid * per, w1 = min(vec ? (nw + 3) & ~3 : nw, w0 + per);
+  auto words = [&](int i) {
+    return vec ? *reinterpret_cast<const uint4*>(&S.bm[i]) : make_uint4(S.bm[i], 0u, 0u, 0u);
+  };
   uint32_t cnt = 0;
-  for (int i = w0; i < w1; i += 4) {
-    const uint4 b4 = *reinterpret_cast<const uint4*>(&S.bm[i]);
+  for (int i = w0; i < w1; i += step) {
+    const uint4 b4 = words(i);
     cnt += __popc(b4.x) + __popc(b4.y) + __popc(b4.z) + __popc(b4.w);
   }
   uint32_t incl = cnt;
@@ -2218,8 +2229,8 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   }
   uint32_t* out_pos = S.cand_key;
   static_assert(kSsCand >= 2048, "the candidate space holds the k <= 2048 positions");
-  for (int i = w0; i < w1; i += 4) {
-    const uint4 b4 = *reinterpret_cast<const uint4*>(&S.bm[i]);
+  for (int i = w0; i < w1; i += step) {
+    const uint4 b4 = words(i);
     const uint32_t wb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
