@@ -1751,7 +1751,7 @@ constexpr int kSelBmBits = 1 << 18;
 //     reach, e being the number expected among the row's top k (one 4096-bin
 //     histogram of the sample's key range);
 //  2. one pass stages every key >= t_lo (and its position) in shared memory,
-//     one atomic per warp and 512 keys;
+//     one atomic per warp and 1024 keys;
 //  3. when between k and kSsCand keys were staged, they hold the row's top-k.
 //     A 4096-bin histogram of the staged keys over [t_lo, the sample's largest
 //     key] (larger keys in the top bin) gives the bin of the k-th staged key;
@@ -1774,7 +1774,7 @@ constexpr int kSsCand = 6144;       // staged candidates
 constexpr int kSsMinRuns = 32, kSsMaxRuns = 96;  // sampled runs of 128 keys
 constexpr int kSsSampleMax = kSsMaxRuns * 128;   // held in the two candidate arrays
 constexpr int kSsBins = 4096;       // 12-bit digits
-constexpr int kSsPass = 4 * kSsThreads * 4;  // keys per iteration of the staging pass
+constexpr int kSsPass = 8 * kSsThreads * 4;  // keys per iteration of the staging pass
 constexpr int kSsPrefetchAhead = 2;          // iterations of the row prefetched into L2 ahead of the pass
 static_assert(kSsSampleMax <= 2 * kSsCand, "the sample is held in the candidate space");
 
@@ -1887,7 +1887,7 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
   auto sync = []() { __syncthreads(); };
   // the staging pass reads the whole row once: its next iterations are
   // prefetched into L2 ahead of it (one bulk prefetch per iteration), the first
-  // ones while the sample is taken
+  // ones while the sample is processed
   const uint32_t row_bytes = static_cast<uint32_t>(n) * 4u;
   auto prefetch_pass = [&](int it) {
     const uint32_t off = static_cast<uint32_t>(it) * kSsPass * 4u;
@@ -1896,8 +1896,6 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
       prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(keys) + off, len);
     }
   };
-#pragma unroll
-  for (int it = 0; it < kSsPrefetchAhead; ++it) prefetch_pass(it);
   const bool use_bm = n <= kSelBmBits;  // else the selected positions are sorted in shared memory
   const int nw = (n + 31) / 32;
   // 1. a key that about 1.1 e + 3 sqrt(e) + 3 of the sampled keys reach; the
@@ -1919,6 +1917,9 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
       }
     }
   }
+  // the pass's first iterations, behind the sample's loads
+#pragma unroll
+  for (int it = 0; it < kSsPrefetchAhead; ++it) prefetch_pass(it);
   if (use_bm)
     for (int b = tid; b < ((nw + 3) & ~3); b += kSsThreads) S.bm[b] = 0;
   if (tid == 0) {
@@ -1957,13 +1958,13 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
     }
   }
   __syncthreads();  // the bitmap, bins and counts are cleared; the sample's space takes the candidates
-  // 2. every key >= t_lo to the staging space. A lane takes 16 keys per
-  //    iteration (four 16-byte loads, each coalesced over the warp) and the warp
-  //    appends its lanes' hits with one prefix sum and one shared atomic: about
-  //    k / n of the keys pass, so nearly every 128-key segment holds one, and
-  //    the append, not the load, sets the pass's instruction count
+  // 2. every key >= t_lo to the staging space. A lane takes 32 keys per
+  //    iteration (eight 16-byte loads, each coalesced over the warp) and the
+  //    warp appends its lanes' hits with one prefix sum and one shared atomic:
+  //    about k / n of the keys pass, so nearly every 128-key segment holds one,
+  //    and a per-segment append would set the pass's instruction count
   {
-    constexpr int U = 4;
+    constexpr int U = 8;
     constexpr int kStride = kSsThreads * 4;  // keys between a lane's loads
     static_assert(U * kStride == kSsPass, "one pass iteration");
     for (int b0 = 0, it = 0; b0 < n; b0 += kSsPass, ++it) {
@@ -1977,6 +1978,7 @@ __global__ void __launch_bounds__(kSsThreads, 2) select_sampled_kernel(const Sel
         kv[u] = (full || e0 < n) ? *reinterpret_cast<const uint4*>(keys + e0) : make_uint4(0, 0, 0, 0);
       }
       uint32_t take = 0;  // bit 4u + q: key s0 + u * kStride + q passes
+      static_assert(4 * U <= 32, "one bit per key of the iteration");
       if (full) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {

@@ -313,6 +313,45 @@ def test_indexer_rows_beyond_the_bitmap(keys):
         assert np.array_equal(gs[rows[r]], full[g[rows[r]]])
 
 
+@pytest.mark.parametrize("case", ["k1", "k7", "k100", "tie_groups"])
+def test_indexer_selection_small_k_and_tie_groups(case):
+    """Score-array rows of 17,001-17,700 keys through the sampled selection.
+    With k = 1 or 7 the k-th key lies above the sample's largest key, in the
+    top bin of the staged keys' histogram (where every larger key is counted);
+    with k = 100 a few bins below it. tie_groups copies 3,000 key rows to 8
+    other positions each (groups of 9 keys with equal scores in every row), so
+    the bin of the k-th key often holds equal keys and the lowest positions
+    must win inside it. Index sets and returned scores exact."""
+    topk = {"k1": 1, "k7": 7, "k100": 100, "tie_groups": 2048}[case]
+    spec = wl.scaled(wl.SPECS["prefill16k"], n_tokens=700, prefix_len=17000, shuffled=True, topk=topk)
+    prob = wl.make(spec, "cpu")
+    if case == "tie_groups":
+        g = torch.Generator().manual_seed(41)
+        kr = prob.cache.k_idx.view(-1, spec.d_idx)
+        ks = prob.cache.k_idx_scale.view(-1) if prob.cache.k_idx_scale is not None else None
+        n = kr.shape[0]
+        for s in torch.randint(0, n, (3000,), generator=g).tolist():
+            dst = torch.randint(0, n, (8,), generator=g)
+            kr[dst] = kr[s].clone()
+            if ks is not None:
+                ks[dst] = ks[s].clone()
+    dev = prob.to("cuda")
+    L = spec.prefix_len + spec.n_tokens
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    gidx, gsc, ws = smla.indexer_topk(dev.cache, dev.page_table, seq_lens, L, spec.n_tokens, dev.q_idx, dev.w,
+                                      topk, want_scores=True)
+    assert smla.read_status(ws)[0] == 0
+    g_idx, g_sc = _host(gidx), _host(gsc)
+    assert (np.diff(g_idx, axis=1) > 0).all(), "indices not ascending"
+    rows = np.arange(0, spec.n_tokens, 7)
+    o = oracle.Oracle(prob)
+    ridx, *_ = o.rows(rows, attend=False)
+    compare_idx(g_idx[rows], ridx)
+    for r in rows:
+        full = o.scores(int(r))
+        assert np.array_equal(g_sc[r], full[g_idx[r]])
+
+
 def test_decode_rows_beyond_the_bitmap():
     """Decode sequences of 270K-300K keys (split mode, the selection's sorted
     output): every row's index set and the attention match the oracle."""
