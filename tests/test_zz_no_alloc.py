@@ -75,6 +75,8 @@ CASES = {
     "bf16-no-shadow": ("prefill16k", 1900, 14000, "bf16"),
     # FP8 cache with per-token scales
     "fp8": ("prefill16k", 2000, 5000, "fp8"),
+    # 656-byte tile-scaled FP8 rows (512 e4m3 values, a scale per 128, 64 bf16 rope values)
+    "fp8_ds_mla": ("prefill16k", 1200, 2500, wl.FP8_DS_MLA),
 }
 
 
