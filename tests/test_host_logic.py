@@ -54,6 +54,31 @@ def test_bench_stage_counts_match_the_workload_sizing():
     assert round(cnt["idx_flops"] / 1e12, 2) == 1.10 and round(cnt["mla_flops"] / 1e12, 2) == 4.38
 
 
+def test_bench_launch_count_matches_the_measured_launch_lists(monkeypatch):
+    """The bench's `gpu_launches` comes from PrefillStep.launches(), which
+    mirrors the library's score-array block rule. On a 152-SM GB300 it must give
+    the launch counts of the committed ncu launch lists: 62 per 131,072-token
+    step (16 indexers, 14 selections, 16 f16 copies, 16 attentions), 8 for the
+    1M-token prefix (three row blocks: 3 indexers, 3 selections, the copy, the
+    attention) and 3 for the 16K prefill (rows within the dense mode)."""
+    import types
+
+    import torch
+    sys.argv = ["bench.py"]
+    import bench
+    from indexer_top_sparse_score_gb300 import workloads as wl
+    monkeypatch.setattr(torch.cuda, "get_device_properties", lambda i: types.SimpleNamespace(multi_processor_count=152))
+
+    def launches(spec):
+        step = object.__new__(bench.PrefillStep)  # no device buffers: only the schedule is read
+        step.spec, step.chunks = spec, bench.chunk_list(spec)
+        return step.launches()
+
+    assert launches(wl.SPECS["prefill128k"]) == 62
+    assert launches(wl.SPECS["prefix1m"]) == 8
+    assert launches(wl.SPECS["prefill16k"]) == 3
+
+
 def test_output_checker_catches_one_wrong_head_and_one_wrong_lse():
     """The GPU parity checker (per-(row, head) bound on top of the aggregate bar):
     outputs rounded like the kernel's pass; one (row, head) among 128 x 64 that is
